@@ -1,0 +1,270 @@
+/*
+ * Oracle for the delayed (single-pass) mHC seam -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, single-threaded CPU restatement of what the seam computes, in
+ * double precision, with a rounding step exactly where a stored format asks for
+ * one.  Only the test-suite, the smoke check and the benchmark's CPU-baseline
+ * leg load this library; the product path (the CUDA library) never does, and
+ * the two share no code, header or table.
+ *
+ * Sources (three pull-request pages on the subject):
+ *  - "[FlyDSL] Single-launch Mega-mHC on gfx950", Motivation and Kernel
+ *    Architecture: the step order post-mix -> collapse (input mix with the
+ *    carried pre) -> sum of squares + gate projection -> split-K reduce -> rstd
+ *    -> Sinkhorn -> layer input, then the bf16 norm and, optionally, the per-32
+ *    ue8m0 FP8 quantisation of it.
+ *  - The seam's defining formula: R' = comb . R + post (x) Y; 24 logits from
+ *    the 4H-long projection R'_flat . fn scaled by the RMS of R'; pre = sigmoid,
+ *    post = 2 sigmoid, comb = Sinkhorn20(exp(.)) of a 4x4 block; x = sum_i
+ *    pre_carried[i] R'[i]; norm = RMSNorm(x) * gamma in bf16.
+ *  - "[Triton/Gluon] [gfx950] [dsv4.1-flash] mHC fused kernel": the unfused
+ *    pipeline (post kernel, pre GEMM + sum of squares, gate finish, head
+ *    reduce, RMSNorm + quant) whose stages the fused seam replaces.
+ *
+ * Readings where the pages are silent (each is also listed in the design
+ * notes): logit order [pre 0..3 | post 4..7 | comb 8..23 row-major]; alpha[0]
+ * scales pre, alpha[1] post, alpha[2] comb; comb row i mixes into output
+ * stream i; one eps inside both square roots; Sinkhorn = 20 rounds of (row
+ * normalise, column normalise) on exp(logits), no max subtraction; pre/post
+ * use the plain logistic; x uses the CARRIED pre; the stored bf16 R' (not the
+ * unrounded one) feeds the sums, the projection and x; x is not rounded before
+ * the norm; ue8m0 exponent = smallest e with amax <= 448 * 2^e, amax floored
+ * at amax_floor (1e-10 by default), clamped to [-127, 127]; e4m3fn codes by
+ * round-to-nearest-even, saturating at +-448, sign of zero kept.
+ *
+ * Parity pins: every function here is checked by the CPU test-suite against
+ * closed forms, invariants, an exhaustive quantiser sweep and a
+ * high-precision brute force at T=1, H=8.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define N_HC 4
+#define N_LOG 24
+
+/* ---------------------------------------------------------------- bf16 ---- */
+
+/* bf16 = 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits: the top half
+ * of an IEEE binary32. */
+double mhc_oracle_bf16_to_double(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Round a double to the nearest bf16, ties to even, in one step.
+ * Normal bf16 numbers carry 8 significant bits, so the spacing of the grid
+ * around |v| in [2^E, 2^(E+1)) is 2^(E-7); below 2^-126 the grid is the
+ * subnormal spacing 2^-133.  v / spacing is exact in double (a power-of-two
+ * scale), rint() rounds it half-to-even, and the product is the rounded value;
+ * anything at or beyond 2^128 after rounding is infinity. */
+uint16_t mhc_oracle_bf16_rne(double v) {
+    if (isnan(v)) return 0x7FC0;
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (a == 0.0) return sign;
+    if (isinf(a)) return sign | 0x7F80;
+    int e;
+    frexp(a, &e);               /* a = m * 2^e, m in [0.5, 1): leading bit 2^(e-1) */
+    int E = e - 1;
+    if (E < -126) E = -126;     /* subnormal range shares the 2^-126 spacing base */
+    double spacing = ldexp(1.0, E - 7);
+    double r = rint(a / spacing) * spacing;
+    if (r >= ldexp(1.0, 128)) return sign | 0x7F80;
+    float f = (float)r;         /* exact: r is on the bf16 grid */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return sign | (uint16_t)((u >> 16) & 0x7FFF);
+}
+
+/* ------------------------------------------------------------- e4m3fn ---- */
+
+/* OCP 8-bit floating point, E4M3 ("fn": no infinities, 0x7F/0xFF = NaN):
+ * exponent bias 7, 3 fraction bits, largest finite 448 (0x7E), smallest
+ * normal 2^-6, subnormals m * 2^-9 for m = 1..7.  Round to nearest even, and
+ * saturate finite values beyond 448 to +-448; the sign of zero is kept. */
+uint8_t mhc_oracle_e4m3_rne_satfinite(double v) {
+    if (isnan(v)) return 0x7F;
+    uint8_t sign = signbit(v) ? 0x80 : 0;
+    double a = fabs(v);
+    if (a >= 448.0) return sign | 0x7E;
+    double spacing;
+    if (a < ldexp(1.0, -6)) {
+        spacing = ldexp(1.0, -9);
+    } else {
+        int e;
+        frexp(a, &e);
+        spacing = ldexp(1.0, (e - 1) - 3);
+    }
+    double r = rint(a / spacing) * spacing;   /* r <= 448: 448 is on the grid */
+    if (r == 0.0) return sign;
+    if (r < ldexp(1.0, -6)) return sign | (uint8_t)(r / ldexp(1.0, -9));
+    int e;
+    double m = frexp(r, &e);                  /* r = m * 2^e, m in [0.5, 1) */
+    int E = e - 1;                            /* r = (2m) * 2^E, 2m in [1, 2) */
+    int frac = (int)((2.0 * m - 1.0) * 8.0);  /* exact: 3 fraction bits */
+    return sign | (uint8_t)(((E + 7) << 3) | frac);
+}
+
+/* ------------------------------------------------------------- ue8m0 ----- */
+
+/* Shared exponent of one 32-element group: the smallest integer e with
+ * amax <= 448 * 2^e (i.e. ceil(log2(amax / 448)) evaluated exactly), with amax
+ * first raised to amax_floor, then clamped to [-127, 127].  Every comparison
+ * is exact in double because 448 * 2^e is a power-of-two multiple of 448. */
+int mhc_oracle_ue8m0_exponent(double amax, double amax_floor) {
+    if (amax < amax_floor) amax = amax_floor;
+    int k;
+    frexp(amax, &k);
+    int e = k - 9;
+    while (ldexp(448.0, e) < amax) ++e;
+    while (ldexp(448.0, e - 1) >= amax) --e;
+    if (e < -127) e = -127;
+    if (e > 127) e = 127;
+    return e;
+}
+
+/* Quantise rows of bf16 values in groups of 32 contiguous elements.
+ * codes[r, h] = e4m3(x[r, h] * 2^-e_g); scales[r, g] = e_g + 127 (the e8m0
+ * byte).  Returns 0, or -1 when H is not a multiple of 32. */
+int mhc_oracle_quant_ue8m0(const uint16_t* x, int64_t rows, int H, double amax_floor,
+                           uint8_t* codes, uint8_t* scales) {
+    if (H % 32 != 0) return -1;
+    int G = H / 32;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int g = 0; g < G; ++g) {
+            const uint16_t* src = x + r * H + g * 32;
+            double amax = 0.0;
+            for (int j = 0; j < 32; ++j) {
+                double a = fabs(mhc_oracle_bf16_to_double(src[j]));
+                if (a > amax) amax = a;
+            }
+            int e = mhc_oracle_ue8m0_exponent(amax, amax_floor);
+            scales[r * G + g] = (uint8_t)(e + 127);
+            for (int j = 0; j < 32; ++j)
+                codes[r * H + g * 32 + j] =
+                    mhc_oracle_e4m3_rne_satfinite(ldexp(mhc_oracle_bf16_to_double(src[j]), -e));
+        }
+    }
+    return 0;
+}
+
+/* ----------------------------------------------------------- Sinkhorn ---- */
+
+/* n x n Sinkhorn normalisation of a positive matrix (row-major, in place):
+ * `iters` rounds of "divide every row by its sum, then every column by its
+ * sum".  After each round the columns sum to one; the rows converge to one. */
+void mhc_oracle_sinkhorn(int n, double* M, int iters) {
+    for (int it = 0; it < iters; ++it) {
+        for (int i = 0; i < n; ++i) {
+            double s = 0.0;
+            for (int j = 0; j < n; ++j) s += M[i * n + j];
+            for (int j = 0; j < n; ++j) M[i * n + j] /= s;
+        }
+        for (int j = 0; j < n; ++j) {
+            double s = 0.0;
+            for (int i = 0; i < n; ++i) s += M[i * n + j];
+            for (int i = 0; i < n; ++i) M[i * n + j] /= s;
+        }
+    }
+}
+
+double mhc_oracle_sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
+
+/* --------------------------------------------------------------- seam ---- */
+
+/* One seam call over T tokens (every token is independent).
+ *
+ * Layouts (row-major, contiguous): R, residual_out [T,4,H] bf16 bits; Y, norm
+ * [T,H] bf16 bits; post_prev, pre_prev [T,4], comb_prev [T,4,4] fp32; fn
+ * [4H,24] fp32 with row i*H + h for stream i, column h; bias [24], alpha [3]
+ * fp32; gamma [H] bf16 bits.  Y and post_prev are both NULL for the no_post
+ * form (R' = comb . R).  Outputs pre_out, post_out [T,4], comb_out [T,16] in
+ * double; rstd_out [T,2] = (rstd over 4H of R', rstd over H of x) and x_out
+ * [T,H] are optional.  rprime_unrounded = 1 feeds the unrounded R' (instead
+ * of the stored bf16 one) to the sums, the projection and x; it exists to
+ * measure how much that reading matters.
+ * Returns 0, or -1 on a NULL required pointer or a half-present post input. */
+int mhc_oracle_seam(int64_t T, int H,
+                    const uint16_t* R, const uint16_t* Y,
+                    const float* post_prev, const float* comb_prev, const float* pre_prev,
+                    const float* fn, const float* bias, const float* alpha, const uint16_t* gamma,
+                    double eps, int sinkhorn_iters, int rprime_unrounded,
+                    uint16_t* residual_out, uint16_t* norm,
+                    double* pre_out, double* post_out, double* comb_out,
+                    double* rstd_out, double* x_out) {
+    if ((Y == NULL) != (post_prev == NULL)) return -1;
+    if (!R || !comb_prev || !pre_prev || !fn || !bias || !alpha || !gamma) return -1;
+    if (!residual_out || !norm || !pre_out || !post_out || !comb_out) return -1;
+    const int K = N_HC * H;
+    double* rp = (double*)malloc(sizeof(double) * (size_t)K);
+    double* x = (double*)malloc(sizeof(double) * (size_t)H);
+    if (!rp || !x) { free(rp); free(x); return -1; }
+
+    for (int64_t t = 0; t < T; ++t) {
+        const uint16_t* Rt = R + t * K;
+        const float* comb = comb_prev + t * 16;
+        /* 1. post-mix: R'[i][h] = sum_j comb[i][j] R[j][h] + post[i] Y[h],
+         *    stored as bf16 (round to nearest even). */
+        for (int i = 0; i < N_HC; ++i) {
+            for (int h = 0; h < H; ++h) {
+                double v = 0.0;
+                for (int j = 0; j < N_HC; ++j)
+                    v += (double)comb[i * 4 + j] * mhc_oracle_bf16_to_double(Rt[j * H + h]);
+                if (Y) v += (double)post_prev[t * 4 + i] * mhc_oracle_bf16_to_double(Y[t * H + h]);
+                uint16_t b = mhc_oracle_bf16_rne(v);
+                residual_out[t * K + i * H + h] = b;
+                rp[i * H + h] = rprime_unrounded ? v : mhc_oracle_bf16_to_double(b);
+            }
+        }
+        /* 2. sum of squares and the 24-wide projection over K = 4H. */
+        double sR = 0.0, d[N_LOG];
+        for (int k = 0; k < N_LOG; ++k) d[k] = 0.0;
+        for (int r = 0; r < K; ++r) {
+            sR += rp[r] * rp[r];
+            for (int k = 0; k < N_LOG; ++k) d[k] += rp[r] * (double)fn[(size_t)r * N_LOG + k];
+        }
+        /* 3. rstd of R' over 4H, then the logits. */
+        double rstdR = 1.0 / sqrt(sR / (double)K + eps);
+        double l[N_LOG];
+        for (int k = 0; k < N_LOG; ++k) {
+            int g = k < 4 ? 0 : (k < 8 ? 1 : 2);
+            l[k] = (double)alpha[g] * rstdR * d[k] + (double)bias[k];
+        }
+        /* 4. gates for the next seam. */
+        for (int i = 0; i < 4; ++i) {
+            pre_out[t * 4 + i] = mhc_oracle_sigmoid(l[i]);
+            post_out[t * 4 + i] = 2.0 * mhc_oracle_sigmoid(l[4 + i]);
+        }
+        /* 5. comb = Sinkhorn(exp(l[8..23])) as a 4x4 row-major matrix. */
+        double M[16];
+        for (int q = 0; q < 16; ++q) M[q] = exp(l[8 + q]);
+        mhc_oracle_sinkhorn(4, M, sinkhorn_iters);
+        for (int q = 0; q < 16; ++q) comb_out[t * 16 + q] = M[q];
+        /* 6. layer input with the CARRIED pre, its RMS over H, and the norm. */
+        const float* pre = pre_prev + t * 4;
+        double sx = 0.0;
+        for (int h = 0; h < H; ++h) {
+            double v = 0.0;
+            for (int i = 0; i < N_HC; ++i) v += (double)pre[i] * rp[i * H + h];
+            x[h] = v;
+            sx += v * v;
+        }
+        double rstdx = 1.0 / sqrt(sx / (double)H + eps);
+        for (int h = 0; h < H; ++h) {
+            norm[t * H + h] = mhc_oracle_bf16_rne(x[h] * rstdx * mhc_oracle_bf16_to_double(gamma[h]));
+            if (x_out) x_out[t * H + h] = x[h];
+        }
+        if (rstd_out) {
+            rstd_out[t * 2 + 0] = rstdR;
+            rstd_out[t * 2 + 1] = rstdx;
+        }
+    }
+    free(rp);
+    free(x);
+    return 0;
+}
