@@ -1,0 +1,335 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 delayed mHC seam (one JSON line on rank 0).
+
+A step is one seam call over one batch of synthetic input: post-mix, gate
+projection with its split-K finish, gates, collapse, RMSNorm (and the ue8m0
+quantiser for mxfp8 workloads).  The default workload is the prefill post
+seam at T = 16384, H = 5120, bf16 out; ``value`` is the achieved HBM
+bandwidth in TB/s (algorithmic bytes, 20 H per token, over the device time of
+the step), ``ms_per_step`` the seam time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-e2e] [--no-cpu-baseline]
+
+Under torchrun every rank runs the full workload on its own GPU (the seam is
+per token, so ranks shard tokens with no exchange: weak scaling); rank 0
+prints the whole-job value.  ``--impl reference`` times the oracle (plain
+single-threaded C, fp64) on the host cores on a bounded token sample of the
+same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mhc_residual_seam_gb300 import accounting as ACC  # noqa: E402
+from mhc_residual_seam_gb300 import inputs as I  # noqa: E402
+
+METRIC = "mHC seam achieved HBM bandwidth (algorithmic bytes / seam time) at T=16384, H=5120"
+UNIT = "TB/s"
+
+WORKLOADS = {
+    "seam_T16384_H5120_post_bf16": dict(T=16384, H=5120, post=True, out="bf16", seed=1004),
+    "seam_T16384_H5120_nopost_bf16": dict(T=16384, H=5120, post=False, out="bf16", seed=1004),
+    "seam_T4160_H5120_post_bf16": dict(T=4160, H=5120, post=True, out="bf16", seed=1003),
+    "seam_T1024_H5120_post_mxfp8": dict(T=1024, H=5120, post=True, out="mxfp8", seed=1002),
+    "seam_T64_H5120_post_bf16": dict(T=64, H=5120, post=True, out="bf16", seed=1001),
+    "seam_T64_H5120_nopost_bf16": dict(T=64, H=5120, post=False, out="bf16", seed=1001),
+    "seam_T4_H5120_post_bf16": dict(T=4, H=5120, post=True, out="bf16", seed=1000),
+}
+DEFAULT = "seam_T16384_H5120_post_bf16"
+UNIQUE_TOKENS = 2048  # distinct tokens drawn; repeated along T (the device streams all T)
+L2_BYTES = 126 * 1024 * 1024
+
+# ncu DRAM bytes (read + write) per launch of the dominant kernel, keyed by the
+# hash of the CUDA sources they were captured with; a source change voids them.
+NCU_TRAFFIC = {}
+
+
+def src_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "mhc_residual_seam_gb300", "csrc", "*"))):
+        h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def carried_gates(pre_l, post_l, comb_l, iters: int = 20):
+    """Input preparation: carried gates in the form a previous seam emits them
+    (sigmoid, 2 sigmoid, Sinkhorn of exp) from the U(-1,1) draws, fp64 -> fp32."""
+    pre = torch.sigmoid(torch.from_numpy(pre_l))
+    post = 2.0 * torch.sigmoid(torch.from_numpy(post_l))
+    M = torch.exp(torch.from_numpy(comb_l))
+    for _ in range(iters):
+        M = M / M.sum(-1, keepdim=True)
+        M = M / M.sum(-2, keepdim=True)
+    return pre.float().contiguous(), post.float().contiguous(), M.float().contiguous()
+
+
+def make_workload(w: dict, device) -> dict:
+    d = I.seam_draws(w["T"], w["H"], w["seed"], post=w["post"], unique_tokens=UNIQUE_TOKENS)
+    pre, post, comb = carried_gates(d["pre_logits"], d["post_logits"], d["comb_logits"])
+    host = {"R": d["R"], "Y": d["Y"], "post_prev": post if w["post"] else None, "comb_prev": comb, "pre_prev": pre,
+            "fn": d["fn"], "bias": d["bias"], "alpha": d["alpha"], "gamma": d["gamma"]}
+    dev = {k: (None if v is None else v.to(device)) for k, v in host.items()}
+    return {"host": host, "dev": dev, "eps": d["eps"], "draws": d}
+
+
+# ------------------------------------------------------------------ clocks --
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
+        sel = []
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            sel = []
+        self.cmd = ["nvidia-smi", *sel, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(self.cmd, stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ our arm --
+def run_ours(args, w: dict, rank: int, world: int, local_rank: int) -> dict | None:
+    from mhc_residual_seam_gb300 import binding as B
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    B.lib()
+    wl = make_workload(w, device)
+    g, host = wl["dev"], wl["host"]
+    T, H = w["T"], w["H"]
+    mx = w["out"] == "mxfp8"
+    mode = B.MHC_OUT_MXFP8 if mx else B.MHC_OUT_BF16
+    out = B.alloc_outputs(T, H, mode, device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        B.mhc_seam(g["R"], g["Y"], g["post_prev"], g["comb_prev"], g["pre_prev"], g["fn"], None, g["bias"],
+                   g["alpha"], g["gamma"], wl["eps"], mode, out["residual_out"], out["norm"], out["fp8_codes"],
+                   out["e8m0_scales"], out["pre_out"], out["post_out"], out["comb_out"], out["workspace"],
+                   stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+    launches = B.mhc_last_launch_count()
+    B.mhc_check_status(out["workspace"])
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.2)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(device)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(device)
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    B.mhc_check_status(out["workspace"])
+
+    # end to end through the C ABI with host buffers: H2D inputs, seam, D2H outputs
+    e2e = None
+    if not args.no_e2e:
+        pin = {k: (None if v is None else v.pin_memory()) for k, v in host.items()
+               if k in ("R", "Y", "post_prev", "comb_prev", "pre_prev")}
+        outs = ["residual_out", "norm", "pre_out", "post_out", "comb_out"] + (["fp8_codes", "e8m0_scales"] if mx else [])
+        pout = {k: torch.empty(out[k].shape, dtype=out[k].dtype).pin_memory() for k in outs}
+        bi = sum(v.numel() * v.element_size() for v in pin.values() if v is not None)
+        bo = sum(v.numel() * v.element_size() for v in pout.values())
+
+        def e2e_step():
+            for k, v in pin.items():
+                if v is not None:
+                    g[k].copy_(v, non_blocking=True)
+            step()
+            for k in outs:
+                pout[k].copy_(out[k], non_blocking=True)
+
+        n_e2e = max(3, min(args.steps, 20))
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(device)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize(device)
+        e2e_ms = a0.elapsed_time(a1) / n_e2e
+        e2e = {"ms": e2e_ms, "h2d": bi, "d2h": bo}
+
+    ms_t = torch.tensor([ms, e2e["ms"] if e2e else 0.0], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(ms_t, op=torch.distributed.ReduceOp.MAX)
+    return {"ms": float(ms_t[0]), "e2e": e2e and dict(e2e, ms=float(ms_t[1])), "launches": launches,
+            "clocks": clocks, "wl": wl}
+
+
+def cpu_baseline(w: dict, wl: dict | None, budget_s: float = 15.0, steps: int = 1) -> dict:
+    """The oracle, as it stands, on a bounded token sample of the workload (one
+    host thread).  Returns the same metric on the sample."""
+    import oracle as O
+
+    d = wl["draws"] if wl else I.seam_draws(w["T"], w["H"], w["seed"], post=w["post"], unique_tokens=UNIQUE_TOKENS)
+    pre, post, comb = carried_gates(d["pre_logits"], d["post_logits"], d["comb_logits"])
+    t0 = time.perf_counter()
+    O.seam(d["R"][:1], d["Y"][:1] if w["post"] else None, post[:1] if w["post"] else None, comb[:1], pre[:1],
+           d["fn"], d["bias"], d["alpha"], d["gamma"], d["eps"])
+    per_tok = max(time.perf_counter() - t0, 1e-4)
+    n = int(max(1, min(w["T"], budget_s / per_tok)))
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        o = O.seam(d["R"][:n], d["Y"][:n] if w["post"] else None, post[:n] if w["post"] else None, comb[:n],
+                   pre[:n], d["fn"], d["bias"], d["alpha"], d["gamma"], d["eps"])
+        if w["out"] == "mxfp8":
+            O.quant_ue8m0(o["norm"])
+        times.append(time.perf_counter() - t0)
+    sec = statistics.median(times)
+    b = ACC.seam_bytes(n, w["H"], post=w["post"], out=w["out"])
+    return {"value": b / sec / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle", "seconds": sec,
+            "sample": f"first {n} of {w['T']} tokens of the same workload, single-threaded C oracle (fp64)"}
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "src": "measured"}
+    return {"hbm_gbs": 6800.0, "src": "fallback"}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = WORKLOADS[args.workload]
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    config = {"workload": args.workload, "T": w["T"], "H": w["H"], "n_hc": 4,
+              "form": "post" if w["post"] else "no_post", "out": w["out"],
+              "tokens_per_rank": w["T"], "parallelism": f"token-shard x{args.gpus} (independent)",
+              "l2": "inputs larger than L2" if ACC.seam_bytes(w["T"], w["H"], w["post"], w["out"]) > 2 * L2_BYTES
+              else "inputs smaller than L2 (warm)"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        budget = max(0.05, 150.0 / (args.steps + args.warmup))
+        for _ in range(args.warmup):
+            cpu_baseline(w, None, budget_s=min(budget, 2.0))
+        cb = cpu_baseline(w, None, budget_s=budget, steps=args.steps)
+        line = {"metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": cb["seconds"] * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+                "impl": "reference",
+                "cpu_baseline": {"value": cb["value"], "unit": UNIT, "cores": 1, "kind": "oracle", "sample": cb["sample"]},
+                "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    r = run_ours(args, w, rank, world, local_rank)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return
+    step_bytes = ACC.seam_bytes(w["T"], w["H"], post=w["post"], out=w["out"])
+    value = world * step_bytes / (r["ms"] * 1e-3) / 1e12
+    peaks = load_peaks()
+    launch_ms = r["ms"] / max(1, r["launches"])
+    achieved_gbs = step_bytes / max(1, r["launches"]) / (launch_ms * 1e-3) / 1e9
+    traffic = NCU_TRAFFIC.get((src_hash(), args.workload))
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": r["ms"], "us_per_seam": r["ms"] * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 in/out, fp32 compute", "data": "synthetic", "config": config,
+        "gpu_launches": r["launches"] * args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": traffic,
+                     "peak_src": f"{peaks['src']} hbm_gbs (copy)",
+                     "algorithmic_bytes_per_launch": step_bytes / max(1, r["launches"]),
+                     "launches_per_step": r["launches"]},
+        "clocks": r["clocks"],
+    }
+    if r["e2e"]:
+        e = r["e2e"]
+        line["e2e"] = {"value": world * step_bytes / (e["ms"] * 1e-3) / 1e12, "unit": UNIT,
+                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"], "ms_per_step": e["ms"]}
+    if not args.no_cpu_baseline:
+        cb = cpu_baseline(w, r["wl"])
+        line["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -88,14 +88,29 @@ N_HC = 4
 N_LOGITS = 24
 
 
-def seam_draws(T: int, H: int, seed: int, post: bool = True) -> dict:
+def seam_draws(T: int, H: int, seed: int, post: bool = True, unique_tokens: int | None = None) -> dict:
     """All random inputs of one seam call (CPU tensors).
 
     Returns bf16 ``R [T,4,H]``, ``Y [T,H]`` (absent when ``post`` is False),
     fp32 ``fn [4H,24]``, ``bias [24]``, ``alpha [3]``, bf16 ``gamma [H]``, and
     float64 U(-1,1) logits ``pre_logits [T,4]``, ``post_logits [T,4]``,
     ``comb_logits [T,4,4]`` for the carried gates.
+
+    ``unique_tokens``: draw only that many tokens and repeat them along T (the
+    per-token inputs of token t are those of token t mod unique_tokens).  Large
+    workloads use this to keep the CPU draw short; the device still streams
+    every byte of the full T.
     """
+    if unique_tokens is not None and 0 < unique_tokens < T:
+        d = seam_draws(unique_tokens, H, seed, post=post)
+        reps = (T + unique_tokens - 1) // unique_tokens
+        for k in ("R", "Y"):
+            if d[k] is not None:
+                d[k] = d[k].repeat((reps,) + (1,) * (d[k].dim() - 1))[:T].contiguous()
+        for k in ("pre_logits", "post_logits", "comb_logits"):
+            d[k] = np.concatenate([d[k]] * reps, axis=0)[:T]
+        d["T"] = T
+        return d
     K = N_HC * H
     d = {
         "T": T,

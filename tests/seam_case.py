@@ -1,0 +1,119 @@
+"""Shared helpers of the parity tests: build one seeded seam workload, run it
+through the C ABI on the GPU, run the oracle on the same inputs (all tokens or
+a sample), and compare with the acceptance bar.
+
+Acceptance (per output):
+  residual_out, norm   within 1 bf16 ulp on >= 99.99% of elements
+  pre, post, comb      within 1e-3 absolute
+  fp8 codes, scales    bit-exact against the oracle quantiser applied to the
+                       kernel's own norm
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle as O
+from mhc_residual_seam_gb300 import binding as B
+from mhc_residual_seam_gb300 import inputs as I
+
+ULP_FRAC = 0.9999
+GATE_TOL = 1e-3
+
+
+def make_case(T: int, H: int, seed: int, post: bool = True, mxfp8: bool = False, craft: bool = False,
+              unique_tokens: int | None = None) -> dict:
+    d = I.seam_draws(T, H, seed, post=post, unique_tokens=unique_tokens)
+    if craft:
+        I.craft_mxfp8(d, seed)
+    pre, post_g, comb = O.carried_gates(d["pre_logits"], d["post_logits"], d["comb_logits"])
+    d["pre_prev"] = torch.from_numpy(pre)
+    d["post_prev"] = torch.from_numpy(post_g) if post else None
+    d["comb_prev"] = torch.from_numpy(comb)
+    d["out_mode"] = B.MHC_OUT_MXFP8 if mxfp8 else B.MHC_OUT_BF16
+    return d
+
+
+def to_dev(d: dict, device="cuda") -> dict:
+    g = {}
+    for k in ("R", "Y", "post_prev", "comb_prev", "pre_prev", "fn", "bias", "alpha", "gamma"):
+        g[k] = None if d.get(k) is None else d[k].contiguous().to(device)
+    return g
+
+
+def run_gpu(d: dict, cfg=None, g: dict | None = None, out: dict | None = None, stream=None, inplace=False) -> dict:
+    T, H = d["T"], d["H"]
+    if g is None:
+        g = to_dev(d)
+    if out is None:
+        out = B.alloc_outputs(T, H, d["out_mode"], "cuda", cfg)
+    if inplace:
+        out["residual_out"] = g["R"]
+    B.mhc_seam(g["R"], g["Y"], g["post_prev"], g["comb_prev"], g["pre_prev"], g["fn"], None, g["bias"],
+               g["alpha"], g["gamma"], d["eps"], d["out_mode"], out["residual_out"], out["norm"],
+               out["fp8_codes"], out["e8m0_scales"], out["pre_out"], out["post_out"], out["comb_out"],
+               out["workspace"], cfg=cfg, stream=stream, T=T, H=H)
+    return out
+
+
+def to_host(out: dict) -> dict:
+    torch.cuda.synchronize()
+    h = {}
+    for k, v in out.items():
+        if v is None or k == "workspace":
+            continue
+        if v.dtype == torch.bfloat16:
+            h[k] = I.bf16_bits(v.cpu())
+        else:
+            h[k] = v.cpu().numpy()
+    return h
+
+
+def oracle_on(d: dict, idx: np.ndarray | None = None) -> dict:
+    """Oracle outputs for all tokens, or for the tokens `idx` (inputs sliced;
+    every token is independent)."""
+    sl = (lambda x: x) if idx is None else (lambda x: None if x is None else x[torch.from_numpy(idx)])
+    return O.seam(sl(d["R"]), sl(d["Y"]), sl(d["post_prev"]), sl(d["comb_prev"]), sl(d["pre_prev"]), d["fn"],
+                  d["bias"], d["alpha"], d["gamma"], d["eps"])
+
+
+def ulp_diff(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    def ordered(x):
+        u = x.astype(np.int64)
+        return np.where(u & 0x8000, -(u & 0x7FFF), u & 0x7FFF)
+    return np.abs(ordered(a) - ordered(b))
+
+
+def compare(d: dict, h: dict, idx: np.ndarray | None = None, check_quant: bool = True) -> dict:
+    """Compare GPU outputs `h` with the oracle on tokens `idx` (all if None);
+    asserts the acceptance bar and returns the measured agreement."""
+    o = oracle_on(d, idx)
+    take = (lambda x: x) if idx is None else (lambda x: x[idx])
+    rep = {}
+    for k in ("residual_out", "norm"):
+        u = ulp_diff(take(h[k]), o[k])
+        rep[k + "_exact"] = float(np.mean(u == 0))
+        rep[k + "_within1"] = float(np.mean(u <= 1))
+        rep[k + "_maxulp"] = int(u.max()) if u.size else 0
+        assert rep[k + "_within1"] >= ULP_FRAC, (k, rep)
+    for gk, ok in (("pre_out", "pre"), ("post_out", "post"), ("comb_out", "comb")):
+        err = np.abs(take(h[gk]).astype(np.float64) - o[ok].reshape(take(h[gk]).shape))
+        rep[ok + "_maxerr"] = float(err.max()) if err.size else 0.0
+        assert rep[ok + "_maxerr"] <= GATE_TOL, (ok, rep)
+    if d["out_mode"] == B.MHC_OUT_MXFP8 and check_quant:
+        # bit-exact against the oracle quantiser run on the kernel's own norm (all tokens)
+        codes, scales = O.quant_ue8m0(h["norm"])
+        rep["codes_mismatch"] = int(np.sum(codes != h["fp8_codes"]))
+        rep["scales_mismatch"] = int(np.sum(scales != h["e8m0_scales"]))
+        assert rep["codes_mismatch"] == 0 and rep["scales_mismatch"] == 0, rep
+    return rep
+
+
+def sample_tokens(T: int, n: int, seed: int, must: np.ndarray | None = None) -> np.ndarray:
+    """Token sample for the full-size cases: the first and last few tokens
+    (ragged tails) plus seeded picks, plus any tokens in `must`."""
+    picks = I.stream_bits(seed, 99, n) % np.uint64(max(T, 1))
+    s = set(range(min(T, 4))) | set(range(max(0, T - 4), T)) | set(int(p) for p in picks)
+    if must is not None:
+        s |= set(int(v) for v in must)
+    return np.array(sorted(s), dtype=np.int64)

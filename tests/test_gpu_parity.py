@@ -1,0 +1,233 @@
+"""GPU parity of the seam against the oracle, through the C ABI.
+
+Workloads are the pages' configurations at H = 5120 (T = 4, 64, 1024 mxfp8
+with crafted quantiser groups, 4160, 16384; post and no_post), tails and odd
+widths, and every launch-policy branch.  Small cases compare every element;
+the full-size cases compare a token sample (first/last tokens plus seeded
+picks) against the oracle and check the quantiser on all tokens.
+"""
+import numpy as np
+import pytest
+import torch
+
+from mhc_residual_seam_gb300 import binding as B
+from mhc_residual_seam_gb300 import inputs as I
+
+from seam_case import compare, make_case, run_gpu, sample_tokens, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    B.lib()
+
+
+# ------------------------------------------------------ the pages' configs --
+def test_config0_T4_post_bf16():
+    d = make_case(4, 5120, 1000)
+    compare(d, to_host(run_gpu(d)))
+
+
+@pytest.mark.parametrize("post", [True, False])
+def test_config1_T64(post):
+    d = make_case(64, 5120, 1001, post=post)
+    compare(d, to_host(run_gpu(d)))
+
+
+def test_config2_T1024_mxfp8_crafted():
+    d = make_case(1024, 5120, 1002, mxfp8=True, craft=True)
+    h = to_host(run_gpu(d))
+    idx = sample_tokens(1024, 24, 1002, must=d["crafted_rows"])
+    rep = compare(d, h, idx)
+    # the crafted tokens really carry the crafted groups: their norm is gamma
+    g = I.bf16_bits(d["gamma"])
+    for t in d["crafted_rows"]:
+        for grp in d["crafted_groups"]:
+            sl = slice(32 * grp, 32 * grp + 32)
+            assert np.array_equal(h["norm"][t, sl], g[sl]), (t, grp)
+    assert rep["codes_mismatch"] == 0
+
+
+@pytest.mark.parametrize("T", [4160])
+def test_config3_wave_edge(T):
+    d = make_case(T, 5120, 1003, unique_tokens=1024)
+    h = to_host(run_gpu(d))
+    compare(d, h, sample_tokens(T, 24, 1003))
+
+
+@pytest.mark.parametrize("post", [True, False])
+def test_config4_T16384(post):
+    d = make_case(16384, 5120, 1004, post=post, unique_tokens=2048)
+    h = to_host(run_gpu(d))
+    compare(d, h, sample_tokens(16384, 24, 1004))
+
+
+# ----------------------------------------------------------- tails, widths --
+@pytest.mark.parametrize("T", [1, 2, 3, 5, 9, 17, 33, 129, 257])
+def test_ragged_token_counts(T):
+    d = make_case(T, 5120, 2000 + T)
+    compare(d, to_host(run_gpu(d)))
+
+
+@pytest.mark.parametrize("H,mx", [(8, False), (40, False), (64, False), (136, False), (1024, False),
+                                  (7168, False), (32, True), (96, True), (4096, True)])
+def test_widths(H, mx):
+    d = make_case(37, H, 3000 + H, mxfp8=mx)
+    compare(d, to_host(run_gpu(d)))
+
+
+@pytest.mark.parametrize("bm,cols", [(1, 64), (2, 64), (4, 96), (8, 128), (16, 640), (32, 1024), (2, 5120)])
+def test_policy_overrides(bm, cols):
+    d = make_case(45, 5120, 4000 + bm)
+    cfg = B.MhcConfig(path=1, block_m=bm, cols_per_cta=cols)
+    compare(d, to_host(run_gpu(d, cfg=cfg)))
+
+
+def test_policy_rejects_oversized_tile():
+    d = make_case(4, 5120, 4050)
+    with pytest.raises(B.MhcError) as e:
+        run_gpu(d, cfg=B.MhcConfig(path=1, block_m=32, cols_per_cta=4096))
+    assert e.value.code == -10
+
+
+def test_multi_wave_launch():
+    # more token groups than fit on the GPU at once: several cooperative waves
+    d = make_case(3000, 1024, 4100)
+    cfg = B.MhcConfig(path=1, block_m=1, cols_per_cta=32)
+    out = run_gpu(d, cfg=cfg)
+    assert B.mhc_last_launch_count() >= 2
+    compare(d, to_host(out), sample_tokens(3000, 40, 4100))
+
+
+# ------------------------------------------------------------ behaviours ----
+def test_in_place_residual():
+    d = make_case(33, 5120, 5000)
+    compare(d, to_host(run_gpu(d, inplace=True)))
+
+
+def test_repeat_calls_are_deterministic_and_self_resetting():
+    d = make_case(64, 5120, 5001, mxfp8=True)
+    g = to_dev(d)
+    out = B.alloc_outputs(64, 5120, d["out_mode"], "cuda")
+    a = to_host(run_gpu(d, g=g, out=out))
+    b = to_host(run_gpu(d, g=g, out=out))
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+    compare(d, b)
+    B.mhc_check_status(out["workspace"])
+
+
+def test_cuda_graph_capture_and_replay():
+    d = make_case(64, 5120, 5002)
+    g = to_dev(d)
+    out = B.alloc_outputs(64, 5120, d["out_mode"], "cuda")
+    run_gpu(d, g=g, out=out)  # eager first call (per-device set-up)
+    torch.cuda.synchronize()
+    for v in out.values():
+        if v is not None and v is not out["workspace"]:
+            v.zero_()
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            run_gpu(d, g=g, out=out, stream=s)
+    for _ in range(3):
+        graph.replay()
+    compare(d, to_host(out))
+
+
+def test_two_streams_separate_workspaces():
+    d1, d2 = make_case(16, 5120, 5003), make_case(40, 5120, 5004, post=False)
+    g1, g2 = to_dev(d1), to_dev(d2)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    o1 = B.alloc_outputs(16, 5120, 0, "cuda")
+    o2 = B.alloc_outputs(40, 5120, 0, "cuda")
+    torch.cuda.synchronize()
+    for _ in range(4):
+        run_gpu(d1, g=g1, out=o1, stream=s1)
+        run_gpu(d2, g=g2, out=o2, stream=s2)
+    compare(d1, to_host(o1))
+    compare(d2, to_host(o2))
+
+
+def test_bounded_wait_runs_out_and_reports():
+    # A spin limit of one iteration makes the non-finishing CTAs give up
+    # waiting for rstd: the kernel still returns, the status word reports it,
+    # and the next call on the same workspace is correct again.
+    d = make_case(8, 5120, 5005)
+    g = to_dev(d)
+    out = B.alloc_outputs(8, 5120, 0, "cuda")
+    cfg = B.MhcConfig(path=1, spin_limit=1)
+    hit = False
+    for _ in range(5):
+        run_gpu(d, g=g, out=out, cfg=cfg)
+        try:
+            B.mhc_check_status(out["workspace"])
+        except B.MhcError as e:
+            assert e.code == -7
+            hit = True
+            break
+    assert hit
+    run_gpu(d, g=g, out=out)
+    B.mhc_check_status(out["workspace"])
+    compare(d, to_host(out))
+
+
+def test_empty_input_launches_nothing():
+    d = make_case(0, 5120, 5006)
+    out = B.alloc_outputs(0, 5120, 0, "cuda")
+    run_gpu(d, out=out)
+    assert B.mhc_last_launch_count() == 0
+
+
+# ------------------------------------------------------- standalone kernels --
+def test_standalone_quantiser_crafted_groups():
+    import oracle as O
+    x, picked = I.crafted_quant_tensor(1024, 5120, seed=1002)
+    xd = x.cuda()
+    codes = torch.empty((1024, 5120), dtype=torch.uint8, device="cuda")
+    scales = torch.empty((1024, 160), dtype=torch.uint8, device="cuda")
+    B.mhc_quant_ue8m0(xd, codes, scales)
+    c_ref, s_ref = O.quant_ue8m0(x)
+    assert np.array_equal(codes.cpu().numpy(), c_ref)
+    assert np.array_equal(scales.cpu().numpy(), s_ref)
+
+
+def test_standalone_quantiser_every_bf16_value():
+    # every finite bf16 bit pattern, in groups whose amax sets every exponent
+    import oracle as O
+    bits = np.arange(0, 0x10000, dtype=np.uint32)
+    bits = bits[((bits & 0x7F80) != 0x7F80)].astype(np.uint16)
+    n = (len(bits) + 31) // 32 * 32
+    bits = np.concatenate([bits, np.zeros(n - len(bits), np.uint16)]).reshape(-1, 32)
+    x = I.from_bf16_bits(bits)
+    xd = x.cuda()
+    rows, H = x.shape
+    codes = torch.empty((rows, H), dtype=torch.uint8, device="cuda")
+    scales = torch.empty((rows, H // 32), dtype=torch.uint8, device="cuda")
+    B.mhc_quant_ue8m0(xd, codes, scales)
+    c_ref, s_ref = O.quant_ue8m0(x)
+    assert np.array_equal(codes.cpu().numpy(), c_ref)
+    assert np.array_equal(scales.cpu().numpy(), s_ref)
+
+
+def test_pack_fn_hi_lo():
+    d = make_case(1, 256, 6000)
+    fn = d["fn"].cuda()
+    pk = torch.empty(B.mhc_packed_fn_bytes(256) // 2, dtype=torch.bfloat16, device="cuda")
+    B.mhc_pack_fn(fn, pk)
+    p = pk.view(48, 1024).cpu().to(torch.float64)
+    f = d["fn"].to(torch.float64).t()
+    hi, lo = p[:24], p[24:]
+    assert torch.equal(hi, f.to(torch.bfloat16).to(torch.float64))
+    assert torch.max(torch.abs(hi + lo - f) / torch.abs(f).clamp_min(1e-30)).item() < 2.0 ** -15
+
+
+def test_copy_kernel():
+    src = torch.randint(0, 255, (1 << 24,), dtype=torch.uint8, device="cuda")
+    dst = torch.empty_like(src)
+    B.mhc_copy(src, dst)
+    assert torch.equal(src, dst)
