@@ -16,6 +16,10 @@ cudaError_t split_init(size_t max_smem);
 cudaError_t split_capacity(bool post, bool mxfp8, int BT, int Wd, int num_sms, int* ctas);
 cudaError_t split_launch(const SeamArgs& a, int BT, int Wd, int64_t groups_per_launch, char* slots,
                          cudaStream_t stream, int* launches);
+// mhc_stream.cu
+cudaError_t stream_init();
+int stream_cols(int H);
+cudaError_t stream_launch(const SeamArgs& a, cudaStream_t stream, unsigned long long limit_ns, int* launches);
 // mhc_aux.cu
 cudaError_t pack_fn_launch(const float* fn, void* out, int H, cudaStream_t s);
 cudaError_t quant_launch(const void* x, int64_t rows, int H, float floor_, uint8_t* codes, uint8_t* scales,
@@ -29,6 +33,7 @@ constexpr size_t kHeaderBytes = 256;  // status word + padding, at the start of 
 constexpr long long kDefaultSpin = 10000000LL;
 constexpr int kMaxDevices = 64;
 constexpr size_t kSplitMaxSmem = 160 * 1024;
+constexpr int64_t kStreamMinT = 1024;  // auto policy: streaming path from this many tokens
 
 thread_local std::string g_err;
 thread_local int g_launches = 0;
@@ -71,6 +76,8 @@ int ensure_device(cudaStream_t stream, DeviceState** out) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
     e = mhc::split_init(kSplitMaxSmem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute (split path)");
+    e = mhc::stream_init();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute (streaming path)");
     st.ready = true;
   }
   *out = &st;
@@ -96,12 +103,17 @@ int make_plan(int64_t T, int H, const mhc_config* cfg, Plan* p) {
   if (c.path < 0 || c.path > 2) return fail(MHC_ERR_CONFIG, "cfg.path must be 0, 1 or 2");
   if (c.block_m != 0 && (c.block_m < 0 || c.block_m > 32 || (c.block_m & (c.block_m - 1)) != 0))
     return fail(MHC_ERR_CONFIG, "cfg.block_m must be 0 or a power of two <= 32");
-  if (c.cols_per_cta != 0 && (c.cols_per_cta < 32 || c.cols_per_cta % 32 != 0 || c.cols_per_cta > 4096))
-    return fail(MHC_ERR_CONFIG, "cfg.cols_per_cta must be 0 or a multiple of 32 in [32, 4096]");
+  if (c.cols_per_cta != 0 && (c.cols_per_cta < 32 || c.cols_per_cta % 32 != 0 || c.cols_per_cta > 16384))
+    return fail(MHC_ERR_CONFIG, "cfg.cols_per_cta must be 0 or a multiple of 32 in [32, 16384]");
   if (c.sinkhorn_iters < 0 || c.sinkhorn_iters > 10000) return fail(MHC_ERR_CONFIG, "cfg.sinkhorn_iters out of range");
   if (!(c.amax_floor >= 0.f) || c.amax_floor > 1e30f) return fail(MHC_ERR_CONFIG, "cfg.amax_floor out of range");
   if (c.spin_limit < 0) return fail(MHC_ERR_CONFIG, "cfg.spin_limit must be >= 0");
-  p->path = 1;
+  p->path = (c.path == 2 || (c.path == 0 && T >= kStreamMinT && mhc::stream_cols(H) > 0)) ? 2 : 1;
+  if (p->path == 2) {
+    if (mhc::stream_cols(H) == 0)
+      return fail(MHC_ERR_SHAPE, "the streaming path needs H a multiple of 64 with 512 <= H <= 7168");
+    return MHC_OK;
+  }
   if (T <= 8) {
     p->BT = next_pow2(T < 1 ? 1 : T);
     p->Wd = 64;
@@ -119,7 +131,6 @@ int make_plan(int64_t T, int H, const mhc_config* cfg, Plan* p) {
   if (c.cols_per_cta) p->Wd = c.cols_per_cta;
   const int Hr = (H + 31) / 32 * 32;
   if (p->Wd > Hr) p->Wd = Hr;
-  if (c.path == 2) return fail(MHC_ERR_CONFIG, "cfg.path = 2 is not available in this build");
   if (mhc::split_smem_bytes(p->BT, p->Wd) > kSplitMaxSmem)
     return fail(MHC_ERR_CONFIG, "block_m * cols_per_cta too large: x of one CTA does not fit in shared memory");
   return MHC_OK;
@@ -262,6 +273,15 @@ int mhc_seam(const void* R, const void* Y, const float* post_prev, const float* 
   a.spin_limit = (cfg && cfg->spin_limit) ? cfg->spin_limit : kDefaultSpin;
 
   int launches = 0;
+  if (plan.path == 2) {
+    if (!fn_packed) return fail(MHC_ERR_NULL, "the streaming path needs fn_packed (mhc_pack_fn) or cfg.path = 1");
+    if (T >= ((int64_t)1 << 31)) return fail(MHC_ERR_SHAPE, "the streaming path takes T < 2^31");
+    cudaError_t e = mhc::stream_launch(a, s, (unsigned long long)a.spin_limit * 100ull, &launches);
+    if (e == cudaErrorInvalidValue) return fail(MHC_ERR_CUDA, "tensor map encoding failed (streaming path)");
+    if (e != cudaSuccess) return cuda_fail(e, "seam launch (streaming path)");
+    g_launches = launches;
+    return MHC_OK;
+  }
   int cap = 0;
   cudaError_t e = mhc::split_capacity(Y != nullptr, mx, plan.BT, plan.Wd, dev->num_sms, &cap);
   if (e != cudaSuccess) return cuda_fail(e, "occupancy query (split path)");

@@ -38,10 +38,14 @@ def to_dev(d: dict, device="cuda") -> dict:
     g = {}
     for k in ("R", "Y", "post_prev", "comb_prev", "pre_prev", "fn", "bias", "alpha", "gamma"):
         g[k] = None if d.get(k) is None else d[k].contiguous().to(device)
+    H = d["H"]
+    g["fn_packed"] = torch.empty(B.mhc_packed_fn_bytes(H) // 2, dtype=torch.bfloat16, device=device)
+    B.mhc_pack_fn(g["fn"], g["fn_packed"])
     return g
 
 
-def run_gpu(d: dict, cfg=None, g: dict | None = None, out: dict | None = None, stream=None, inplace=False) -> dict:
+def run_gpu(d: dict, cfg=None, g: dict | None = None, out: dict | None = None, stream=None, inplace=False,
+            packed: bool = True) -> dict:
     T, H = d["T"], d["H"]
     if g is None:
         g = to_dev(d)
@@ -49,7 +53,8 @@ def run_gpu(d: dict, cfg=None, g: dict | None = None, out: dict | None = None, s
         out = B.alloc_outputs(T, H, d["out_mode"], "cuda", cfg)
     if inplace:
         out["residual_out"] = g["R"]
-    B.mhc_seam(g["R"], g["Y"], g["post_prev"], g["comb_prev"], g["pre_prev"], g["fn"], None, g["bias"],
+    B.mhc_seam(g["R"], g["Y"], g["post_prev"], g["comb_prev"], g["pre_prev"], g["fn"],
+               g["fn_packed"] if packed else None, g["bias"],
                g["alpha"], g["gamma"], d["eps"], d["out_mode"], out["residual_out"], out["norm"],
                out["fp8_codes"], out["e8m0_scales"], out["pre_out"], out["post_out"], out["comb_out"],
                out["workspace"], cfg=cfg, stream=stream, T=T, H=H)

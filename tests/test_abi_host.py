@@ -100,8 +100,10 @@ def test_config_validation(L):
 def test_workspace_grows_with_tokens_and_columns(L):
     a = L.mhc_workspace_bytes(4, 5120, None)
     b = L.mhc_workspace_bytes(64, 5120, None)
-    c = L.mhc_workspace_bytes(1024, 5120, None)
-    assert 256 < a < b < c
+    c = L.mhc_workspace_bytes(1024, 5120, None)          # streaming path: status word only
+    p1 = B.MhcConfig(path=1)
+    d = L.mhc_workspace_bytes(1024, 5120, C.byref(p1))   # split path forced
+    assert 256 < a < b < d and c == 256
     cfg = B.MhcConfig(block_m=8, cols_per_cta=64)
     assert L.mhc_workspace_bytes(64, 5120, C.byref(cfg)) == 256 + 8 * (((64 + 128 + 80 * 8 * 128) + 255) // 256 * 256)
 

@@ -231,3 +231,79 @@ def test_copy_kernel():
     dst = torch.empty_like(src)
     B.mhc_copy(src, dst)
     assert torch.equal(src, dst)
+
+
+# ------------------------------------------------- streaming path (path 2) --
+STREAM = dict(path=2)
+
+
+@pytest.mark.parametrize("T", [1, 31, 32, 33, 257, 1000])
+def test_stream_ragged_tokens(T):
+    d = make_case(T, 5120, 7000 + T)
+    compare(d, to_host(run_gpu(d, cfg=B.MhcConfig(**STREAM))))
+
+
+@pytest.mark.parametrize("H", [512, 576, 1024, 4096, 7168])
+@pytest.mark.parametrize("mx", [False, True])
+def test_stream_widths(H, mx):
+    d = make_case(70, H, 7100 + H, mxfp8=mx)
+    compare(d, to_host(run_gpu(d, cfg=B.MhcConfig(**STREAM))))
+
+
+def test_stream_no_post_and_in_place():
+    d = make_case(300, 5120, 7200, post=False)
+    compare(d, to_host(run_gpu(d, cfg=B.MhcConfig(**STREAM), inplace=True)))
+
+
+def test_stream_mxfp8_crafted():
+    d = make_case(256, 5120, 7300, mxfp8=True, craft=True)
+    h = to_host(run_gpu(d, cfg=B.MhcConfig(**STREAM)))
+    compare(d, h, sample_tokens(256, 16, 7300, must=d["crafted_rows"]))
+    g = I.bf16_bits(d["gamma"])
+    for t in d["crafted_rows"]:
+        for grp in d["crafted_groups"]:
+            sl = slice(32 * grp, 32 * grp + 32)
+            assert np.array_equal(h["norm"][t, sl], g[sl]), (t, grp)
+
+
+def test_stream_matches_split_path_closely():
+    d = make_case(200, 5120, 7400)
+    a = to_host(run_gpu(d, cfg=B.MhcConfig(path=1)))
+    b = to_host(run_gpu(d, cfg=B.MhcConfig(path=2)))
+    from seam_case import ulp_diff
+    assert np.mean(ulp_diff(a["residual_out"], b["residual_out"]) <= 1) >= 0.9999
+    assert np.max(np.abs(a["comb_out"] - b["comb_out"])) < 1e-3
+
+
+def test_stream_repeat_deterministic_and_graph():
+    d = make_case(1024, 5120, 7500, mxfp8=True)
+    g = to_dev(d)
+    out = B.alloc_outputs(1024, 5120, d["out_mode"], "cuda")
+    a = to_host(run_gpu(d, g=g, out=out))
+    assert B.mhc_last_launch_count() == 1
+    b = to_host(run_gpu(d, g=g, out=out))
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    out["norm"].zero_()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            run_gpu(d, g=g, out=out, stream=s)
+    graph.replay()
+    c = to_host(out)
+    assert np.array_equal(a["norm"], c["norm"])
+    compare(d, c, sample_tokens(1024, 16, 7500))
+    B.mhc_check_status(out["workspace"])
+
+
+def test_stream_requires_packed_fn_and_supported_width():
+    d = make_case(40, 5120, 7600)
+    with pytest.raises(B.MhcError) as e:
+        run_gpu(d, cfg=B.MhcConfig(**STREAM), packed=False)
+    assert e.value.code == -1
+    d = make_case(40, 520, 7601)
+    with pytest.raises(B.MhcError) as e:
+        run_gpu(d, cfg=B.MhcConfig(**STREAM))
+    assert e.value.code == -2
