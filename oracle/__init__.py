@@ -113,7 +113,7 @@ def sinkhorn(M: np.ndarray, iters: int = 20) -> np.ndarray:
 def carried_gates(pre_logits, post_logits, comb_logits, iters: int = 20):
     """Carried-gate inputs from U(-1,1) draws, in the form the seam itself
     emits: pre = sigmoid, post = 2 sigmoid, comb = Sinkhorn20(exp(.)), fp32."""
-    sig = np.vectorize(sigmoid)
+    sig = np.vectorize(sigmoid, otypes=[np.float64])
     pre = sig(np.asarray(pre_logits, np.float64)).astype(np.float32)
     post = (2.0 * sig(np.asarray(post_logits, np.float64))).astype(np.float32)
     comb = sinkhorn(np.exp(np.asarray(comb_logits, np.float64)), iters).astype(np.float32)
