@@ -37,25 +37,31 @@ def build(force: bool = False) -> str:
 def lib():
     global _lib
     if _lib is None:
-        _lib = C.CDLL(build())
-        P = C.c_void_p
-        _lib.mhc_oracle_bf16_rne.restype = C.c_uint16
-        _lib.mhc_oracle_bf16_rne.argtypes = [C.c_double]
-        _lib.mhc_oracle_bf16_to_double.restype = C.c_double
-        _lib.mhc_oracle_bf16_to_double.argtypes = [C.c_uint16]
-        _lib.mhc_oracle_e4m3_rne_satfinite.restype = C.c_uint8
-        _lib.mhc_oracle_e4m3_rne_satfinite.argtypes = [C.c_double]
-        _lib.mhc_oracle_ue8m0_exponent.restype = C.c_int
-        _lib.mhc_oracle_ue8m0_exponent.argtypes = [C.c_double, C.c_double]
-        _lib.mhc_oracle_quant_ue8m0.restype = C.c_int
-        _lib.mhc_oracle_quant_ue8m0.argtypes = [P, C.c_int64, C.c_int, C.c_double, P, P]
-        _lib.mhc_oracle_sinkhorn.restype = None
-        _lib.mhc_oracle_sinkhorn.argtypes = [C.c_int, P, C.c_int]
-        _lib.mhc_oracle_sigmoid.restype = C.c_double
-        _lib.mhc_oracle_sigmoid.argtypes = [C.c_double]
-        _lib.mhc_oracle_seam.restype = C.c_int
-        _lib.mhc_oracle_seam.argtypes = [C.c_int64, C.c_int] + [P] * 9 + [C.c_double, C.c_int, C.c_int] + [P] * 7
+        _lib = bind(C.CDLL(build()))
     return _lib
+
+
+def bind(cdll):
+    """Declare the C signatures on a loaded oracle library."""
+    L = cdll
+    P = C.c_void_p
+    L.mhc_oracle_bf16_rne.restype = C.c_uint16
+    L.mhc_oracle_bf16_rne.argtypes = [C.c_double]
+    L.mhc_oracle_bf16_to_double.restype = C.c_double
+    L.mhc_oracle_bf16_to_double.argtypes = [C.c_uint16]
+    L.mhc_oracle_e4m3_rne_satfinite.restype = C.c_uint8
+    L.mhc_oracle_e4m3_rne_satfinite.argtypes = [C.c_double]
+    L.mhc_oracle_ue8m0_exponent.restype = C.c_int
+    L.mhc_oracle_ue8m0_exponent.argtypes = [C.c_double, C.c_double]
+    L.mhc_oracle_quant_ue8m0.restype = C.c_int
+    L.mhc_oracle_quant_ue8m0.argtypes = [P, C.c_int64, C.c_int, C.c_double, P, P]
+    L.mhc_oracle_sinkhorn.restype = None
+    L.mhc_oracle_sinkhorn.argtypes = [C.c_int, P, C.c_int]
+    L.mhc_oracle_sigmoid.restype = C.c_double
+    L.mhc_oracle_sigmoid.argtypes = [C.c_double]
+    L.mhc_oracle_seam.restype = C.c_int
+    L.mhc_oracle_seam.argtypes = [C.c_int64, C.c_int] + [P] * 9 + [C.c_double, C.c_int, C.c_int] + [P] * 7
+    return L
 
 
 def _ptr(a):

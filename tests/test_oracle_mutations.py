@@ -1,0 +1,76 @@
+"""The pins catch plausible mistakes: each case plants one slip in a copy of
+the oracle's C source (on the CPU), builds it, and checks that at least one
+pin of tests/test_oracle_pins.py fails against the planted copy."""
+import ctypes as C
+import os
+import subprocess
+
+import pytest
+
+import oracle as O
+import test_oracle_pins as P
+
+SRC = os.path.join(os.path.dirname(O.__file__), "mhc_oracle.c")
+
+MUTATIONS = {
+    "comb_transposed": ("(double)comb[i * 4 + j]", "(double)comb[j * 4 + i]"),
+    "post_term_dropped": ("if (Y) v += (double)post_prev", "if (0) v += (double)post_prev"),
+    "rstd_mean_over_H": ("sqrt(sR / (double)K + eps)", "sqrt(sR / (double)H + eps)"),
+    "post_gate_not_doubled": ("2.0 * mhc_oracle_sigmoid(l[4 + i])", "mhc_oracle_sigmoid(l[4 + i])"),
+    "alpha_groups_shifted": ("int g = k < 4 ? 0 : (k < 8 ? 1 : 2);", "int g = k < 8 ? 0 : 1;"),
+    "unrounded_rprime": ("rp[i * H + h] = rprime_unrounded ? v : mhc_oracle_bf16_to_double(b);",
+                         "rp[i * H + h] = v;"),
+    "gamma_dropped": ("x[h] * rstdx * mhc_oracle_bf16_to_double(gamma[h])", "x[h] * rstdx"),
+    "fn_index_transposed": ("(double)fn[(size_t)r * N_LOG + k]", "(double)fn[(size_t)k * K + r]"),
+    "sinkhorn_columns_first": ("for (int it = 0; it < iters; ++it) {\n        for (int i = 0; i < n; ++i) {",
+                               "for (int it = 0; it < iters; ++it) {\n        for (int i = 0; i < 0; ++i) {"),
+    "bf16_truncates": ("double r = rint(a / spacing) * spacing;\n    if (r >= ldexp(1.0, 128))",
+                       "double r = floor(a / spacing) * spacing;\n    if (r >= ldexp(1.0, 128))"),
+    "e4m3_one_bit_short": ("spacing = ldexp(1.0, (e - 1) - 3);", "spacing = ldexp(1.0, (e - 1) - 2);"),
+    "e8m0_bias_off_by_one": ("scales[r * G + g] = (uint8_t)(e + 127);", "scales[r * G + g] = (uint8_t)(e + 128);"),
+    "x_uses_equal_weights": ("v += (double)pre[i] * rp[i * H + h];", "v += 0.25 * rp[i * H + h];"),
+}
+
+PINS = [
+    P.test_bf16_rne_matches_torch_cast_on_float32_inputs,
+    P.test_e4m3_golden_codes_from_ocp_spec,
+    P.test_ue8m0_exponent_exhaustive_over_bf16_amax,
+    P.test_crafted_groups_448_times_power_of_two,
+    P.test_sinkhorn_one_round_is_row_then_column,
+    P.test_permutation_comb_permutes_streams,
+    P.test_post_term_adds_post_times_Y,
+    P.test_collapse_uses_carried_pre,
+    P.test_zero_fn_gives_bias_gates,
+    P.test_one_hot_fn_picks_stream_signs,
+    P.test_constant_row_norm_closed_form,
+]
+
+
+def _build_mutant(tmp_path, name):
+    old, new = MUTATIONS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, name
+    path = tmp_path / f"{name}.c"
+    path.write_text(src.replace(old, new))
+    so = tmp_path / f"lib_{name}.so"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", str(so), str(path), "-lm"])
+    return O.bind(C.CDLL(str(so)))
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_slip_fails_a_pin(tmp_path, monkeypatch, name):
+    mutant = _build_mutant(tmp_path, name)
+    monkeypatch.setattr(O, "_lib", mutant)
+    failed = []
+    for pin in PINS:
+        try:
+            pin(O)
+        except AssertionError:
+            failed.append(pin.__name__)
+    extra = []
+    if not failed:  # the brute force is the slowest pin; run it only if needed
+        try:
+            P.test_brute_force_T1_H8_asymmetric_comb(O, 31)
+        except AssertionError:
+            extra.append("brute_force")
+    assert failed or extra, f"no pin caught {name}"
