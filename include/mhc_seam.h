@@ -153,6 +153,29 @@ int mhc_quant_ue8m0(const void* x, int64_t rows, int H, float amax_floor, uint8_
  * equal the seam's). */
 int mhc_copy(const void* src, void* dst, size_t bytes, void* stream);
 
+/* mhc_seam() on the split path (cfg->path 0 or 1; path 2 is refused) for
+ * callers that cannot allocate device memory: a plug-in inside a host program
+ * that owns every device allocation, code running inside an allocator
+ * callback, or a loop that must never block in the allocator.  The paper has
+ * no counterpart; this entry point exists only for such callers.
+ * Arguments are those of mhc_seam() without fn_packed, workspace and ws_bytes.
+ * The scratch (partial sums, arrival counters, status word) lives in a fixed
+ * 1 MiB static device array in the library, held by every GPU that loads it
+ * until the process exits; a call whose mhc_workspace_bytes(T, H, cfg with
+ * path 1) exceeds 1 MiB is refused with MHC_ERR_WORKSPACE (at H = 5120 and
+ * the default policy: T above 480).  It calls no cudaMalloc/cudaFree or
+ * allocating routine.  The first call on a device resolves the array's
+ * address (cudaGetSymbolAddress) and should be made before any stream
+ * capture.  Every call first clears the part of the array it uses
+ * (cudaMemsetAsync on `stream`); all calls share the array, so calls that can
+ * overlap on the GPU race on it and must be serialised by the caller.  A
+ * bounded wait that runs out is not reported by this entry point. */
+int mhc_seam_noalloc(const void* R, const void* Y, const float* post_prev, const float* comb_prev,
+                     const float* pre_prev, const float* fn, const float* bias, const float* alpha,
+                     const void* gamma, float eps, int64_t T, int H, mhc_out_mode out_mode, void* residual_out,
+                     void* norm, uint8_t* fp8_codes, uint8_t* e8m0_scales, float* pre_out, float* post_out,
+                     float* comb_out, const mhc_config* cfg, void* stream);
+
 /* Number of kernel launches the last successful mhc_seam() on this host
  * thread issued (1 for every non-empty call). */
 int mhc_last_launch_count(void);

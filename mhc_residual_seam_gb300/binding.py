@@ -59,6 +59,8 @@ def lib():
         L.mhc_pack_fn.argtypes = [P, P, I, P]
         L.mhc_seam.restype = I
         L.mhc_seam.argtypes = [P] * 10 + [C.c_float, I64, I, I] + [P] * 7 + [P, C.c_size_t, P, P]
+        L.mhc_seam_noalloc.restype = I
+        L.mhc_seam_noalloc.argtypes = [P] * 9 + [C.c_float, I64, I, I] + [P] * 7 + [P, P]
         L.mhc_quant_ue8m0.restype = I
         L.mhc_quant_ue8m0.argtypes = [P, I64, I, C.c_float, P, P, P]
         L.mhc_copy.restype = I
@@ -143,6 +145,21 @@ def mhc_seam(R, Y, post_prev, comb_prev, pre_prev, fn, fn_packed, bias, alpha, g
                           int(out_mode), _ptr(residual_out), _ptr(norm), _ptr(fp8_codes), _ptr(e8m0_scales),
                           _ptr(pre_out), _ptr(post_out), _ptr(comb_out), _ptr(workspace), ws_bytes, _cfg(cfg),
                           _stream(stream)))
+
+
+def mhc_seam_noalloc(R, Y, post_prev, comb_prev, pre_prev, fn, bias, alpha, gamma, eps: float, out_mode: int,
+                     residual_out, norm, fp8_codes, e8m0_scales, pre_out, post_out, comb_out, cfg=None,
+                     stream=None, T: int | None = None, H: int | None = None) -> None:
+    """mhc_seam on the split path with the library's own static scratch, for
+    callers that cannot allocate device memory (no workspace argument)."""
+    if T is None:
+        T = R.shape[0]
+    if H is None:
+        H = R.shape[-1]
+    _check(lib().mhc_seam_noalloc(_ptr(R), _ptr(Y), _ptr(post_prev), _ptr(comb_prev), _ptr(pre_prev), _ptr(fn),
+                                  _ptr(bias), _ptr(alpha), _ptr(gamma), float(eps), int(T), int(H), int(out_mode),
+                                  _ptr(residual_out), _ptr(norm), _ptr(fp8_codes), _ptr(e8m0_scales),
+                                  _ptr(pre_out), _ptr(post_out), _ptr(comb_out), _cfg(cfg), _stream(stream)))
 
 
 def mhc_quant_ue8m0(x, codes, scales, amax_floor: float = 0.0, stream=None) -> None:

@@ -327,3 +327,7 @@ int mhc_last_launch_count(void) { return g_launches; }
 const char* mhc_last_error_string(void) { return g_err.c_str(); }
 
 }  // extern "C"
+
+namespace mhc {
+void set_last_error(const std::string& msg) { g_err = msg; }
+}  // namespace mhc
