@@ -56,6 +56,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+__device__ __forceinline__ float2 bf16pair(uint32_t u) { return make_float2(bf16lo(u), bf16hi(u)); }
+
 __device__ __forceinline__ void unpack8(const uint4& v, float* f) {
   f[0] = bf16lo(v.x); f[1] = bf16hi(v.x);
   f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
@@ -123,6 +125,9 @@ __device__ __forceinline__ uint8_t quant_group32(const uint32_t* nb, uint32_t* c
 // 24 projections d[k]).  Logit order [pre 0..3 | post 4..7 | comb 8..23
 // row-major], alpha[0] pre, alpha[1] post, alpha[2] comb.  The Sinkhorn runs
 // on exp(l - rowmax): the row scale cancels in the first row normalisation.
+// Reciprocals use the hardware approximation (__fdividef, a few ulp): the 160
+// normalisations of the Sinkhorn are a serial chain per token, and the gates
+// are checked to 1e-3.
 __device__ __forceinline__ void finish_gates(float sR, const float* d, const float* alpha,
                                              const float* bias, int K, float eps, int iters,
                                              float* pre, float* post, float* comb) {
@@ -130,8 +135,8 @@ __device__ __forceinline__ void finish_gates(float sR, const float* d, const flo
   float a0 = alpha[0] * rstdR, a1 = alpha[1] * rstdR, a2 = alpha[2] * rstdR;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    pre[i] = 1.0f / (1.0f + expf(-(a0 * d[i] + bias[i])));
-    post[i] = 2.0f / (1.0f + expf(-(a1 * d[4 + i] + bias[4 + i])));
+    pre[i] = __fdividef(1.0f, 1.0f + expf(-(a0 * d[i] + bias[i])));
+    post[i] = __fdividef(2.0f, 1.0f + expf(-(a1 * d[4 + i] + bias[4 + i])));
   }
   float M[16];
 #pragma unroll
@@ -148,13 +153,13 @@ __device__ __forceinline__ void finish_gates(float sR, const float* d, const flo
   for (int it = 0; it < iters; ++it) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      float s = 1.0f / ((M[4 * i] + M[4 * i + 1]) + (M[4 * i + 2] + M[4 * i + 3]));
+      float s = __fdividef(1.0f, (M[4 * i] + M[4 * i + 1]) + (M[4 * i + 2] + M[4 * i + 3]));
 #pragma unroll
       for (int j = 0; j < 4; ++j) M[4 * i + j] *= s;
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      float s = 1.0f / ((M[j] + M[4 + j]) + (M[8 + j] + M[12 + j]));
+      float s = __fdividef(1.0f, (M[j] + M[4 + j]) + (M[8 + j] + M[12 + j]));
 #pragma unroll
       for (int i = 0; i < 4; ++i) M[4 * i + j] *= s;
     }

@@ -1,384 +1,499 @@
 // Streaming path of the delayed mHC seam: bandwidth-tuned for large T.
 //
-// One cluster of 8 CTAs per block of 32 tokens; CTA r of the cluster owns
-// columns [r W, (r+1) W) of H for all four streams (W = H / 8).  Per 64-column
-// chunk, TMA brings the four R tiles, the Y tile and the four hi/lo-packed fn
-// tiles into shared memory (128-byte swizzle); eight compute warps (thread =
-// token, warp = 8-column slice) post-mix in fp32, round R' to bf16 in place,
-// accumulate the sums of squares, and store the collapsed x in tensor memory;
-// one thread issues the gate projection on the tensor cores (tcgen05,
-// D[64 x 32] += fn^T[64 x 64] . R'^T[64 x 32] per stream and 16-wide k step,
-// rows 0..23 hi, 24..47 lo, fp32 accumulation in TMEM) and stores R' with TMA.
-// The split over the 8 CTAs is reduced through distributed shared memory:
-// each CTA sends its per-token partials to the token's owner CTA, the owner
-// finishes the gates and sends rstd_x back, and every CTA normalises its own
-// x from tensor memory ("[FlyDSL] Single-launch Mega-mHC on gfx950", Kernel
-// Architecture: split-K, DIST_FINISH -- here co-residency is guaranteed by
-// the cluster launch, so no wait can depend on an unscheduled CTA).
+// Persistent clusters of 4 CTAs (one CTA per SM).  CTA r of a cluster owns
+// columns [r W, (r+1) W) of H for all four streams (W = H / 4) and the cluster
+// walks blocks of 32 tokens.  Per 64-column chunk:
+//  - an input producer warp TMA-loads the four R tiles and the Y tile into a
+//    ring of 5 input stages (128-byte swizzle, L2 evict-first);
+//  - an fn producer warp TMA-loads the four hi/lo-packed fn tiles [48 x 64]
+//    into a ring of 2 fn stages (L2 evict-last: every cluster reuses them);
+//  - eight compute warps (thread = token, warp = 8-column slice; the swizzle
+//    makes the column reads conflict-free) read their inputs, release the
+//    input stage, post-mix in fp32, round R' to bf16 into a ring of 2 output
+//    stages, accumulate s_R and s_x, and store x in tensor memory;
+//  - one thread issues the gate projection on the tensor cores (tcgen05,
+//    D[64 x 32] += fn^T[64 x 64] . R'^T[64 x 32] per stream and 16-wide k
+//    step; rows 0..23 hi, 24..47 lo; fp32 accumulation in TMEM, one
+//    accumulator per stream so consecutive MMAs do not wait on each other)
+//    and TMA-stores the R' tiles.
+// After the last chunk of a block each CTA sends its per-token partial sums
+// (24 projections, s_R, s_x) to the token's owner CTA through distributed
+// shared memory and arrives on the owner's barrier; the owner's finisher warp
+// returns rstd_x at once and then computes the gates; every CTA normalises its
+// x from tensor memory and TMA-stores the norm (and the ue8m0 codes), staging
+// the tiles in the output ring, which is idle at that point.  The producers
+// run ahead into the next block meanwhile.  ("[FlyDSL] Single-launch
+// Mega-mHC on gfx950", Kernel Architecture: split-K with a distributed finish;
+// here the cluster launch makes every CTA of a split co-resident.)
 //
-// Roles: warps 0-7 compute, warp 8 TMA producer, warp 9 MMA issuer, R' store
-// and tensor-memory owner.  Two pipeline stages; two CTAs per SM.
-
-#include <cooperative_groups.h>
+// Every wait is bounded; after the first wait that runs out, the CTA records
+// the error (bit 1 of the status word) and every later wait returns at once,
+// so the kernel always terminates.
 
 #include "mhc_common.cuh"
 #include "mhc_sm100.cuh"
 
-namespace cg = cooperative_groups;
-
 namespace mhc {
 
+namespace {
+
+constexpr int kCl = 4;                 // CTAs per cluster
+constexpr int kBM = 32;                // tokens per block
+constexpr int kChunk = 64;             // columns per chunk
+constexpr int kNI = 6, kNF = 2, kNO = 2;
+constexpr int kComputeThreads = 256;   // warps 0-7
+constexpr int kThreads = 384;          // + warp 8 input producer, 9 MMA, 10 fn producer, 11 finisher
+constexpr int kFnRows = 48;
+constexpr uint32_t kRTile = kBM * 128;                 // 4 KB
+constexpr uint32_t kFnTile = kFnRows * 128;            // 6 KB
+constexpr uint32_t kFnStage = 4 * kFnTile;             // 24 KB
+constexpr uint32_t kOutStage = 4 * kRTile;             // 16 KB
+constexpr uint32_t kInStage = 5 * kRTile;              // 20 KB (R tiles 0-3, Y tile 4)
+constexpr uint32_t kOffFn = 0;
+constexpr uint32_t kOffOut = kOffFn + kNF * kFnStage;  // fn tile 3's extra A rows read into here
+constexpr uint32_t kOffIn = kOffOut + kNO * kOutStage;
+constexpr uint32_t kOffTail = kOffIn + kNI * kInStage;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColD = 0;                          // accumulators: 32 columns (tokens) each
+constexpr int kMaxChunks = (int)((kTmemCols - 2 * 32) / 16);  // x: 16 columns per chunk after 2-4 accumulators
+constexpr uint32_t kIdesc = idesc_bf16_f32(64, kBM);
+constexpr int kSlots = kBM / kCl;                      // tokens owned per CTA and block
+constexpr int kPartPad = 28;                           // 26 parts padded to 7 float4
+
+struct Tail {
+  uint64_t in_full[kNI], in_empty[kNI], fn_full[kNF], fn_empty[kNF], out_full[kNO], out_empty[kNO];
+  uint64_t d_full, recv_full[2], rstd_full[2];
+  uint32_t tmem_base;
+  volatile int err;
+  float red[8][kBM][2];                  // per compute warp: s_R, s_x of each token
+  float dmat[kFnRows][kBM];              // D rows (hi 0..23, lo 24..47) x tokens
+  float recv[2][kCl][kSlots][kPartPad];  // [block parity][source CTA][owned token][part]
+  float rstd[2][kBM];                    // [block parity][token]
+};
+
+constexpr size_t kSmemBytes = kOffTail + sizeof(Tail) + 1024;
+
+struct Ctx {
+  const SeamArgs* a;
+  Tail* tl;
+  uint64_t limit_ns;
+};
+
+__device__ __forceinline__ void flag_error(const Ctx& x) {
+  if (!x.tl->err) {
+    x.tl->err = 1;
+    atomicOr(x.a->status, 2u);
+  }
+}
+// Bounded wait on a CTA-local barrier; returns at once after an earlier error.
+__device__ __forceinline__ void wait_local(const Ctx& x, uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity, 0)) return;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity, 20000)) {
+    if (x.tl->err) return;
+    if (globaltimer_ns() - t0 > x.limit_ns) {
+      flag_error(x);
+      return;
+    }
+  }
+}
+__device__ __forceinline__ void wait_remote(const Ctx& x, uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait_cluster(bar, parity, 0)) return;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait_cluster(bar, parity, 20000)) {
+    if (x.tl->err) return;
+    if (globaltimer_ns() - t0 > x.limit_ns) {
+      flag_error(x);
+      return;
+    }
+  }
+}
+
+}  // namespace
+
 // Gate finish of one token on its owner CTA, kept out of line so its arrays
-// do not raise the register pressure of the streaming loop.
-__device__ __noinline__ void finish_owner(const SeamArgs& a, int64_t t, const float* p, int H, float* r) {
+// do not raise the register pressure of the kernel.
+__device__ __noinline__ void finish_store_gates(const SeamArgs& a, int64_t t, const float* p, int H) {
   float pre[4], post[4], cb[16];
   finish_gates(p[24], p, a.alpha, a.bias, kStreams * H, a.eps, a.sinkhorn_iters, pre, post, cb);
   store_gates(a, t, pre, post, cb);
-  *r = 1.0f / sqrtf(p[25] / (float)H + a.eps);
-}
-constexpr int kClusterCtas = 8;
-constexpr int kBM = 32;                 // tokens per cluster
-constexpr int kChunk = 64;              // columns per pipeline stage
-constexpr int kStreamThreads = 320;     // 8 compute warps + producer + MMA
-constexpr int kFnRows = 48;             // 24 hi + 24 lo
-constexpr uint32_t kFnTile = kFnRows * 128;    // 6 KB
-constexpr uint32_t kRTile = kBM * 128;         // 4 KB
-constexpr uint32_t kOffFn = 0;
-constexpr uint32_t kOffR = 4 * kFnTile;        // 24 KB
-constexpr uint32_t kOffY = kOffR + 4 * kRTile; // 40 KB
-constexpr uint32_t kStageBytes = kOffY + kRTile;  // 44 KB
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColD = 0;           // D: 32 columns (tokens)
-constexpr uint32_t kColX = 32;          // x: 16 columns per chunk
-constexpr int kMaxChunks = (int)((kTmemCols - kColX) / 16);  // 14
-constexpr uint32_t kIdesc = idesc_bf16_f32(64, kBM);
-
-struct StreamTail {
-  uint64_t full[2], rdy[2], empty[2], dfull, drained;
-  uint32_t tmem_base;
-  int err;
-  float red[8][kBM][2];       // per compute warp: sum R'^2, sum x^2 of each token
-  float dmat[kFnRows][kBM];   // D rows (hi 0..23, lo 24..47) x tokens
-  float recv[kClusterCtas][kBM / kClusterCtas][kParts];  // partials sent to this owner CTA
-  float rstd[kBM];            // rstd_x of the block's tokens
-};
-
-size_t stream_smem_bytes() { return 2 * kStageBytes + sizeof(StreamTail) + 1024; }
-
-__device__ __forceinline__ void note_timeout(const SeamArgs& a, StreamTail* tl) {
-  tl->err = 1;
-  atomicOr(a.status, 2u);
 }
 
 template <bool POST, bool MXFP8>
-__global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kStreamThreads, 2)
+__global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
     stream_seam_kernel(const SeamArgs a, const __grid_constant__ CUtensorMap tmR,
                        const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmRo,
                        const __grid_constant__ CUtensorMap tmFn, const __grid_constant__ CUtensorMap tmN,
-                       const __grid_constant__ CUtensorMap tmC, int W, unsigned long long limit_ns) {
+                       const __grid_constant__ CUtensorMap tmC, int W, int n_blocks, unsigned long long limit_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* stage0 = sm;
-  StreamTail* tl = reinterpret_cast<StreamTail*>(sm + 2 * kStageBytes);
+  Tail* tl = reinterpret_cast<Tail*>(sm + kOffTail);
+  const Ctx X{&a, tl, limit_ns};
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  cg::cluster_group cluster = cg::this_cluster();
-  const int rank = (int)cluster.block_rank();
+  const uint32_t rank = cluster_ctarank();
   const int H = a.H;
   const int64_t T = a.T;
-  const int64_t t0 = (int64_t)(blockIdx.x / kClusterCtas) * kBM;
-  const int hbase = rank * W;
-  const int wcols = max(0, min(W, H - hbase));
-  const int nch = (wcols + kChunk - 1) / kChunk;
+  const int hbase = (int)rank * W;
+  const int nch = (max(0, min(W, H - hbase)) + kChunk - 1) / kChunk;
+  const int cid = blockIdx.x / kCl, ncl = gridDim.x / kCl;
 
   if (tid == 0) {
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&tl->full[s], 1);
-      mbar_init(&tl->rdy[s], 8);
-      mbar_init(&tl->empty[s], 2);
+    for (int s = 0; s < kNI; ++s) {
+      mbar_init(&tl->in_full[s], 1);
+      mbar_init(&tl->in_empty[s], 8);
     }
-    mbar_init(&tl->dfull, 1);
-    mbar_init(&tl->drained, 1);
+    for (int s = 0; s < kNF; ++s) {
+      mbar_init(&tl->fn_full[s], 1);
+      mbar_init(&tl->fn_empty[s], 1);
+    }
+    for (int s = 0; s < kNO; ++s) {
+      mbar_init(&tl->out_full[s], 8);
+      mbar_init(&tl->out_empty[s], 2);
+    }
+    mbar_init(&tl->d_full, 1);
+    for (int p = 0; p < 2; ++p) {
+      mbar_init(&tl->recv_full[p], kCl);
+      mbar_init(&tl->rstd_full[p], kCl);
+    }
     tl->err = 0;
     mbar_fence_init();
   }
   if (warp == 8 && lane == 0) {
     prefetch_tmap(&tmR);
-    prefetch_tmap(&tmFn);
     if (POST) prefetch_tmap(&tmY);
     prefetch_tmap(&tmRo);
+    prefetch_tmap(&tmN);
   }
+  if (warp == 10 && lane == 0) prefetch_tmap(&tmFn);
+  if (warp == 11 && lane == 0) prefetch_tmap(&tmC);
   if (warp == 9) {
     tmem_alloc(&tl->tmem_base, kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
-  cluster.sync();  // barriers initialised; every CTA of the cluster is running
+  __syncwarp();
+  cluster_sync_all();  // barriers initialised in every CTA of the cluster
   tc_fence_after();
   const uint32_t tmem = tl->tmem_base;
 
+  const int nacc = nch <= kMaxChunks - 8 ? 4 : 2;  // independent accumulators (TMEM room permitting)
+  const uint32_t colx = 32u * (uint32_t)nacc;       // x columns start after the accumulators
+
   if (warp == 8) {
-    // ------------------------------------------------------ TMA producer --
+    // --------------------------------------------------- input producer --
     if (lane == 0) {
-      const uint64_t pol_stream = l2_evict_first(), pol_w = l2_evict_last();
-      const uint32_t bytes = 4 * kFnTile + 4 * kRTile + (POST ? kRTile : 0);
-      int issued = 0;
-      for (int c = 0; c < nch; ++c) {
-        const int s = c & 1;
-        const uint32_t ph = (c >> 1) & 1;
-        if (!mbar_wait(&tl->empty[s], ph ^ 1, limit_ns)) {
-          note_timeout(a, tl);
-          break;
+      const uint64_t pol = l2_evict_first();
+      const uint32_t bytes = (POST ? 5 : 4) * kRTile;
+      int j = 0;
+      for (int b = cid; b < n_blocks; b += ncl) {
+        const int t0 = b * kBM;
+        for (int c = 0; c < nch; ++c, ++j) {
+          const int s = j % kNI;
+          wait_local(X, &tl->in_empty[s], ((j / kNI) & 1) ^ 1);
+          uint8_t* st = sm + kOffIn + s * kInStage;
+          const int h = hbase + c * kChunk;
+          mbar_arrive_expect_tx(&tl->in_full[s], bytes);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) tma_load_3d(st + i * kRTile, &tmR, &tl->in_full[s], h, i, t0, pol);
+          if (POST) tma_load_2d(st + 4 * kRTile, &tmY, &tl->in_full[s], h, t0, pol);
         }
-        uint8_t* st = stage0 + s * kStageBytes;
-        const int h = hbase + c * kChunk;
-        mbar_arrive_expect_tx(&tl->full[s], bytes);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) tma_load_3d(st + kOffFn + i * kFnTile, &tmFn, &tl->full[s], h, i, 0, pol_w);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          tma_load_3d(st + kOffR + i * kRTile, &tmR, &tl->full[s], h, i, (int)t0, pol_stream);
-        if (POST) tma_load_2d(st + kOffY, &tmY, &tl->full[s], h, (int)t0, pol_stream);
-        issued = c + 1;
       }
-      // Every load this CTA issued has landed before it can exit (bounded;
-      // immediate unless a consumer gave up waiting).
-      for (int c = (issued > 2 ? issued - 2 : 0); c < issued; ++c)
-        if (!mbar_wait(&tl->full[c & 1], (c >> 1) & 1, limit_ns)) note_timeout(a, tl);
+      // every load issued has landed before the CTA can exit
+      for (int jj = (j > kNI ? j - kNI : 0); jj < j; ++jj) {
+        if (!mbar_wait(&tl->in_full[jj % kNI], (jj / kNI) & 1, limit_ns)) flag_error(X);
+      }
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------ fn producer --
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_last();
+      int j = 0;
+      for (int b = cid; b < n_blocks; b += ncl) {
+        for (int c = 0; c < nch; ++c, ++j) {
+          const int f = j % kNF;
+          wait_local(X, &tl->fn_empty[f], ((j / kNF) & 1) ^ 1);
+          uint8_t* st = sm + kOffFn + f * kFnStage;
+          const int h = hbase + c * kChunk;
+          mbar_arrive_expect_tx(&tl->fn_full[f], kFnStage);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) tma_load_3d(st + i * kFnTile, &tmFn, &tl->fn_full[f], h, i, 0, pol);
+        }
+      }
+      for (int jj = (j > kNF ? j - kNF : 0); jj < j; ++jj) {
+        if (!mbar_wait(&tl->fn_full[jj % kNF], (jj / kNF) & 1, limit_ns)) flag_error(X);
+      }
     }
   } else if (warp == 9) {
-    // -------------------------------------- MMA issuer and R' tile store --
+    // ------------------------------------- MMA issuer and R' tile stores --
     if (lane == 0) {
-      for (int c = 0; c < nch; ++c) {
-        const int s = c & 1;
-        const uint32_t ph = (c >> 1) & 1;
-        if (!mbar_wait(&tl->rdy[s], ph, limit_ns)) {
-          note_timeout(a, tl);
-          break;
-        }
-        tc_fence_after();
-        uint8_t* st = stage0 + s * kStageBytes;
-        const uint32_t fa = smem_u32(st + kOffFn), rb = smem_u32(st + kOffR);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
+      int j = 0;
+      for (int b = cid; b < n_blocks; b += ncl) {
+        const int t0 = b * kBM;
+        for (int c = 0; c < nch; ++c, ++j) {
+          const int o = j % kNO, f = j % kNF;
+          wait_local(X, &tl->out_full[o], (j / kNO) & 1);
+          wait_local(X, &tl->fn_full[f], (j / kNF) & 1);
+          tc_fence_after();
+          const uint32_t fa = smem_u32(sm + kOffFn + f * kFnStage);
+          const uint32_t rb = smem_u32(sm + kOffOut + o * kOutStage);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            tc_mma_bf16(tmem + kColD, sdesc_k_sw128(fa + i * kFnTile + kk * 32), sdesc_k_sw128(rb + i * kRTile + kk * 32),
-                        kIdesc, (c | i | kk) != 0);
-          }
-        }
-        tc_commit(&tl->empty[s]);
-        const int h = hbase + c * kChunk;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) tma_store_3d(&tmRo, st + kOffR + i * kRTile, h, i, (int)t0);
-        tma_store_commit();
-        tma_store_wait_read_all();
-        mbar_arrive(&tl->empty[s]);
+            for (int i = 0; i < 4; ++i) {
+              const int acc = i % nacc;
+              tc_mma_bf16(tmem + kColD + 32 * acc, sdesc_k_sw128(fa + i * kFnTile + kk * 32),
+                          sdesc_k_sw128(rb + i * kRTile + kk * 32), kIdesc, !(c == 0 && kk == 0 && i < nacc));
+            }
+          }
+          tc_commit(&tl->fn_empty[f]);
+          tc_commit(&tl->out_empty[o]);
+          if (c == nch - 1) tc_commit(&tl->d_full);
+          const int h = hbase + c * kChunk;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) tma_store_3d(&tmRo, sm + kOffOut + o * kOutStage + i * kRTile, h, i, t0);
+          tma_store_commit();
+          tma_store_wait_read_all();
+          mbar_arrive(&tl->out_empty[o]);
+        }
       }
-      tc_commit(&tl->dfull);
-      mbar_arrive(&tl->drained);
       tma_store_wait_all();
     }
-  } else {
-    // ------------------------------------------------------- compute warps --
-    const int q = warp & 3, wq = warp >> 2;
-    const int64_t t = t0 + lane;
-    const bool tv = t < T;
-    float comb[16], postg[4], preg[4];
+  } else if (warp == 11) {
+    // ----------------- finisher: rstd_x first, then the gates of 8 tokens --
+    int lb = 0;
+    for (int b = cid; b < n_blocks; b += ncl, ++lb) {
+      const int par = lb & 1;
+      if (lane < kSlots) {
+        wait_remote(X, &tl->recv_full[par], (lb >> 1) & 1);
+        const int tok = (int)rank + kCl * lane;
+        const int64_t tt = (int64_t)b * kBM + tok;
+        float sx = 0.f;
 #pragma unroll
-    for (int k = 0; k < 16; ++k) comb[k] = 0.f;
+        for (int src = 0; src < kCl; ++src) sx += tl->recv[par][src][lane][25];
+        const float r = tt < T ? 1.0f / sqrtf(sx / (float)H + a.eps) : 0.f;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) postg[k] = preg[k] = 0.f;
-    if (tv) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        float4 v = __ldg(reinterpret_cast<const float4*>(a.comb_prev + t * 16) + k);
-        comb[4 * k] = v.x; comb[4 * k + 1] = v.y; comb[4 * k + 2] = v.z; comb[4 * k + 3] = v.w;
+        for (int dst = 0; dst < kCl; ++dst) st_cluster_f32(mapa_shared(smem_u32(&tl->rstd[par][tok]), dst), r);
+        fence_acq_rel_cluster();
       }
-      float4 p = __ldg(reinterpret_cast<const float4*>(a.pre_prev + t * 4));
-      preg[0] = p.x; preg[1] = p.y; preg[2] = p.z; preg[3] = p.w;
-      if (POST) {
-        float4 v = __ldg(reinterpret_cast<const float4*>(a.post_prev + t * 4));
-        postg[0] = v.x; postg[1] = v.y; postg[2] = v.z; postg[3] = v.w;
-      }
-    }
-    const uint32_t xaddr = tmem + ((uint32_t)(32 * q) << 16) + kColX + 8 * wq;
-    const uint32_t off = lane * 128 + ((warp ^ (lane & 7)) << 4);  // row = token, 16-byte chunk = warp
-    float sR = 0.f, sx = 0.f;
-    for (int c = 0; c < nch; ++c) {
-      const int s = c & 1;
-      const uint32_t ph = (c >> 1) & 1;
-      if (!mbar_wait(&tl->full[s], ph, limit_ns)) {
-        note_timeout(a, tl);
-        break;
-      }
-      uint8_t* st = stage0 + s * kStageBytes;
-      // inputs stay packed (bf16x2 words); one word = two columns at a time
-      uint4 rin[4], yin = make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) rin[j] = *reinterpret_cast<const uint4*>(st + kOffR + j * kRTile + off);
-      if (POST) yin = *reinterpret_cast<const uint4*>(st + kOffY + off);
-      uint32_t ow[4][4];
-      float x[8];
-#pragma unroll
-      for (int wd = 0; wd < 4; ++wd) {
-        const uint32_t w0 = (&rin[0].x)[wd], w1 = (&rin[1].x)[wd], w2 = (&rin[2].x)[wd], w3 = (&rin[3].x)[wd];
-        const uint32_t wy = (&yin.x)[wd];
-        const float a0 = bf16lo(w0), a1 = bf16lo(w1), a2 = bf16lo(w2), a3 = bf16lo(w3), ya = bf16lo(wy);
-        const float b0 = bf16hi(w0), b1 = bf16hi(w1), b2 = bf16hi(w2), b3 = bf16hi(w3), yb = bf16hi(wy);
-        float xa = 0.f, xb = 0.f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float va = comb[4 * i] * a0, vb = comb[4 * i] * b0;
-          va = fmaf(comb[4 * i + 1], a1, va); vb = fmaf(comb[4 * i + 1], b1, vb);
-          va = fmaf(comb[4 * i + 2], a2, va); vb = fmaf(comb[4 * i + 2], b2, vb);
-          va = fmaf(comb[4 * i + 3], a3, va); vb = fmaf(comb[4 * i + 3], b3, vb);
-          if (POST) { va = fmaf(postg[i], ya, va); vb = fmaf(postg[i], yb, vb); }
-          const uint32_t o = pack_bf16x2(va, vb);
-          ow[i][wd] = o;
-          const float ra = bf16lo(o), rb = bf16hi(o);
-          sR = fmaf(ra, ra, sR);
-          sR = fmaf(rb, rb, sR);
-          xa = fmaf(preg[i], ra, xa);
-          xb = fmaf(preg[i], rb, xb);
-        }
-        x[2 * wd] = xa;
-        x[2 * wd + 1] = xb;
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        *reinterpret_cast<uint4*>(st + kOffR + i * kRTile + off) = make_uint4(ow[i][0], ow[i][1], ow[i][2], ow[i][3]);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) sx = fmaf(x[e], x[e], sx);
-      tc_st_x8(xaddr + 16 * c, x);
-      fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tl->rdy[s]);
-    }
-    tc_wait_st();
-    tl->red[warp][lane][0] = sR;
-    tl->red[warp][lane][1] = sx;
-  }
-
-  // ---------------------------------------------------- partial sums out --
-  __syncthreads();
-  if (warp < 4) {
-    float dv[32];
-    bool ok = nch > 0 && mbar_wait(&tl->dfull, 0, limit_ns);
-    if (nch > 0 && !ok) note_timeout(a, tl);
-    tc_fence_after();
-    if (ok) {
-      // M = 64 accumulator: row m sits in lane 32 (m / 16) + m % 16
-      const uint32_t daddr = tmem + ((uint32_t)(32 * warp) << 16) + kColD;
+      if (lane < kCl) mbar_arrive_remote(mapa_shared(smem_u32(&tl->rstd_full[par]), lane));
+      if (lane < kSlots) {
+        const int64_t tt = (int64_t)b * kBM + (int)rank + kCl * lane;
+        float p[kParts];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) tc_ld_x8(daddr + 8 * k, dv + 8 * k);
-    } else {
+        for (int k = 0; k < kParts; ++k) {
+          float s = 0.f;
 #pragma unroll
-      for (int k = 0; k < 32; ++k) dv[k] = 0.f;
+          for (int src = 0; src < kCl; ++src) s += tl->recv[par][src][lane][k];
+          p[k] = s;
+        }
+        if (tt < T) finish_store_gates(a, tt, p, H);
+      }
+      __syncwarp();
     }
-    const int m = 16 * warp + lane;
-    if (lane < 16 && m < kFnRows) {
-#pragma unroll
-      for (int n = 0; n < kBM; ++n) tl->dmat[m][n] = dv[n];
-    }
-  }
-  __syncthreads();
-  for (int idx = tid; idx < kBM * kParts; idx += kStreamThreads) {
-    const int tok = idx / kParts, k = idx - tok * kParts;
-    float v;
-    if (k < 24) {
-      v = tl->dmat[k][tok] + tl->dmat[24 + k][tok];
-    } else {
-      v = 0.f;
-#pragma unroll
-      for (int w = 0; w < 8; ++w) v += tl->red[w][tok][k - 24];
-    }
-    float* dst = cluster.map_shared_rank(&tl->recv[rank][tok / kClusterCtas][k], tok % kClusterCtas);
-    *dst = v;
-  }
-  cluster.sync();
-
-  // ---------------------------------------- owner: gates and rstd_x -----
-  if (tid < kBM / kClusterCtas) {
-    const int tok = rank + kClusterCtas * tid;
-    const int64_t t = t0 + tok;
-    float p[kParts];
-#pragma unroll
-    for (int k = 0; k < kParts; ++k) {
-      float s = 0.f;
-#pragma unroll
-      for (int src = 0; src < kClusterCtas; ++src) s += tl->recv[src][tid][k];
-      p[k] = s;
-    }
-    float r = 0.f;
-    if (t < T) {
-      finish_owner(a, t, p, H, &r);
-    }
-    for (int dst = 0; dst < kClusterCtas; ++dst) *cluster.map_shared_rank(&tl->rstd[tok], dst) = r;
-  }
-  cluster.sync();
-
-  // --------------------------------------------------------------- norm --
-  uint8_t* nbuf = stage0;                       // nch x [32 x 64] bf16, 128-byte swizzle
-  uint8_t* cbuf = stage0 + kMaxChunks * kRTile; // nch x [32 x 64] u8, row-major
-  if (warp < 8) {
-    if (!mbar_wait(&tl->drained, 0, limit_ns)) note_timeout(a, tl);
+  } else {
+    // ---------------------------------------------------- compute warps --
     const int q = warp & 3, wq = warp >> 2;
-    const uint32_t xaddr = tmem + ((uint32_t)(32 * q) << 16) + kColX + 8 * wq;
-    const uint32_t off = lane * 128 + ((warp ^ (lane & 7)) << 4);
-    const float r = tl->rstd[lane];
-    for (int c = 0; c < nch; ++c) {
-      float x[8], gm[8];
-      tc_ld_x8(xaddr + 16 * c, x);
-      const int h = hbase + c * kChunk + 8 * warp;
-      if (h < H) {
-        unpack8(__ldg(reinterpret_cast<const uint4*>(a.gamma + h)), gm);
-      } else {
+    const uint32_t xaddr = tmem + ((uint32_t)(32 * q) << 16) + colx + 8 * wq;
+    const uint32_t daddr = tmem + ((uint32_t)(32 * warp) << 16) + kColD;  // warps 0-3
+    const uint32_t off = lane * 128 + ((warp ^ (lane & 7)) << 4);       // row = token, 16-byte chunk = warp
+    const int per_phase = MXFP8 ? 5 : 8;                                // norm chunks staged per pass
+    int j = 0, lb = 0;
+    for (int b = cid; b < n_blocks; b += ncl, ++lb) {
+      const int t0 = b * kBM;
+      const int64_t t = (int64_t)t0 + lane;
+      float2 comb2[16], post2[4], pre2[4];  // each gate duplicated for the fp32x2 FMAs
 #pragma unroll
-        for (int e = 0; e < 8; ++e) gm[e] = 0.f;
-      }
-      uint4 ov;
-      ov.x = pack_bf16x2(x[0] * r * gm[0], x[1] * r * gm[1]);
-      ov.y = pack_bf16x2(x[2] * r * gm[2], x[3] * r * gm[3]);
-      ov.z = pack_bf16x2(x[4] * r * gm[4], x[5] * r * gm[5]);
-      ov.w = pack_bf16x2(x[6] * r * gm[6], x[7] * r * gm[7]);
-      *reinterpret_cast<uint4*>(nbuf + c * kRTile + off) = ov;
-    }
-  }
-  __syncthreads();
-  if (MXFP8) {
-    // one thread per (token, 32-column group): the group's amax and codes
-    for (int idx = tid; idx < kBM * nch * 2; idx += kStreamThreads) {
-      const int tok = idx % kBM, grp = idx / kBM;
-      const int c = grp >> 1, half = grp & 1;
-      const int h = hbase + c * kChunk + 32 * half;
-      uint32_t nb[16];
+      for (int k = 0; k < 16; ++k) comb2[k] = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int ch = 4 * half + j;
-        uint4 v = *reinterpret_cast<const uint4*>(nbuf + c * kRTile + tok * 128 + ((ch ^ (tok & 7)) << 4));
-        nb[4 * j] = v.x; nb[4 * j + 1] = v.y; nb[4 * j + 2] = v.z; nb[4 * j + 3] = v.w;
+      for (int k = 0; k < 4; ++k) post2[k] = pre2[k] = make_float2(0.f, 0.f);
+      if (t < T) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float4 v = __ldg(reinterpret_cast<const float4*>(a.comb_prev + t * 16) + k);
+          comb2[4 * k] = make_float2(v.x, v.x); comb2[4 * k + 1] = make_float2(v.y, v.y);
+          comb2[4 * k + 2] = make_float2(v.z, v.z); comb2[4 * k + 3] = make_float2(v.w, v.w);
+        }
+        float4 p = __ldg(reinterpret_cast<const float4*>(a.pre_prev + t * 4));
+        pre2[0] = make_float2(p.x, p.x); pre2[1] = make_float2(p.y, p.y);
+        pre2[2] = make_float2(p.z, p.z); pre2[3] = make_float2(p.w, p.w);
+        if (POST) {
+          float4 v = __ldg(reinterpret_cast<const float4*>(a.post_prev + t * 4));
+          post2[0] = make_float2(v.x, v.x); post2[1] = make_float2(v.y, v.y);
+          post2[2] = make_float2(v.z, v.z); post2[3] = make_float2(v.w, v.w);
+        }
       }
-      uint32_t cw[8];
-      const uint8_t sb = quant_group32(nb, cw, a.amax_floor);
-      uint4* cd = reinterpret_cast<uint4*>(cbuf + c * (kBM * 64) + tok * 64 + 32 * half);
-      cd[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-      cd[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-      const int64_t t = t0 + tok;
-      if (t < T && h < H) a.scales[t * (H / 32) + h / 32] = sb;
+      float2 sR2 = make_float2(0.f, 0.f), sx2 = make_float2(0.f, 0.f);
+      for (int c = 0; c < nch; ++c, ++j) {
+        const int s = j % kNI, o = j % kNO;
+        wait_local(X, &tl->in_full[s], (j / kNI) & 1);
+        const uint8_t* st = sm + kOffIn + s * kInStage;
+        uint4 rin[4], yin = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) rin[i] = *reinterpret_cast<const uint4*>(st + i * kRTile + off);
+        if (POST) yin = *reinterpret_cast<const uint4*>(st + 4 * kRTile + off);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tl->in_empty[s]);
+        // Two columns at a time with packed fp32x2 FMAs (each half rounds
+        // exactly like a scalar FMA).
+        uint32_t ow[4][4];
+        float x[8];
+#pragma unroll
+        for (int wd = 0; wd < 4; ++wd) {
+          const float2 r0 = bf16pair((&rin[0].x)[wd]), r1 = bf16pair((&rin[1].x)[wd]);
+          const float2 r2 = bf16pair((&rin[2].x)[wd]), r3 = bf16pair((&rin[3].x)[wd]);
+          const float2 yy = bf16pair((&yin.x)[wd]);
+          float2 xx = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float2 v = __fmul2_rn(comb2[4 * i], r0);
+            v = __ffma2_rn(comb2[4 * i + 1], r1, v);
+            v = __ffma2_rn(comb2[4 * i + 2], r2, v);
+            v = __ffma2_rn(comb2[4 * i + 3], r3, v);
+            if (POST) v = __ffma2_rn(post2[i], yy, v);
+            const uint32_t w = pack_bf16x2(v.x, v.y);
+            ow[i][wd] = w;
+            const float2 rr = bf16pair(w);
+            sR2 = __ffma2_rn(rr, rr, sR2);
+            xx = __ffma2_rn(pre2[i], rr, xx);
+          }
+          x[2 * wd] = xx.x;
+          x[2 * wd + 1] = xx.y;
+          sx2 = __ffma2_rn(xx, xx, sx2);
+        }
+        wait_local(X, &tl->out_empty[o], ((j / kNO) & 1) ^ 1);
+        uint8_t* ost = sm + kOffOut + o * kOutStage;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          *reinterpret_cast<uint4*>(ost + i * kRTile + off) = make_uint4(ow[i][0], ow[i][1], ow[i][2], ow[i][3]);
+        tc_st_x8(xaddr + 16 * c, x);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tl->out_full[o]);
+      }
+      tc_wait_st();
+
+      // ------------------------------------------ block finish: partials --
+      tl->red[warp][lane][0] = sR2.x + sR2.y;
+      tl->red[warp][lane][1] = sx2.x + sx2.y;
+      if (warp < 4) {
+        float dv[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) dv[k] = 0.f;
+        if (nch > 0) {
+          wait_local(X, &tl->d_full, lb & 1);
+          tc_fence_after();
+          for (int acc = 0; acc < nacc; ++acc) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              float v[8];
+              tc_ld_x8(daddr + 32 * acc + 8 * k, v);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) dv[8 * k + e] += v[e];
+            }
+          }
+        }
+        const int m = 16 * warp + lane;  // M = 64 accumulator: row m in lane 32 (m / 16) + m % 16
+        if (lane < 16 && m < kFnRows) {
+#pragma unroll
+          for (int n = 0; n < kBM; ++n) tl->dmat[m][n] = dv[n];
+        }
+      }
+      tc_fence_before();
+      named_bar_sync(1, kComputeThreads);
+      const int par = lb & 1;
+      if (tid < kBM * (kPartPad / 4)) {  // one 16-byte remote store per (token, 4 parts)
+        const int tok = tid / (kPartPad / 4), k0 = 4 * (tid - tok * (kPartPad / 4));
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int k = k0 + e;
+          if (k < 24) {
+            v[e] = tl->dmat[k][tok] + tl->dmat[24 + k][tok];
+          } else if (k < kParts) {
+            float s = 0.f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) s += tl->red[w][tok][k - 24];
+            v[e] = s;
+          } else {
+            v[e] = 0.f;
+          }
+        }
+        st_cluster_v4(mapa_shared(smem_u32(&tl->recv[par][rank][tok / kCl][k0]), tok % kCl),
+                      make_float4(v[0], v[1], v[2], v[3]));
+      }
+      fence_acq_rel_cluster();
+      named_bar_sync(1, kComputeThreads);
+      if (tid < kCl) mbar_arrive_remote(mapa_shared(smem_u32(&tl->recv_full[par]), tid));
+
+      // -------------------------------------------- norm (and ue8m0) out --
+      // The output ring is idle once the MMA thread is done with the last two
+      // chunks of this block; the norm tiles are staged there.
+      wait_local(X, &tl->out_empty[j % kNO], ((j / kNO) & 1) ^ 1);
+      wait_local(X, &tl->out_empty[(j + 1) % kNO], (((j + 1) / kNO) & 1) ^ 1);
+      wait_remote(X, &tl->rstd_full[par], (lb >> 1) & 1);
+      const float r = tl->rstd[par][lane];
+      uint8_t* nbase = sm + kOffOut;
+      for (int c0 = 0; c0 < nch; c0 += per_phase) {
+        const int cn = min(per_phase, nch - c0);
+        if (c0 > 0) {
+          if (tid == 0) tma_store_wait_read_all();
+          named_bar_sync(1, kComputeThreads);
+        }
+        for (int cc = 0; cc < cn; ++cc) {
+          const int c = c0 + cc;
+          float xv[8], gm[8];
+          tc_ld_x8(xaddr + 16 * c, xv);
+          unpack8(__ldg(reinterpret_cast<const uint4*>(a.gamma + hbase + c * kChunk + 8 * warp)), gm);
+          uint4 ov;
+          ov.x = pack_bf16x2(xv[0] * r * gm[0], xv[1] * r * gm[1]);
+          ov.y = pack_bf16x2(xv[2] * r * gm[2], xv[3] * r * gm[3]);
+          ov.z = pack_bf16x2(xv[4] * r * gm[4], xv[5] * r * gm[5]);
+          ov.w = pack_bf16x2(xv[6] * r * gm[6], xv[7] * r * gm[7]);
+          *reinterpret_cast<uint4*>(nbase + cc * kRTile + off) = ov;
+        }
+        if (MXFP8) {
+          named_bar_sync(1, kComputeThreads);
+          for (int g = tid; g < 2 * kBM * cn; g += kComputeThreads) {  // (token, 32-column group)
+            const int tok = g & (kBM - 1), half = (g >> 5) & 1, cc = g >> 6;
+            const uint8_t* nt = nbase + cc * kRTile;
+            uint32_t nb[16];
+#pragma unroll
+            for (int jq = 0; jq < 4; ++jq) {
+              const int ch = 4 * half + jq;
+              uint4 v = *reinterpret_cast<const uint4*>(nt + tok * 128 + ((ch ^ (tok & 7)) << 4));
+              nb[4 * jq] = v.x; nb[4 * jq + 1] = v.y; nb[4 * jq + 2] = v.z; nb[4 * jq + 3] = v.w;
+            }
+            uint32_t cw[8];
+            const uint8_t sb = quant_group32(nb, cw, a.amax_floor);
+            uint4* cd = reinterpret_cast<uint4*>(nbase + per_phase * kRTile + cc * (kBM * 64) + tok * 64 + 32 * half);
+            cd[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+            cd[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+            const int64_t tt = (int64_t)t0 + tok;
+            if (tt < T) a.scales[tt * (H / 32) + (hbase + (c0 + cc) * kChunk + 32 * half) / 32] = sb;
+          }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, kComputeThreads);
+        if (tid == 0) {
+          for (int cc = 0; cc < cn; ++cc) {
+            tma_store_2d(&tmN, nbase + cc * kRTile, hbase + (c0 + cc) * kChunk, t0);
+            if (MXFP8) tma_store_2d(&tmC, nbase + per_phase * kRTile + cc * (kBM * 64), hbase + (c0 + cc) * kChunk, t0);
+          }
+          tma_store_commit();
+        }
+      }
+      // the output ring is handed back to the next block once the norm stores have read it
+      if (tid == 0) tma_store_wait_read_all();
+      named_bar_sync(1, kComputeThreads);
     }
+    if (tid == 0) tma_store_wait_all();
   }
-  fence_proxy_async_smem();
+
   tc_fence_before();
-  __syncthreads();
-  if (tid == 0) {
-    for (int c = 0; c < nch; ++c) {
-      tma_store_2d(&tmN, nbuf + c * kRTile, hbase + c * kChunk, (int)t0);
-      if (MXFP8) tma_store_2d(&tmC, cbuf + c * (kBM * 64), hbase + c * kChunk, (int)t0);
-    }
-    tma_store_commit();
-    tma_store_wait_all();
-  }
+  __syncwarp();
+  cluster_sync_all();  // no CTA leaves while a peer may still write into it
   if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -386,19 +501,18 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kStreamTh
 }
 
 // ------------------------------------------------------------- host side --
-using StreamKernel = void (*)(SeamArgs, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
-                              CUtensorMap, int, unsigned long long);
-
 static void* stream_kernel_ptr(bool post, bool mxfp8) {
   if (post) return mxfp8 ? (void*)stream_seam_kernel<true, true> : (void*)stream_seam_kernel<true, false>;
   return mxfp8 ? (void*)stream_seam_kernel<false, true> : (void*)stream_seam_kernel<false, false>;
 }
 
+size_t stream_smem_bytes() { return kSmemBytes; }
+
 cudaError_t stream_init() {
   for (int p = 0; p < 2; ++p)
     for (int m = 0; m < 2; ++m) {
-      cudaError_t e = cudaFuncSetAttribute(stream_kernel_ptr(p, m), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)stream_smem_bytes());
+      cudaError_t e =
+          cudaFuncSetAttribute(stream_kernel_ptr(p, m), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
       if (e != cudaSuccess) return e;
     }
   return cudaSuccess;
@@ -406,8 +520,8 @@ cudaError_t stream_init() {
 
 // Columns per CTA for width H, or 0 when the streaming path cannot take H.
 int stream_cols(int H) {
-  if (H % kChunk != 0 || H < kChunk * kClusterCtas) return 0;
-  const int chunks = (H / kChunk + kClusterCtas - 1) / kClusterCtas;
+  if (H % kChunk != 0 || H < 512) return 0;
+  const int chunks = (H / kChunk + kCl - 1) / kCl;
   if (chunks > kMaxChunks) return 0;
   return chunks * kChunk;
 }
@@ -437,8 +551,24 @@ static bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void*
              sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Clusters that fit at once, per device (queried once).
+static int max_clusters(void* kernel) {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cache[dev] > 0) return cache[dev];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kCl, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) return 0;
+  cache[dev] = n;
+  return n;
+}
+
 // Returns cudaSuccess, or cudaErrorInvalidValue when a tensor map cannot be
-// encoded (the caller reports it).
+// encoded or no cluster fits (the caller reports it).
 cudaError_t stream_launch(const SeamArgs& a, cudaStream_t stream, unsigned long long limit_ns, int* launches) {
   const int H = a.H;
   const int W = stream_cols(H);
@@ -463,15 +593,18 @@ cudaError_t stream_launch(const SeamArgs& a, cudaStream_t stream, unsigned long 
   if (ok) ok = encode(&mC, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.codes ? (const void*)a.codes : (const void*)a.norm, d2,
                       sC, b2, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (!ok) return cudaErrorInvalidValue;
-  const int64_t blocks = (a.T + kBM - 1) / kBM;
   void* k = stream_kernel_ptr(a.Y != nullptr, a.codes != nullptr);
+  const int n_blocks = (int)((a.T + kBM - 1) / kBM);
+  const int fit = max_clusters(k);
+  if (fit <= 0) return cudaErrorInvalidValue;
+  const int ncl = n_blocks < fit ? n_blocks : fit;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(blocks * kClusterCtas), 1, 1);
-  cfg.blockDim = dim3(kStreamThreads, 1, 1);
-  cfg.dynamicSmemBytes = stream_smem_bytes();
+  cfg.gridDim = dim3((unsigned)(ncl * kCl), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
-  int Wi = W;
-  void* args[] = {const_cast<SeamArgs*>(&a), &mR, &mY, &mRo, &mFn, &mN, &mC, &Wi, &limit_ns};
+  int Wi = W, nb = n_blocks;
+  void* args[] = {const_cast<SeamArgs*>(&a), &mR, &mY, &mRo, &mFn, &mN, &mC, &Wi, &nb, &limit_ns};
   cudaError_t e = cudaLaunchKernelExC(&cfg, k, args);
   if (e == cudaSuccess) ++*launches;
   return e;
