@@ -157,11 +157,13 @@ def run_ours(args, w: dict, rank: int, world: int, local_rank: int) -> dict | No
     g["fn_packed"] = torch.empty(B.mhc_packed_fn_bytes(H) // 2, dtype=torch.bfloat16, device=device)
     B.mhc_pack_fn(g["fn"], g["fn_packed"], stream=stream)  # once per weight update, outside the timed region
 
+    cfg = B.MhcConfig(projection={"auto": 0, "mma": 1, "tcgen05": 2}[args.projection])
+
     def step():
         B.mhc_seam(g["R"], g["Y"], g["post_prev"], g["comb_prev"], g["pre_prev"], g["fn"], g["fn_packed"], g["bias"],
                    g["alpha"], g["gamma"], wl["eps"], mode, out["residual_out"], out["norm"], out["fp8_codes"],
                    out["e8m0_scales"], out["pre_out"], out["post_out"], out["comb_out"], out["workspace"],
-                   stream=stream)
+                   cfg=cfg, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -279,6 +281,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--projection", choices=["auto", "mma", "tcgen05"], default="auto",
+                    help="streaming path's gate projection (auto = the library's policy)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -290,6 +294,7 @@ def main():
     config = {"workload": args.workload, "T": w["T"], "H": w["H"], "n_hc": 4,
               "form": "post" if w["post"] else "no_post", "out": w["out"],
               "tokens_per_rank": w["T"], "parallelism": f"token-shard x{args.gpus} (independent)",
+              "projection": args.projection,
               "l2": "inputs larger than L2" if ACC.seam_bytes(w["T"], w["H"], w["post"], w["out"]) > 2 * L2_BYTES
               else "inputs smaller than L2 (warm)"}
 

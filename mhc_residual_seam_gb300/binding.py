@@ -34,7 +34,7 @@ class MhcError(RuntimeError):
 class MhcConfig(C.Structure):
     """mhc_config: zero in a field means the policy decides."""
     _fields_ = [("path", C.c_int), ("block_m", C.c_int), ("cols_per_cta", C.c_int), ("sinkhorn_iters", C.c_int),
-                ("amax_floor", C.c_float), ("spin_limit", C.c_longlong)]
+                ("amax_floor", C.c_float), ("spin_limit", C.c_longlong), ("projection", C.c_int)]
 
 
 _lib = None

@@ -19,7 +19,8 @@ cudaError_t split_launch(const SeamArgs& a, int BT, int Wd, int64_t groups_per_l
 // mhc_stream.cu
 cudaError_t stream_init();
 int stream_cols(int H);
-cudaError_t stream_launch(const SeamArgs& a, cudaStream_t stream, unsigned long long limit_ns, int* launches);
+cudaError_t stream_launch(const SeamArgs& a, bool tcgen05_proj, cudaStream_t stream, unsigned long long limit_ns,
+                          int* launches);
 // mhc_aux.cu
 cudaError_t pack_fn_launch(const float* fn, void* out, int H, cudaStream_t s);
 cudaError_t quant_launch(const void* x, int64_t rows, int H, float floor_, uint8_t* codes, uint8_t* scales,
@@ -86,6 +87,7 @@ int ensure_device(cudaStream_t stream, DeviceState** out) {
 
 struct Plan {
   int path = 1;
+  bool tc_proj = false;  // streaming path: tcgen05 projection instead of warp-level MMA
   int BT = 8;   // tokens per CTA (split path)
   int Wd = 64;  // columns per CTA (split path)
 };
@@ -108,6 +110,8 @@ int make_plan(int64_t T, int H, const mhc_config* cfg, Plan* p) {
   if (c.sinkhorn_iters < 0 || c.sinkhorn_iters > 10000) return fail(MHC_ERR_CONFIG, "cfg.sinkhorn_iters out of range");
   if (!(c.amax_floor >= 0.f) || c.amax_floor > 1e30f) return fail(MHC_ERR_CONFIG, "cfg.amax_floor out of range");
   if (c.spin_limit < 0) return fail(MHC_ERR_CONFIG, "cfg.spin_limit must be >= 0");
+  if (c.projection < 0 || c.projection > 2) return fail(MHC_ERR_CONFIG, "cfg.projection must be 0, 1 or 2");
+  p->tc_proj = c.projection == 2;
   p->path = (c.path == 2 || (c.path == 0 && T >= kStreamMinT && mhc::stream_cols(H) > 0)) ? 2 : 1;
   if (p->path == 2) {
     if (mhc::stream_cols(H) == 0)
@@ -276,7 +280,7 @@ int mhc_seam(const void* R, const void* Y, const float* post_prev, const float* 
   if (plan.path == 2) {
     if (!fn_packed) return fail(MHC_ERR_NULL, "the streaming path needs fn_packed (mhc_pack_fn) or cfg.path = 1");
     if (T >= ((int64_t)1 << 31)) return fail(MHC_ERR_SHAPE, "the streaming path takes T < 2^31");
-    cudaError_t e = mhc::stream_launch(a, s, (unsigned long long)a.spin_limit * 100ull, &launches);
+    cudaError_t e = mhc::stream_launch(a, plan.tc_proj, s, (unsigned long long)a.spin_limit * 100ull, &launches);
     if (e == cudaErrorInvalidValue) return fail(MHC_ERR_CUDA, "tensor map encoding failed (streaming path)");
     if (e != cudaSuccess) return cuda_fail(e, "seam launch (streaming path)");
     g_launches = launches;

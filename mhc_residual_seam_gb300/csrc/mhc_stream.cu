@@ -119,7 +119,7 @@ __device__ __noinline__ void finish_store_gates(const SeamArgs& a, int64_t t, co
   store_gates(a, t, pre, post, cb);
 }
 
-template <bool POST, bool MXFP8>
+template <bool POST, bool MXFP8, bool MS>
 __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
     stream_seam_kernel(const SeamArgs a, const __grid_constant__ CUtensorMap tmR,
                        const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmRo,
@@ -145,11 +145,11 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < kNF; ++s) {
       mbar_init(&tl->fn_full[s], 1);
-      mbar_init(&tl->fn_empty[s], 1);
+      mbar_init(&tl->fn_empty[s], MS ? 8 : 1);
     }
     for (int s = 0; s < kNO; ++s) {
       mbar_init(&tl->out_full[s], 8);
-      mbar_init(&tl->out_empty[s], 2);
+      mbar_init(&tl->out_empty[s], MS ? 9 : 2);
     }
     mbar_init(&tl->d_full, 1);
     for (int p = 0; p < 2; ++p) {
@@ -177,7 +177,7 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tl->tmem_base;
 
-  const int nacc = nch <= kMaxChunks - 8 ? 4 : 2;  // independent accumulators (TMEM room permitting)
+  const int nacc = MS ? 0 : (nch <= kMaxChunks - 8 ? 4 : 2);  // tcgen05 accumulators (TMEM room permitting)
   const uint32_t colx = 32u * (uint32_t)nacc;       // x columns start after the accumulators
 
   if (warp == 8) {
@@ -223,6 +223,25 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
       for (int jj = (j > kNF ? j - kNF : 0); jj < j; ++jj) {
         if (!mbar_wait(&tl->fn_full[jj % kNF], (jj / kNF) & 1, limit_ns)) flag_error(X);
       }
+    }
+  } else if (warp == 9 && MS) {
+    // --------------------------------------------------- R' tile stores --
+    if (lane == 0) {
+      int j = 0;
+      for (int b = cid; b < n_blocks; b += ncl) {
+        const int t0 = b * kBM;
+        for (int c = 0; c < nch; ++c, ++j) {
+          const int o = j % kNO;
+          wait_local(X, &tl->out_full[o], (j / kNO) & 1);
+          const int h = hbase + c * kChunk;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) tma_store_3d(&tmRo, sm + kOffOut + o * kOutStage + i * kRTile, h, i, t0);
+          tma_store_commit();
+          tma_store_wait_read_all();
+          mbar_arrive(&tl->out_empty[o]);
+        }
+      }
+      tma_store_wait_all();
     }
   } else if (warp == 9) {
     // ------------------------------------- MMA issuer and R' tile stores --
@@ -300,6 +319,50 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t off = lane * 128 + ((warp ^ (lane & 7)) << 4);       // row = token, 16-byte chunk = warp
     const int per_phase = MXFP8 ? 5 : 8;                                // norm chunks staged per pass
     int j = 0, lb = 0;
+    // Warp-level tensor-core projection (MS): warp w owns stream w % 4 and the
+    // 32 columns [32 (w / 4), +32) of every chunk: D[32 tokens x 24 logits] +=
+    // R'[32 x 32] . (fn_hi + fn_lo)[32 x 24] as m16n8k16 MMAs with fp32
+    // accumulation, one chunk behind the R' writes of all eight warps.
+    float acc[2][3][4];
+    auto mma_chunk = [&](int jj) {
+      const int oo = jj % kNO, ff = jj % kNF;
+      wait_local(X, &tl->out_full[oo], (jj / kNO) & 1);
+      wait_local(X, &tl->fn_full[ff], (jj / kNF) & 1);
+      const uint32_t rt = smem_u32(sm + kOffOut + oo * kOutStage + (warp & 3) * kRTile);
+      const uint32_t ft = smem_u32(sm + kOffFn + ff * kFnStage + (warp & 3) * kFnTile);
+      const int mi = lane >> 3, rr = lane & 7;
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        const int kg = 2 * (warp >> 2) + kk;  // 16-column group of the chunk
+        uint32_t af[2][4], bq[3][4];
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          const int row = 16 * m + (mi & 1) * 8 + rr, ch = 2 * kg + (mi >> 1);
+          ldmatrix_x4(rt + row * 128 + ((ch ^ rr) << 4), af[m][0], af[m][1], af[m][2], af[m][3]);
+        }
+#pragma unroll
+        for (int pq = 0; pq < 3; ++pq) {  // fn rows 16 pq .. 16 pq + 15 (n8 tiles 2 pq, 2 pq + 1)
+          const int row = 16 * pq + (mi >> 1) * 8 + rr, ch = 2 * kg + (mi & 1);
+          ldmatrix_x4(ft + row * 128 + ((ch ^ rr) << 4), bq[pq][0], bq[pq][1], bq[pq][2], bq[pq][3]);
+        }
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+#pragma unroll
+          for (int n = 0; n < 3; ++n) {
+            const int th = n, tlo = 3 + n;  // hi and lo rows of logits 8n .. 8n + 7
+            mma_bf16_16816(acc[m][n], af[m][0], af[m][1], af[m][2], af[m][3], bq[th >> 1][2 * (th & 1)],
+                           bq[th >> 1][2 * (th & 1) + 1]);
+            mma_bf16_16816(acc[m][n], af[m][0], af[m][1], af[m][2], af[m][3], bq[tlo >> 1][2 * (tlo & 1)],
+                           bq[tlo >> 1][2 * (tlo & 1) + 1]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&tl->out_empty[oo]);
+        mbar_arrive(&tl->fn_empty[ff]);
+      }
+    };
     for (int b = cid; b < n_blocks; b += ncl, ++lb) {
       const int t0 = b * kBM;
       const int64_t t = (int64_t)t0 + lane;
@@ -325,6 +388,12 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
       float2 sR2 = make_float2(0.f, 0.f), sx2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int n = 0; n < 3; ++n)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[m][n][e] = 0.f;
       for (int c = 0; c < nch; ++c, ++j) {
         const int s = j % kNI, o = j % kNO;
         wait_local(X, &tl->in_full[s], (j / kNI) & 1);
@@ -371,13 +440,41 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tl->out_full[o]);
+        if (MS && c > 0) mma_chunk(j - 1);
       }
+      if (MS && nch > 0) mma_chunk(j - 1);
       tc_wait_st();
 
       // ------------------------------------------ block finish: partials --
       tl->red[warp][lane][0] = sR2.x + sR2.y;
       tl->red[warp][lane][1] = sx2.x + sx2.y;
-      if (warp < 4) {
+      if (MS) {
+        // the output ring is idle once the stores and MMAs of its last two
+        // chunks are done: it holds the eight warps' projection partials
+        wait_local(X, &tl->out_empty[j % kNO], ((j / kNO) & 1) ^ 1);
+        wait_local(X, &tl->out_empty[(j + 1) % kNO], (((j + 1) / kNO) & 1) ^ 1);
+        float* buf = reinterpret_cast<float*>(sm + kOffOut);  // [8 warps][32 tokens][24 logits]
+        const int g = lane >> 2, t4 = lane & 3;
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+#pragma unroll
+          for (int n = 0; n < 3; ++n) {
+            float* r0 = buf + ((size_t)warp * kBM + 16 * m + g) * 24 + 8 * n + 2 * t4;
+            r0[0] = acc[m][n][0];
+            r0[1] = acc[m][n][1];
+            r0[8 * 24] = acc[m][n][2];
+            r0[8 * 24 + 1] = acc[m][n][3];
+          }
+        }
+        named_bar_sync(1, kComputeThreads);
+        for (int idx = tid; idx < kBM * 24; idx += kComputeThreads) {
+          const int tok = idx / 24, k = idx - tok * 24;
+          float sum = 0.f;
+#pragma unroll
+          for (int w = 0; w < 8; ++w) sum += buf[((size_t)w * kBM + tok) * 24 + k];
+          tl->dmat[k][tok] = sum;
+        }
+      } else if (warp < 4) {
         float dv[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) dv[k] = 0.f;
@@ -410,7 +507,7 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 4; ++e) {
           const int k = k0 + e;
           if (k < 24) {
-            v[e] = tl->dmat[k][tok] + tl->dmat[24 + k][tok];
+            v[e] = MS ? tl->dmat[k][tok] : tl->dmat[k][tok] + tl->dmat[24 + k][tok];
           } else if (k < kParts) {
             float s = 0.f;
 #pragma unroll
@@ -501,20 +598,25 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------- host side --
-static void* stream_kernel_ptr(bool post, bool mxfp8) {
-  if (post) return mxfp8 ? (void*)stream_seam_kernel<true, true> : (void*)stream_seam_kernel<true, false>;
-  return mxfp8 ? (void*)stream_seam_kernel<false, true> : (void*)stream_seam_kernel<false, false>;
+template <bool MS>
+static void* stream_kernel_ptr_(bool post, bool mxfp8) {
+  if (post) return mxfp8 ? (void*)stream_seam_kernel<true, true, MS> : (void*)stream_seam_kernel<true, false, MS>;
+  return mxfp8 ? (void*)stream_seam_kernel<false, true, MS> : (void*)stream_seam_kernel<false, false, MS>;
+}
+static void* stream_kernel_ptr(bool post, bool mxfp8, bool ms) {
+  return ms ? stream_kernel_ptr_<true>(post, mxfp8) : stream_kernel_ptr_<false>(post, mxfp8);
 }
 
 size_t stream_smem_bytes() { return kSmemBytes; }
 
 cudaError_t stream_init() {
   for (int p = 0; p < 2; ++p)
-    for (int m = 0; m < 2; ++m) {
-      cudaError_t e =
-          cudaFuncSetAttribute(stream_kernel_ptr(p, m), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-      if (e != cudaSuccess) return e;
-    }
+    for (int m = 0; m < 2; ++m)
+      for (int v = 0; v < 2; ++v) {
+        cudaError_t e = cudaFuncSetAttribute(stream_kernel_ptr(p, m, v), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+      }
   return cudaSuccess;
 }
 
@@ -553,23 +655,25 @@ static bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void*
 
 // Clusters that fit at once, per device (queried once).
 static int max_clusters(void* kernel) {
-  static int cache[64] = {0};
+  static int cache[2][64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (cache[dev] > 0) return cache[dev];
+  const int v = kernel == stream_kernel_ptr(true, false, true) ? 0 : 1;
+  if (cache[v][dev] > 0) return cache[v][dev];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(kCl, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) return 0;
-  cache[dev] = n;
+  cache[v][dev] = n;
   return n;
 }
 
 // Returns cudaSuccess, or cudaErrorInvalidValue when a tensor map cannot be
 // encoded or no cluster fits (the caller reports it).
-cudaError_t stream_launch(const SeamArgs& a, cudaStream_t stream, unsigned long long limit_ns, int* launches) {
+cudaError_t stream_launch(const SeamArgs& a, bool tcgen05_proj, cudaStream_t stream, unsigned long long limit_ns,
+                          int* launches) {
   const int H = a.H;
   const int W = stream_cols(H);
   if (W == 0) return cudaErrorInvalidValue;
@@ -593,7 +697,7 @@ cudaError_t stream_launch(const SeamArgs& a, cudaStream_t stream, unsigned long 
   if (ok) ok = encode(&mC, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.codes ? (const void*)a.codes : (const void*)a.norm, d2,
                       sC, b2, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (!ok) return cudaErrorInvalidValue;
-  void* k = stream_kernel_ptr(a.Y != nullptr, a.codes != nullptr);
+  void* k = stream_kernel_ptr(a.Y != nullptr, a.codes != nullptr, !tcgen05_proj);
   const int n_blocks = (int)((a.T + kBM - 1) / kBM);
   const int fit = max_clusters(k);
   if (fit <= 0) return cudaErrorInvalidValue;

@@ -28,8 +28,9 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_config_struct_layout_matches_c():
-    assert C.sizeof(B.MhcConfig) == 32
+    assert C.sizeof(B.MhcConfig) == 40
     assert B.MhcConfig.spin_limit.offset == 24
+    assert B.MhcConfig.projection.offset == 32
 
 
 def _seam(L, **over):
@@ -92,7 +93,7 @@ def test_workspace_rules(L):
 
 def test_config_validation(L):
     for bad in (dict(path=5), dict(block_m=3), dict(block_m=64), dict(cols_per_cta=48), dict(spin_limit=-1),
-                dict(sinkhorn_iters=-2), dict(amax_floor=-1.0)):
+                dict(sinkhorn_iters=-2), dict(amax_floor=-1.0), dict(projection=3)):
         cfg = B.MhcConfig(**bad)
         assert _seam(L, cfg=C.byref(cfg)) == -10, bad
 

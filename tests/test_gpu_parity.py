@@ -307,3 +307,11 @@ def test_stream_requires_packed_fn_and_supported_width():
     with pytest.raises(B.MhcError) as e:
         run_gpu(d, cfg=B.MhcConfig(**STREAM))
     assert e.value.code == -2
+
+
+@pytest.mark.parametrize("proj", [1, 2])
+@pytest.mark.parametrize("T,H,mx,post", [(300, 5120, False, True), (97, 4096, True, True), (64, 7168, False, False)])
+def test_stream_projection_variants(proj, T, H, mx, post):
+    # 1 = warp-level tensor-core MMA in the compute warps, 2 = tcgen05 MMA into tensor memory
+    d = make_case(T, H, 7700 + T + proj, mxfp8=mx, post=post)
+    compare(d, to_host(run_gpu(d, cfg=B.MhcConfig(path=2, projection=proj))))
