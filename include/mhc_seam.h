@@ -78,9 +78,9 @@ typedef struct {
     int sinkhorn_iters;  /* Sinkhorn rounds; 0 = 20 */
     float amax_floor;    /* ue8m0 amax floor; 0 = 1e-10 */
     long long spin_limit;/* iteration cap of every device-side wait; 0 = default (about 1 s) */
-    int projection;      /* streaming path's gate projection: 0 = policy (1); 1 = warp-level
-                            tensor-core MMA (m16n8k16) in the compute warps; 2 = tcgen05 MMA
-                            issued by one thread into tensor memory */
+    int projection;      /* streaming path's gate projection: 0 = policy (2 when H <= 5120, else 1);
+                            1 = warp-level tensor-core MMA (m16n8k16) in the compute warps;
+                            2 = tcgen05 MMA issued by one thread into tensor memory (H <= 5120) */
 } mhc_config;
 
 /* Bytes of the per-stream workspace for a call of T tokens of width H with

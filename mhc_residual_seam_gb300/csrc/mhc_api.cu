@@ -19,6 +19,7 @@ cudaError_t split_launch(const SeamArgs& a, int BT, int Wd, int64_t groups_per_l
 // mhc_stream.cu
 cudaError_t stream_init();
 int stream_cols(int H);
+bool stream_tc_fits(int H);
 cudaError_t stream_launch(const SeamArgs& a, bool tcgen05_proj, cudaStream_t stream, unsigned long long limit_ns,
                           int* launches);
 // mhc_aux.cu
@@ -111,11 +112,13 @@ int make_plan(int64_t T, int H, const mhc_config* cfg, Plan* p) {
   if (!(c.amax_floor >= 0.f) || c.amax_floor > 1e30f) return fail(MHC_ERR_CONFIG, "cfg.amax_floor out of range");
   if (c.spin_limit < 0) return fail(MHC_ERR_CONFIG, "cfg.spin_limit must be >= 0");
   if (c.projection < 0 || c.projection > 2) return fail(MHC_ERR_CONFIG, "cfg.projection must be 0, 1 or 2");
-  p->tc_proj = c.projection == 2;
+  p->tc_proj = c.projection == 2 || (c.projection == 0 && mhc::stream_tc_fits(H));
   p->path = (c.path == 2 || (c.path == 0 && T >= kStreamMinT && mhc::stream_cols(H) > 0)) ? 2 : 1;
   if (p->path == 2) {
     if (mhc::stream_cols(H) == 0)
-      return fail(MHC_ERR_SHAPE, "the streaming path needs H a multiple of 64 with 512 <= H <= 7168");
+      return fail(MHC_ERR_SHAPE, "the streaming path needs H a multiple of 64 with 512 <= H <= 8192");
+    if (c.projection == 2 && !mhc::stream_tc_fits(H))
+      return fail(MHC_ERR_CONFIG, "the tcgen05 projection needs H <= 5120 (tensor memory holds x and the accumulator)");
     return MHC_OK;
   }
   if (T <= 8) {

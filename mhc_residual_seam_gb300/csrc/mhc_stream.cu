@@ -9,22 +9,27 @@
 //    into a ring of 2 fn stages (L2 evict-last: every cluster reuses them);
 //  - eight compute warps (thread = token, warp = 8-column slice; the swizzle
 //    makes the column reads conflict-free) read their inputs, release the
-//    input stage, post-mix in fp32, round R' to bf16 into a ring of 2 output
-//    stages, accumulate s_R and s_x, and store x in tensor memory;
-//  - one thread issues the gate projection on the tensor cores (tcgen05,
-//    D[64 x 32] += fn^T[64 x 64] . R'^T[64 x 32] per stream and 16-wide k
-//    step; rows 0..23 hi, 24..47 lo; fp32 accumulation in TMEM, one
-//    accumulator per stream so consecutive MMAs do not wait on each other)
-//    and TMA-stores the R' tiles.
+//    input stage, post-mix in fp32 (packed fp32x2 FMAs), round R' to bf16 into
+//    a ring of 2 output stages, accumulate s_R and s_x, keep x in tensor
+//    memory, and normalise the previous block's x of the same chunk into the
+//    same output stage;
+//  - the gate projection runs on the tensor cores, in one of two forms:
+//    tcgen05 (one thread issues 4 MMAs per chunk: A = the four R' tiles
+//    stacked [128 x 64], B = the four fn tiles side by side [192 x 64], so
+//    D[128 x 192] holds stream i's 32 x 48 block on its diagonal, in TMEM
+//    lanes 32 i.. and columns 48 i..; the off-diagonal products are wasted,
+//    but each MMA instruction costs the same whatever its size), or, where x
+//    leaves no room for that accumulator in tensor memory, warp-level m16n8k16
+//    MMAs in the compute warps;
+//  - a store warp TMA-stores the R' tiles and the norm tile of each stage
+//    (and computes the ue8m0 codes of the norm tile).
 // After the last chunk of a block each CTA sends its per-token partial sums
 // (24 projections, s_R, s_x) to the token's owner CTA through distributed
 // shared memory and arrives on the owner's barrier; the owner's finisher warp
-// returns rstd_x at once and then computes the gates; every CTA normalises its
-// x from tensor memory and TMA-stores the norm (and the ue8m0 codes), staging
-// the tiles in the output ring, which is idle at that point.  The producers
-// run ahead into the next block meanwhile.  ("[FlyDSL] Single-launch
-// Mega-mHC on gfx950", Kernel Architecture: split-K with a distributed finish;
-// here the cluster launch makes every CTA of a split co-resident.)
+// returns rstd_x at once and then computes the gates.  ("[FlyDSL]
+// Single-launch Mega-mHC on gfx950", Kernel Architecture: split-K with a
+// distributed finish; here the cluster launch makes every CTA of a split
+// co-resident.)
 //
 // Every wait is bounded; after the first wait that runs out, the CTA records
 // the error (bit 1 of the status word) and every later wait returns at once,
@@ -40,23 +45,27 @@ namespace {
 constexpr int kCl = 4;                 // CTAs per cluster
 constexpr int kBM = 32;                // tokens per block
 constexpr int kChunk = 64;             // columns per chunk
-constexpr int kNI = 6, kNF = 2, kNO = 2;
+constexpr int kNI = 5, kNF = 2, kNO = 2;
 constexpr int kComputeThreads = 256;   // warps 0-7
-constexpr int kThreads = 384;          // + warp 8 input producer, 9 MMA, 10 fn producer, 11 finisher
+constexpr int kThreads = 416;          // + 8 input producer, 9 MMA issuer, 10 fn producer, 11 finisher, 12 store
 constexpr int kFnRows = 48;
 constexpr uint32_t kRTile = kBM * 128;                 // 4 KB
 constexpr uint32_t kFnTile = kFnRows * 128;            // 6 KB
-constexpr uint32_t kFnStage = 4 * kFnTile;             // 24 KB
-constexpr uint32_t kOutStage = 4 * kRTile;             // 16 KB
-constexpr uint32_t kInStage = 5 * kRTile;              // 20 KB (R tiles 0-3, Y tile 4)
+constexpr uint32_t kFnStage = 4 * kFnTile;             // 24 KB: [192 x 64] bf16
+constexpr uint32_t kInStage = 5 * kRTile;              // 20 KB: R tiles 0-3, Y tile 4
+constexpr uint32_t kOffNormT = 4 * kRTile;             // output stage: R' tiles 0-3, then the norm tile,
+constexpr uint32_t kOffCodesT = 5 * kRTile;            //   then the codes tile [32 x 64] u8
+constexpr uint32_t kOutStage = 6 * kRTile;             // 24 KB
 constexpr uint32_t kOffFn = 0;
-constexpr uint32_t kOffOut = kOffFn + kNF * kFnStage;  // fn tile 3's extra A rows read into here
+constexpr uint32_t kOffOut = kOffFn + kNF * kFnStage;
 constexpr uint32_t kOffIn = kOffOut + kNO * kOutStage;
 constexpr uint32_t kOffTail = kOffIn + kNI * kInStage;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColD = 0;                          // accumulators: 32 columns (tokens) each
-constexpr int kMaxChunks = (int)((kTmemCols - 2 * 32) / 16);  // x: 16 columns per chunk after 2-4 accumulators
-constexpr uint32_t kIdesc = idesc_bf16_f32(64, kBM);
+constexpr uint32_t kColD = 0;                          // tcgen05 accumulator D[128 x 192]
+constexpr uint32_t kDCols = 4 * kFnRows;
+constexpr int kMaxChunksTC = (int)((kTmemCols - kDCols) / 16);  // x: 16 columns per chunk
+constexpr int kMaxChunks = (int)(kTmemCols / 16);
+constexpr uint32_t kIdesc = idesc_bf16_f32(128, kDCols);
 constexpr int kSlots = kBM / kCl;                      // tokens owned per CTA and block
 constexpr int kPartPad = 28;                           // 26 parts padded to 7 float4
 
@@ -66,7 +75,7 @@ struct Tail {
   uint32_t tmem_base;
   volatile int err;
   float red[8][kBM][2];                  // per compute warp: s_R, s_x of each token
-  float dmat[kFnRows][kBM];              // D rows (hi 0..23, lo 24..47) x tokens
+  float dmat[24][kBM];                   // projection of the block: logit x token (hi + lo)
   float recv[2][kCl][kSlots][kPartPad];  // [block parity][source CTA][owned token][part]
   float rstd[2][kBM];                    // [block parity][token]
 };
@@ -137,6 +146,7 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
   const int hbase = (int)rank * W;
   const int nch = (max(0, min(W, H - hbase)) + kChunk - 1) / kChunk;
   const int cid = blockIdx.x / kCl, ncl = gridDim.x / kCl;
+  const int nblk = cid < n_blocks ? (n_blocks - cid + ncl - 1) / ncl : 0;  // blocks of this cluster
 
   if (tid == 0) {
     for (int s = 0; s < kNI; ++s) {
@@ -162,11 +172,13 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 8 && lane == 0) {
     prefetch_tmap(&tmR);
     if (POST) prefetch_tmap(&tmY);
-    prefetch_tmap(&tmRo);
-    prefetch_tmap(&tmN);
   }
   if (warp == 10 && lane == 0) prefetch_tmap(&tmFn);
-  if (warp == 11 && lane == 0) prefetch_tmap(&tmC);
+  if (warp == 12 && lane == 0) {
+    prefetch_tmap(&tmRo);
+    prefetch_tmap(&tmN);
+    if (MXFP8) prefetch_tmap(&tmC);
+  }
   if (warp == 9) {
     tmem_alloc(&tl->tmem_base, kTmemCols);
     tmem_relinquish();
@@ -177,17 +189,14 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tl->tmem_base;
 
-  const int nacc = MS ? 0 : (nch <= kMaxChunks - 8 ? 4 : 2);  // tcgen05 accumulators (TMEM room permitting)
-  const uint32_t colx = 32u * (uint32_t)nacc;       // x columns start after the accumulators
-
   if (warp == 8) {
     // --------------------------------------------------- input producer --
     if (lane == 0) {
       const uint64_t pol = l2_evict_first();
       const uint32_t bytes = (POST ? 5 : 4) * kRTile;
       int j = 0;
-      for (int b = cid; b < n_blocks; b += ncl) {
-        const int t0 = b * kBM;
+      for (int lb = 0; lb < nblk; ++lb) {
+        const int t0 = (cid + lb * ncl) * kBM;
         for (int c = 0; c < nch; ++c, ++j) {
           const int s = j % kNI;
           wait_local(X, &tl->in_empty[s], ((j / kNI) & 1) ^ 1);
@@ -209,7 +218,7 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint64_t pol = l2_evict_last();
       int j = 0;
-      for (int b = cid; b < n_blocks; b += ncl) {
+      for (int lb = 0; lb < nblk; ++lb) {
         for (int c = 0; c < nch; ++c, ++j) {
           const int f = j % kNF;
           wait_local(X, &tl->fn_empty[f], ((j / kNF) & 1) ^ 1);
@@ -224,65 +233,87 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&tl->fn_full[jj % kNF], (jj / kNF) & 1, limit_ns)) flag_error(X);
       }
     }
-  } else if (warp == 9 && MS) {
-    // --------------------------------------------------- R' tile stores --
-    if (lane == 0) {
-      int j = 0;
-      for (int b = cid; b < n_blocks; b += ncl) {
-        const int t0 = b * kBM;
+  } else if (warp == 9) {
+    // -------------------------------------- tcgen05 projection (one thread) --
+    if (!MS && lane == 0) {
+      int j = 0, jr = 0;
+      for (int lb = 0; lb <= nblk; ++lb) {  // the last pass only normalises (no R')
+        const bool real = lb < nblk;
         for (int c = 0; c < nch; ++c, ++j) {
           const int o = j % kNO;
           wait_local(X, &tl->out_full[o], (j / kNO) & 1);
-          const int h = hbase + c * kChunk;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) tma_store_3d(&tmRo, sm + kOffOut + o * kOutStage + i * kRTile, h, i, t0);
-          tma_store_commit();
-          tma_store_wait_read_all();
-          mbar_arrive(&tl->out_empty[o]);
-        }
-      }
-      tma_store_wait_all();
-    }
-  } else if (warp == 9) {
-    // ------------------------------------- MMA issuer and R' tile stores --
-    if (lane == 0) {
-      int j = 0;
-      for (int b = cid; b < n_blocks; b += ncl) {
-        const int t0 = b * kBM;
-        for (int c = 0; c < nch; ++c, ++j) {
-          const int o = j % kNO, f = j % kNF;
-          wait_local(X, &tl->out_full[o], (j / kNO) & 1);
-          wait_local(X, &tl->fn_full[f], (j / kNF) & 1);
-          tc_fence_after();
-          const uint32_t fa = smem_u32(sm + kOffFn + f * kFnStage);
-          const uint32_t rb = smem_u32(sm + kOffOut + o * kOutStage);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int acc = i % nacc;
-              tc_mma_bf16(tmem + kColD + 32 * acc, sdesc_k_sw128(fa + i * kFnTile + kk * 32),
-                          sdesc_k_sw128(rb + i * kRTile + kk * 32), kIdesc, !(c == 0 && kk == 0 && i < nacc));
-            }
+          if (!real) {
+            mbar_arrive(&tl->out_empty[o]);
+            continue;
           }
+          const int f = jr % kNF;
+          wait_local(X, &tl->fn_full[f], (jr / kNF) & 1);
+          tc_fence_after();
+          const uint32_t ra = smem_u32(sm + kOffOut + o * kOutStage);   // R' of the 4 streams [128 x 64]
+          const uint32_t fb = smem_u32(sm + kOffFn + f * kFnStage);     // fn of the 4 streams [192 x 64]
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_bf16(tmem + kColD, sdesc_k_sw128(ra + kk * 32), sdesc_k_sw128(fb + kk * 32), kIdesc, (c | kk) != 0);
           tc_commit(&tl->fn_empty[f]);
           tc_commit(&tl->out_empty[o]);
           if (c == nch - 1) tc_commit(&tl->d_full);
-          const int h = hbase + c * kChunk;
+          ++jr;
+        }
+      }
+    }
+  } else if (warp == 12) {
+    // ---------------------------- stores: R' tiles, norm tile, ue8m0 codes --
+    int j = 0;
+    for (int lb = 0; lb <= nblk; ++lb) {
+      const bool real = lb < nblk, prev = lb > 0;
+      const int t0 = (cid + lb * ncl) * kBM, tp = (cid + (lb - 1) * ncl) * kBM;
+      for (int c = 0; c < nch; ++c, ++j) {
+        const int o = j % kNO;
+        uint8_t* ost = sm + kOffOut + o * kOutStage;
+        const int h = hbase + c * kChunk;
+        wait_local(X, &tl->out_full[o], (j / kNO) & 1);
+        if (MXFP8 && prev) {  // lane = token; two 32-column groups each
 #pragma unroll
-          for (int i = 0; i < 4; ++i) tma_store_3d(&tmRo, sm + kOffOut + o * kOutStage + i * kRTile, h, i, t0);
+          for (int half = 0; half < 2; ++half) {
+            uint32_t nb[16];
+#pragma unroll
+            for (int jq = 0; jq < 4; ++jq) {
+              const int ch = 4 * half + jq;
+              uint4 v = *reinterpret_cast<const uint4*>(ost + kOffNormT + lane * 128 + ((ch ^ (lane & 7)) << 4));
+              nb[4 * jq] = v.x; nb[4 * jq + 1] = v.y; nb[4 * jq + 2] = v.z; nb[4 * jq + 3] = v.w;
+            }
+            uint32_t cw[8];
+            const uint8_t sb = quant_group32(nb, cw, a.amax_floor);
+            uint4* cd = reinterpret_cast<uint4*>(ost + kOffCodesT + lane * 64 + 32 * half);
+            cd[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+            cd[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+            const int64_t tt = (int64_t)tp + lane;
+            if (tt < T) a.scales[tt * (H / 32) + (h + 32 * half) / 32] = sb;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        if (lane == 0) {
+          if (real) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) tma_store_3d(&tmRo, ost + i * kRTile, h, i, t0);
+          }
+          if (prev) {
+            tma_store_2d(&tmN, ost + kOffNormT, h, tp);
+            if (MXFP8) tma_store_2d(&tmC, ost + kOffCodesT, h, tp);
+          }
           tma_store_commit();
           tma_store_wait_read_all();
           mbar_arrive(&tl->out_empty[o]);
         }
+        __syncwarp();
       }
-      tma_store_wait_all();
     }
+    if (lane == 0) tma_store_wait_all();
   } else if (warp == 11) {
     // ----------------- finisher: rstd_x first, then the gates of 8 tokens --
-    int lb = 0;
-    for (int b = cid; b < n_blocks; b += ncl, ++lb) {
-      const int par = lb & 1;
+    for (int lb = 0; lb < nblk; ++lb) {
+      const int b = cid + lb * ncl, par = lb & 1;
       if (lane < kSlots) {
         wait_remote(X, &tl->recv_full[par], (lb >> 1) & 1);
         const int tok = (int)rank + kCl * lane;
@@ -311,23 +342,21 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     }
-  } else {
+  } else if (warp < 8) {
     // ---------------------------------------------------- compute warps --
     const int q = warp & 3, wq = warp >> 2;
+    const uint32_t colx = MS ? 0u : kDCols;
     const uint32_t xaddr = tmem + ((uint32_t)(32 * q) << 16) + colx + 8 * wq;
-    const uint32_t daddr = tmem + ((uint32_t)(32 * warp) << 16) + kColD;  // warps 0-3
-    const uint32_t off = lane * 128 + ((warp ^ (lane & 7)) << 4);       // row = token, 16-byte chunk = warp
-    const int per_phase = MXFP8 ? 5 : 8;                                // norm chunks staged per pass
-    int j = 0, lb = 0;
-    // Warp-level tensor-core projection (MS): warp w owns stream w % 4 and the
-    // 32 columns [32 (w / 4), +32) of every chunk: D[32 tokens x 24 logits] +=
-    // R'[32 x 32] . (fn_hi + fn_lo)[32 x 24] as m16n8k16 MMAs with fp32
-    // accumulation, one chunk behind the R' writes of all eight warps.
+    const uint32_t off = lane * 128 + ((warp ^ (lane & 7)) << 4);  // row = token, 16-byte chunk = warp
+    // Warp-level projection (MS): warp w owns stream w % 4 and the 32 columns
+    // [32 (w / 4), +32) of every chunk: D[32 tokens x 24 logits] += R'[32 x 32]
+    // . (fn_hi + fn_lo)[32 x 24], m16n8k16 MMAs with fp32 accumulation, one
+    // chunk behind the R' writes of all eight warps.
     float acc[2][3][4];
-    auto mma_chunk = [&](int jj) {
-      const int oo = jj % kNO, ff = jj % kNF;
+    auto mma_chunk = [&](int jj, int jr) {
+      const int oo = jj % kNO, ff = jr % kNF;
       wait_local(X, &tl->out_full[oo], (jj / kNO) & 1);
-      wait_local(X, &tl->fn_full[ff], (jj / kNF) & 1);
+      wait_local(X, &tl->fn_full[ff], (jr / kNF) & 1);
       const uint32_t rt = smem_u32(sm + kOffOut + oo * kOutStage + (warp & 3) * kRTile);
       const uint32_t ft = smem_u32(sm + kOffFn + ff * kFnStage + (warp & 3) * kFnTile);
       const int mi = lane >> 3, rr = lane & 7;
@@ -363,30 +392,37 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_arrive(&tl->fn_empty[ff]);
       }
     };
-    for (int b = cid; b < n_blocks; b += ncl, ++lb) {
-      const int t0 = b * kBM;
-      const int64_t t = (int64_t)t0 + lane;
+
+    // carried gates of the next block, fetched one block ahead
+    float4 gc[4], gp = make_float4(0.f, 0.f, 0.f, 0.f), gq = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto fetch_gates = [&](int lb) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) gc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      gp = gq = make_float4(0.f, 0.f, 0.f, 0.f);
+      const int64_t t = (int64_t)(cid + lb * ncl) * kBM + lane;
+      if (lb < nblk && t < T) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) gc[k] = __ldg(reinterpret_cast<const float4*>(a.comb_prev + t * 16) + k);
+        gp = __ldg(reinterpret_cast<const float4*>(a.pre_prev + t * 4));
+        if (POST) gq = __ldg(reinterpret_cast<const float4*>(a.post_prev + t * 4));
+      }
+    };
+    fetch_gates(0);
+
+    int j = 0, ji = 0;
+    float rprev = 0.f;
+    for (int lb = 0; lb <= nblk; ++lb) {  // the last pass only normalises the last block
+      const bool real = lb < nblk, prev = lb > 0;
       float2 comb2[16], post2[4], pre2[4];  // each gate duplicated for the fp32x2 FMAs
 #pragma unroll
-      for (int k = 0; k < 16; ++k) comb2[k] = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) post2[k] = pre2[k] = make_float2(0.f, 0.f);
-      if (t < T) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          float4 v = __ldg(reinterpret_cast<const float4*>(a.comb_prev + t * 16) + k);
-          comb2[4 * k] = make_float2(v.x, v.x); comb2[4 * k + 1] = make_float2(v.y, v.y);
-          comb2[4 * k + 2] = make_float2(v.z, v.z); comb2[4 * k + 3] = make_float2(v.w, v.w);
-        }
-        float4 p = __ldg(reinterpret_cast<const float4*>(a.pre_prev + t * 4));
-        pre2[0] = make_float2(p.x, p.x); pre2[1] = make_float2(p.y, p.y);
-        pre2[2] = make_float2(p.z, p.z); pre2[3] = make_float2(p.w, p.w);
-        if (POST) {
-          float4 v = __ldg(reinterpret_cast<const float4*>(a.post_prev + t * 4));
-          post2[0] = make_float2(v.x, v.x); post2[1] = make_float2(v.y, v.y);
-          post2[2] = make_float2(v.z, v.z); post2[3] = make_float2(v.w, v.w);
-        }
+      for (int k = 0; k < 4; ++k) {
+        comb2[4 * k] = make_float2(gc[k].x, gc[k].x); comb2[4 * k + 1] = make_float2(gc[k].y, gc[k].y);
+        comb2[4 * k + 2] = make_float2(gc[k].z, gc[k].z); comb2[4 * k + 3] = make_float2(gc[k].w, gc[k].w);
       }
+      pre2[0] = make_float2(gp.x, gp.x); pre2[1] = make_float2(gp.y, gp.y);
+      pre2[2] = make_float2(gp.z, gp.z); pre2[3] = make_float2(gp.w, gp.w);
+      post2[0] = make_float2(gq.x, gq.x); post2[1] = make_float2(gq.y, gq.y);
+      post2[2] = make_float2(gq.z, gq.z); post2[3] = make_float2(gq.w, gq.w);
       float2 sR2 = make_float2(0.f, 0.f), sx2 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int m = 0; m < 2; ++m)
@@ -394,66 +430,98 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
         for (int n = 0; n < 3; ++n)
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc[m][n][e] = 0.f;
+
       for (int c = 0; c < nch; ++c, ++j) {
-        const int s = j % kNI, o = j % kNO;
-        wait_local(X, &tl->in_full[s], (j / kNI) & 1);
-        const uint8_t* st = sm + kOffIn + s * kInStage;
-        uint4 rin[4], yin = make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) rin[i] = *reinterpret_cast<const uint4*>(st + i * kRTile + off);
-        if (POST) yin = *reinterpret_cast<const uint4*>(st + 4 * kRTile + off);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tl->in_empty[s]);
-        // Two columns at a time with packed fp32x2 FMAs (each half rounds
-        // exactly like a scalar FMA).
+        const int o = j % kNO;
         uint32_t ow[4][4];
         float x[8];
+        if (real) {
+          const int s = ji % kNI;
+          wait_local(X, &tl->in_full[s], (ji / kNI) & 1);
+          const uint8_t* st = sm + kOffIn + s * kInStage;
+          uint4 rin[4], yin = make_uint4(0, 0, 0, 0);
 #pragma unroll
-        for (int wd = 0; wd < 4; ++wd) {
-          const float2 r0 = bf16pair((&rin[0].x)[wd]), r1 = bf16pair((&rin[1].x)[wd]);
-          const float2 r2 = bf16pair((&rin[2].x)[wd]), r3 = bf16pair((&rin[3].x)[wd]);
-          const float2 yy = bf16pair((&yin.x)[wd]);
-          float2 xx = make_float2(0.f, 0.f);
+          for (int i = 0; i < 4; ++i) rin[i] = *reinterpret_cast<const uint4*>(st + i * kRTile + off);
+          if (POST) yin = *reinterpret_cast<const uint4*>(st + 4 * kRTile + off);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tl->in_empty[s]);
+          ++ji;
+          // two columns at a time with packed fp32x2 FMAs (each half rounds like a scalar FMA)
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            float2 v = __fmul2_rn(comb2[4 * i], r0);
-            v = __ffma2_rn(comb2[4 * i + 1], r1, v);
-            v = __ffma2_rn(comb2[4 * i + 2], r2, v);
-            v = __ffma2_rn(comb2[4 * i + 3], r3, v);
-            if (POST) v = __ffma2_rn(post2[i], yy, v);
-            const uint32_t w = pack_bf16x2(v.x, v.y);
-            ow[i][wd] = w;
-            const float2 rr = bf16pair(w);
-            sR2 = __ffma2_rn(rr, rr, sR2);
-            xx = __ffma2_rn(pre2[i], rr, xx);
+          for (int wd = 0; wd < 4; ++wd) {
+            const float2 r0 = bf16pair((&rin[0].x)[wd]), r1 = bf16pair((&rin[1].x)[wd]);
+            const float2 r2 = bf16pair((&rin[2].x)[wd]), r3 = bf16pair((&rin[3].x)[wd]);
+            const float2 yy = bf16pair((&yin.x)[wd]);
+            float2 xx = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              float2 v = __fmul2_rn(comb2[4 * i], r0);
+              v = __ffma2_rn(comb2[4 * i + 1], r1, v);
+              v = __ffma2_rn(comb2[4 * i + 2], r2, v);
+              v = __ffma2_rn(comb2[4 * i + 3], r3, v);
+              if (POST) v = __ffma2_rn(post2[i], yy, v);
+              const uint32_t w = pack_bf16x2(v.x, v.y);
+              ow[i][wd] = w;
+              const float2 rr2 = bf16pair(w);
+              sR2 = __ffma2_rn(rr2, rr2, sR2);
+              xx = __ffma2_rn(pre2[i], rr2, xx);
+            }
+            x[2 * wd] = xx.x;
+            x[2 * wd + 1] = xx.y;
+            sx2 = __ffma2_rn(xx, xx, sx2);
           }
-          x[2 * wd] = xx.x;
-          x[2 * wd + 1] = xx.y;
-          sx2 = __ffma2_rn(xx, xx, sx2);
+        }
+        if (prev && c == 0) {  // rstd_x of the previous block, sent back by the owners
+          const int pp = (lb - 1) & 1;
+          wait_remote(X, &tl->rstd_full[pp], ((lb - 1) >> 1) & 1);
+          rprev = tl->rstd[pp][lane];
         }
         wait_local(X, &tl->out_empty[o], ((j / kNO) & 1) ^ 1);
         uint8_t* ost = sm + kOffOut + o * kOutStage;
+        if (real) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          *reinterpret_cast<uint4*>(ost + i * kRTile + off) = make_uint4(ow[i][0], ow[i][1], ow[i][2], ow[i][3]);
-        tc_st_x8(xaddr + 16 * c, x);
+          for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<uint4*>(ost + i * kRTile + off) = make_uint4(ow[i][0], ow[i][1], ow[i][2], ow[i][3]);
+        }
+        if (prev) {  // norm of the previous block's x in these columns, before x is overwritten
+          float xv[8], gm[8];
+          tc_ld_x8(xaddr + 16 * c, xv);
+          unpack8(__ldg(reinterpret_cast<const uint4*>(a.gamma + hbase + c * kChunk + 8 * warp)), gm);
+          uint4 nv;
+          nv.x = pack_bf16x2(xv[0] * rprev * gm[0], xv[1] * rprev * gm[1]);
+          nv.y = pack_bf16x2(xv[2] * rprev * gm[2], xv[3] * rprev * gm[3]);
+          nv.z = pack_bf16x2(xv[4] * rprev * gm[4], xv[5] * rprev * gm[5]);
+          nv.w = pack_bf16x2(xv[6] * rprev * gm[6], xv[7] * rprev * gm[7]);
+          *reinterpret_cast<uint4*>(ost + kOffNormT + off) = nv;
+        }
+        if (real) tc_st_x8(xaddr + 16 * c, x);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tl->out_full[o]);
-        if (MS && c > 0) mma_chunk(j - 1);
+        if (MS) {
+          if (real && c > 0) mma_chunk(j - 1, ji - 2);
+          if (!real) {  // no projection in the normalise-only pass: release the stage
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tl->out_empty[o]);
+          }
+        }
       }
-      if (MS && nch > 0) mma_chunk(j - 1);
+      if (!real) break;
+      if (MS && nch > 0) mma_chunk(j - 1, ji - 1);
       tc_wait_st();
+      fetch_gates(lb + 1);
 
       // ------------------------------------------ block finish: partials --
       tl->red[warp][lane][0] = sR2.x + sR2.y;
       tl->red[warp][lane][1] = sx2.x + sx2.y;
+      // the output ring is idle once the stores (and projections) of its last
+      // two chunks are done: it stages the projection partials
+      wait_local(X, &tl->out_empty[j % kNO], ((j / kNO) & 1) ^ 1);
+      wait_local(X, &tl->out_empty[(j + 1) % kNO], (((j + 1) / kNO) & 1) ^ 1);
+      float* buf = reinterpret_cast<float*>(sm + kOffOut);  // [warps][32 tokens][24 logits]
+      int nparts;
       if (MS) {
-        // the output ring is idle once the stores and MMAs of its last two
-        // chunks are done: it holds the eight warps' projection partials
-        wait_local(X, &tl->out_empty[j % kNO], ((j / kNO) & 1) ^ 1);
-        wait_local(X, &tl->out_empty[(j + 1) % kNO], (((j + 1) / kNO) & 1) ^ 1);
-        float* buf = reinterpret_cast<float*>(sm + kOffOut);  // [8 warps][32 tokens][24 logits]
+        nparts = 8;
         const int g = lane >> 2, t4 = lane & 3;
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
@@ -466,38 +534,33 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
             r0[8 * 24 + 1] = acc[m][n][3];
           }
         }
-        named_bar_sync(1, kComputeThreads);
-        for (int idx = tid; idx < kBM * 24; idx += kComputeThreads) {
-          const int tok = idx / 24, k = idx - tok * 24;
-          float sum = 0.f;
+      } else {
+        nparts = 4;
+        if (warp < 4) {  // stream q = warp: TMEM lanes 32 q .., columns 48 q .. 48 q + 47
+          float dv[48];
+          if (nch > 0) {
+            wait_local(X, &tl->d_full, lb & 1);
+            tc_fence_after();
 #pragma unroll
-          for (int w = 0; w < 8; ++w) sum += buf[((size_t)w * kBM + tok) * 24 + k];
-          tl->dmat[k][tok] = sum;
-        }
-      } else if (warp < 4) {
-        float dv[32];
+            for (int k = 0; k < 6; ++k)
+              tc_ld_x8(tmem + ((uint32_t)(32 * warp) << 16) + kColD + 48 * warp + 8 * k, dv + 8 * k);
+          } else {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) dv[k] = 0.f;
-        if (nch > 0) {
-          wait_local(X, &tl->d_full, lb & 1);
-          tc_fence_after();
-          for (int acc = 0; acc < nacc; ++acc) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              float v[8];
-              tc_ld_x8(daddr + 32 * acc + 8 * k, v);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) dv[8 * k + e] += v[e];
-            }
+            for (int k = 0; k < 48; ++k) dv[k] = 0.f;
           }
-        }
-        const int m = 16 * warp + lane;  // M = 64 accumulator: row m in lane 32 (m / 16) + m % 16
-        if (lane < 16 && m < kFnRows) {
+          float* r0 = buf + ((size_t)warp * kBM + lane) * 24;
 #pragma unroll
-          for (int n = 0; n < kBM; ++n) tl->dmat[m][n] = dv[n];
+          for (int k = 0; k < 24; ++k) r0[k] = dv[k] + dv[24 + k];
         }
       }
       tc_fence_before();
+      named_bar_sync(1, kComputeThreads);
+      for (int idx = tid; idx < kBM * 24; idx += kComputeThreads) {
+        const int tok = idx / 24, k = idx - tok * 24;
+        float sum = 0.f;
+        for (int w = 0; w < nparts; ++w) sum += buf[((size_t)w * kBM + tok) * 24 + k];
+        tl->dmat[k][tok] = sum;
+      }
       named_bar_sync(1, kComputeThreads);
       const int par = lb & 1;
       if (tid < kBM * (kPartPad / 4)) {  // one 16-byte remote store per (token, 4 parts)
@@ -507,12 +570,12 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 4; ++e) {
           const int k = k0 + e;
           if (k < 24) {
-            v[e] = MS ? tl->dmat[k][tok] : tl->dmat[k][tok] + tl->dmat[24 + k][tok];
+            v[e] = tl->dmat[k][tok];
           } else if (k < kParts) {
-            float s = 0.f;
+            float sum = 0.f;
 #pragma unroll
-            for (int w = 0; w < 8; ++w) s += tl->red[w][tok][k - 24];
-            v[e] = s;
+            for (int w = 0; w < 8; ++w) sum += tl->red[w][tok][k - 24];
+            v[e] = sum;
           } else {
             v[e] = 0.f;
           }
@@ -523,69 +586,7 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
       fence_acq_rel_cluster();
       named_bar_sync(1, kComputeThreads);
       if (tid < kCl) mbar_arrive_remote(mapa_shared(smem_u32(&tl->recv_full[par]), tid));
-
-      // -------------------------------------------- norm (and ue8m0) out --
-      // The output ring is idle once the MMA thread is done with the last two
-      // chunks of this block; the norm tiles are staged there.
-      wait_local(X, &tl->out_empty[j % kNO], ((j / kNO) & 1) ^ 1);
-      wait_local(X, &tl->out_empty[(j + 1) % kNO], (((j + 1) / kNO) & 1) ^ 1);
-      wait_remote(X, &tl->rstd_full[par], (lb >> 1) & 1);
-      const float r = tl->rstd[par][lane];
-      uint8_t* nbase = sm + kOffOut;
-      for (int c0 = 0; c0 < nch; c0 += per_phase) {
-        const int cn = min(per_phase, nch - c0);
-        if (c0 > 0) {
-          if (tid == 0) tma_store_wait_read_all();
-          named_bar_sync(1, kComputeThreads);
-        }
-        for (int cc = 0; cc < cn; ++cc) {
-          const int c = c0 + cc;
-          float xv[8], gm[8];
-          tc_ld_x8(xaddr + 16 * c, xv);
-          unpack8(__ldg(reinterpret_cast<const uint4*>(a.gamma + hbase + c * kChunk + 8 * warp)), gm);
-          uint4 ov;
-          ov.x = pack_bf16x2(xv[0] * r * gm[0], xv[1] * r * gm[1]);
-          ov.y = pack_bf16x2(xv[2] * r * gm[2], xv[3] * r * gm[3]);
-          ov.z = pack_bf16x2(xv[4] * r * gm[4], xv[5] * r * gm[5]);
-          ov.w = pack_bf16x2(xv[6] * r * gm[6], xv[7] * r * gm[7]);
-          *reinterpret_cast<uint4*>(nbase + cc * kRTile + off) = ov;
-        }
-        if (MXFP8) {
-          named_bar_sync(1, kComputeThreads);
-          for (int g = tid; g < 2 * kBM * cn; g += kComputeThreads) {  // (token, 32-column group)
-            const int tok = g & (kBM - 1), half = (g >> 5) & 1, cc = g >> 6;
-            const uint8_t* nt = nbase + cc * kRTile;
-            uint32_t nb[16];
-#pragma unroll
-            for (int jq = 0; jq < 4; ++jq) {
-              const int ch = 4 * half + jq;
-              uint4 v = *reinterpret_cast<const uint4*>(nt + tok * 128 + ((ch ^ (tok & 7)) << 4));
-              nb[4 * jq] = v.x; nb[4 * jq + 1] = v.y; nb[4 * jq + 2] = v.z; nb[4 * jq + 3] = v.w;
-            }
-            uint32_t cw[8];
-            const uint8_t sb = quant_group32(nb, cw, a.amax_floor);
-            uint4* cd = reinterpret_cast<uint4*>(nbase + per_phase * kRTile + cc * (kBM * 64) + tok * 64 + 32 * half);
-            cd[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-            cd[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-            const int64_t tt = (int64_t)t0 + tok;
-            if (tt < T) a.scales[tt * (H / 32) + (hbase + (c0 + cc) * kChunk + 32 * half) / 32] = sb;
-          }
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(1, kComputeThreads);
-        if (tid == 0) {
-          for (int cc = 0; cc < cn; ++cc) {
-            tma_store_2d(&tmN, nbase + cc * kRTile, hbase + (c0 + cc) * kChunk, t0);
-            if (MXFP8) tma_store_2d(&tmC, nbase + per_phase * kRTile + cc * (kBM * 64), hbase + (c0 + cc) * kChunk, t0);
-          }
-          tma_store_commit();
-        }
-      }
-      // the output ring is handed back to the next block once the norm stores have read it
-      if (tid == 0) tma_store_wait_read_all();
-      named_bar_sync(1, kComputeThreads);
     }
-    if (tid == 0) tma_store_wait_all();
   }
 
   tc_fence_before();
@@ -628,6 +629,13 @@ int stream_cols(int H) {
   return chunks * kChunk;
 }
 
+// Whether the tcgen05 projection fits: its accumulator and x share the 512
+// tensor-memory columns.
+bool stream_tc_fits(int H) {
+  const int W = stream_cols(H);
+  return W > 0 && W / kChunk <= kMaxChunksTC;
+}
+
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -658,7 +666,10 @@ static int max_clusters(void* kernel) {
   static int cache[2][64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  const int v = kernel == stream_kernel_ptr(true, false, true) ? 0 : 1;
+  const int v = (kernel == stream_kernel_ptr(true, false, true) || kernel == stream_kernel_ptr(true, true, true) ||
+                 kernel == stream_kernel_ptr(false, false, true) || kernel == stream_kernel_ptr(false, true, true))
+                    ? 0
+                    : 1;
   if (cache[v][dev] > 0) return cache[v][dev];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(kCl, 1, 1);
