@@ -152,12 +152,13 @@ def run_ours(args, w: dict, rank: int, world: int, local_rank: int) -> dict | No
     T, H = w["T"], w["H"]
     mx = w["out"] == "mxfp8"
     mode = B.MHC_OUT_MXFP8 if mx else B.MHC_OUT_BF16
-    out = B.alloc_outputs(T, H, mode, device)
     stream = torch.cuda.current_stream(device)
     g["fn_packed"] = torch.empty(B.mhc_packed_fn_bytes(H) // 2, dtype=torch.bfloat16, device=device)
     B.mhc_pack_fn(g["fn"], g["fn_packed"], stream=stream)  # once per weight update, outside the timed region
 
-    cfg = B.MhcConfig(projection={"auto": 0, "mma": 1, "tcgen05": 2}[args.projection])
+    cfg = B.MhcConfig(projection={"auto": 0, "mma": 1, "tcgen05": 2}[args.projection],
+                      path={"auto": 0, "split": 1, "stream": 2}[args.path])
+    out = B.alloc_outputs(T, H, mode, device, cfg)
 
     def step():
         B.mhc_seam(g["R"], g["Y"], g["post_prev"], g["comb_prev"], g["pre_prev"], g["fn"], g["fn_packed"], g["bias"],
@@ -170,6 +171,20 @@ def run_ours(args, w: dict, rank: int, world: int, local_rank: int) -> dict | No
     torch.cuda.synchronize(device)
     launches = B.mhc_last_launch_count()
     B.mhc_check_status(out["workspace"])
+    run_step = step
+    if args.graph:
+        gstream = torch.cuda.Stream(device)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(gstream):
+            with torch.cuda.graph(graph, stream=gstream):
+                B.mhc_seam(g["R"], g["Y"], g["post_prev"], g["comb_prev"], g["pre_prev"], g["fn"], g["fn_packed"],
+                           g["bias"], g["alpha"], g["gamma"], wl["eps"], mode, out["residual_out"], out["norm"],
+                           out["fp8_codes"], out["e8m0_scales"], out["pre_out"], out["post_out"], out["comb_out"],
+                           out["workspace"], cfg=cfg, stream=gstream)
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize(device)
+        run_step = graph.replay
 
     sampler = ClockSampler(local_rank)
     sampler.start()
@@ -180,7 +195,7 @@ def run_ours(args, w: dict, rank: int, world: int, local_rank: int) -> dict | No
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
     for _ in range(args.steps):
-        step()
+        run_step()
     ev1.record(stream)
     torch.cuda.synchronize(device)
     if world > 1:
@@ -283,6 +298,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--projection", choices=["auto", "mma", "tcgen05"], default="auto",
                     help="streaming path's gate projection (auto = the library's policy)")
+    ap.add_argument("--path", choices=["auto", "split", "stream"], default="auto",
+                    help="kernel path (auto = the library's policy)")
+    ap.add_argument("--graph", action="store_true",
+                    help="time replays of a CUDA graph holding one seam call (as the pages time small T)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -294,7 +313,8 @@ def main():
     config = {"workload": args.workload, "T": w["T"], "H": w["H"], "n_hc": 4,
               "form": "post" if w["post"] else "no_post", "out": w["out"],
               "tokens_per_rank": w["T"], "parallelism": f"token-shard x{args.gpus} (independent)",
-              "projection": args.projection,
+              "projection": args.projection, "path": args.path,
+              "timing": "cuda-graph replay" if args.graph else "back-to-back launches",
               "l2": "inputs larger than L2" if ACC.seam_bytes(w["T"], w["H"], w["post"], w["out"]) > 2 * L2_BYTES
               else "inputs smaller than L2 (warm)"}
 
