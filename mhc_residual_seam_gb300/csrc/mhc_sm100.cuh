@@ -198,6 +198,22 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t caddr, float4 v) {
                "f"(v.w)
                : "memory");
 }
+// Asynchronous stores into a cluster peer's shared memory: each completes its
+// byte count on the peer's mbarrier `cbar` (both addresses from mapa), so the
+// peer sees the data once that barrier's phase completes; no fence needed.
+__device__ __forceinline__ void st_async_f32(uint32_t caddr, float v, uint32_t cbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(caddr), "f"(v),
+               "r"(cbar)
+               : "memory");
+}
+__device__ __forceinline__ void st_async_v2(uint32_t caddr, float v0, float v1, uint32_t cbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(caddr),
+               "f"(v0), "f"(v1), "r"(cbar)
+               : "memory");
+}
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t threads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t caddr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
 }

@@ -23,13 +23,16 @@
 //    MMAs in the compute warps;
 //  - a store warp TMA-stores the R' tiles and the norm tile of each stage
 //    (and computes the ue8m0 codes of the norm tile).
-// After the last chunk of a block each CTA sends its per-token partial sums
-// (24 projections, s_R, s_x) to the token's owner CTA through distributed
-// shared memory and arrives on the owner's barrier; the owner's finisher warp
-// returns rstd_x at once and then computes the gates.  ("[FlyDSL]
-// Single-launch Mega-mHC on gfx950", Kernel Architecture: split-K with a
-// distributed finish; here the cluster launch makes every CTA of a split
-// co-resident.)
+// After the last chunk of a block each CTA sends, through distributed shared
+// memory (st.async completing bytes on the receiver's mbarrier):
+//  - its per-token s_x partials to all four CTAs, which each sum the four in
+//    the same order into rstd_x, needed by the first chunk of the next block;
+//  - its 24 projection partials and s_R of each token to the token's owner
+//    CTA (token % 4), whose finisher warp computes the gates off the critical
+//    path.
+// ("[FlyDSL] Single-launch Mega-mHC on gfx950", Kernel Architecture: split-K
+// with a distributed finish; here the cluster launch makes every CTA of a
+// split co-resident.)
 //
 // Every wait is bounded; after the first wait that runs out, the CTA records
 // the error (bit 1 of the status word) and every later wait returns at once,
@@ -67,20 +70,25 @@ constexpr int kMaxChunksTC = (int)((kTmemCols - kDCols) / 16);  // x: 16 columns
 constexpr int kMaxChunks = (int)(kTmemCols / 16);
 constexpr uint32_t kIdesc = idesc_bf16_f32(128, kDCols);
 constexpr int kSlots = kBM / kCl;                      // tokens owned per CTA and block
-constexpr int kPartPad = 28;                           // 26 parts padded to 7 float4
+constexpr int kOwnerParts = 25;                        // sent to a token's owner: 24 projections, s_R
+constexpr int kPartPad = 26;                           // rows of 8-byte aligned pairs
+constexpr int kDPad = 25;                              // odd row stride: conflict-free columns
+constexpr uint32_t kXsBytes = kCl * kBM * 4;           // s_x partials landing in each CTA per block
+constexpr uint32_t kRecvBytes = kCl * kSlots * kOwnerParts * 4;  // owner partials per CTA per block
 
 struct Tail {
   uint64_t in_full[kNI], in_empty[kNI], fn_full[kNF], fn_empty[kNF], out_full[kNO], out_empty[kNO];
-  uint64_t d_full, recv_full[2], rstd_full[2];
+  uint64_t d_full, xs_full[2], recv_full[2], recv_free[2];
   uint32_t tmem_base;
   volatile int err;
-  float red[8][kBM][2];                  // per compute warp: s_R, s_x of each token
-  float dmat[24][kBM];                   // projection of the block: logit x token (hi + lo)
+  float2 red[2][8][kBM];                 // [block parity][compute warp][token]: s_R, s_x partials
+  float dbuf[4][kBM][kDPad];             // the block's projection per stream (hi + lo): [stream][token][logit]
+  float xs[2][kCl][kBM];                 // [block parity][source CTA][token]: s_x partial
   float recv[2][kCl][kSlots][kPartPad];  // [block parity][source CTA][owned token][part]
-  float rstd[2][kBM];                    // [block parity][token]
 };
 
 constexpr size_t kSmemBytes = kOffTail + sizeof(Tail) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory of the streaming kernel exceeds 227 KB");
 
 struct Ctx {
   const SeamArgs* a;
@@ -163,8 +171,9 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
     }
     mbar_init(&tl->d_full, 1);
     for (int p = 0; p < 2; ++p) {
-      mbar_init(&tl->recv_full[p], kCl);
-      mbar_init(&tl->rstd_full[p], kCl);
+      mbar_init(&tl->xs_full[p], 1);    // + kXsBytes of st.async from the cluster
+      mbar_init(&tl->recv_full[p], 1);  // + kRecvBytes of st.async from the cluster
+      mbar_init(&tl->recv_free[p], kCl);
     }
     tl->err = 0;
     mbar_fence_init();
@@ -311,33 +320,28 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
     }
     if (lane == 0) tma_store_wait_all();
   } else if (warp == 11) {
-    // ----------------- finisher: rstd_x first, then the gates of 8 tokens --
+    // ---------------------------------------- finisher: gates of 8 tokens --
+    // The owner partials of block lb land by st.async on recv_full[lb & 1];
+    // once read, every CTA is told the slot is free (recv_free) so that the
+    // partials of block lb + 2 may overwrite it.
     for (int lb = 0; lb < nblk; ++lb) {
       const int b = cid + lb * ncl, par = lb & 1;
+      if (lane == 0) mbar_arrive_expect_tx(&tl->recv_full[par], kRecvBytes);
+      wait_local(X, &tl->recv_full[par], (lb >> 1) & 1);
+      float p[kOwnerParts];
       if (lane < kSlots) {
-        wait_remote(X, &tl->recv_full[par], (lb >> 1) & 1);
-        const int tok = (int)rank + kCl * lane;
-        const int64_t tt = (int64_t)b * kBM + tok;
-        float sx = 0.f;
 #pragma unroll
-        for (int src = 0; src < kCl; ++src) sx += tl->recv[par][src][lane][25];
-        const float r = tt < T ? 1.0f / sqrtf(sx / (float)H + a.eps) : 0.f;
-#pragma unroll
-        for (int dst = 0; dst < kCl; ++dst) st_cluster_f32(mapa_shared(smem_u32(&tl->rstd[par][tok]), dst), r);
-        fence_acq_rel_cluster();
-      }
-      __syncwarp();
-      if (lane < kCl) mbar_arrive_remote(mapa_shared(smem_u32(&tl->rstd_full[par]), lane));
-      if (lane < kSlots) {
-        const int64_t tt = (int64_t)b * kBM + (int)rank + kCl * lane;
-        float p[kParts];
-#pragma unroll
-        for (int k = 0; k < kParts; ++k) {
+        for (int k = 0; k < kOwnerParts; ++k) {
           float s = 0.f;
 #pragma unroll
           for (int src = 0; src < kCl; ++src) s += tl->recv[par][src][lane][k];
           p[k] = s;
         }
+      }
+      __syncwarp();
+      if (lane < kCl) mbar_arrive_remote(mapa_shared(smem_u32(&tl->recv_free[par]), lane));
+      if (lane < kSlots) {
+        const int64_t tt = (int64_t)b * kBM + (int)rank + kCl * lane;
         if (tt < T) finish_store_gates(a, tt, p, H);
       }
       __syncwarp();
@@ -409,8 +413,20 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
     };
     fetch_gates(0);
 
-    int j = 0, ji = 0;
     float rprev = 0.f;
+    // rstd_x of block lbp from the s_x partials the four CTAs sent (same sum
+    // order in every CTA, so all four hold the same value)
+    auto take_rstd = [&](int lbp) {
+      const int pp = lbp & 1;
+      wait_local(X, &tl->xs_full[pp], (lbp >> 1) & 1);
+      float sx = 0.f;
+#pragma unroll
+      for (int src = 0; src < kCl; ++src) sx += tl->xs[pp][src][lane];
+      const int64_t tt = (int64_t)(cid + lbp * ncl) * kBM + lane;
+      rprev = tt < T ? 1.0f / sqrtf(sx / (float)H + a.eps) : 0.f;
+    };
+
+    int j = 0, ji = 0;
     for (int lb = 0; lb <= nblk; ++lb) {  // the last pass only normalises the last block
       const bool real = lb < nblk, prev = lb > 0;
       float2 comb2[16], post2[4], pre2[4];  // each gate duplicated for the fp32x2 FMAs
@@ -471,11 +487,7 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
             sx2 = __ffma2_rn(xx, xx, sx2);
           }
         }
-        if (prev && c == 0) {  // rstd_x of the previous block, sent back by the owners
-          const int pp = (lb - 1) & 1;
-          wait_remote(X, &tl->rstd_full[pp], ((lb - 1) >> 1) & 1);
-          rprev = tl->rstd[pp][lane];
-        }
+        if (prev && c == 0) take_rstd(lb - 1);
         wait_local(X, &tl->out_empty[o], ((j / kNO) & 1) ^ 1);
         uint8_t* ost = sm + kOffOut + o * kOutStage;
         if (real) {
@@ -506,86 +518,101 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
       }
+      if (prev && nch == 0) take_rstd(lb - 1);  // no columns here: only consume the phase
       if (!real) break;
       if (MS && nch > 0) mma_chunk(j - 1, ji - 1);
       tc_wait_st();
       fetch_gates(lb + 1);
 
       // ------------------------------------------ block finish: partials --
-      tl->red[warp][lane][0] = sR2.x + sR2.y;
-      tl->red[warp][lane][1] = sx2.x + sx2.y;
-      // the output ring is idle once the stores (and projections) of its last
-      // two chunks are done: it stages the projection partials
-      wait_local(X, &tl->out_empty[j % kNO], ((j / kNO) & 1) ^ 1);
-      wait_local(X, &tl->out_empty[(j + 1) % kNO], (((j + 1) / kNO) & 1) ^ 1);
-      float* buf = reinterpret_cast<float*>(sm + kOffOut);  // [warps][32 tokens][24 logits]
-      int nparts;
-      if (MS) {
-        nparts = 8;
-        const int g = lane >> 2, t4 = lane & 3;
-#pragma unroll
-        for (int m = 0; m < 2; ++m) {
-#pragma unroll
-          for (int n = 0; n < 3; ++n) {
-            float* r0 = buf + ((size_t)warp * kBM + 16 * m + g) * 24 + 8 * n + 2 * t4;
-            r0[0] = acc[m][n][0];
-            r0[1] = acc[m][n][1];
-            r0[8 * 24] = acc[m][n][2];
-            r0[8 * 24 + 1] = acc[m][n][3];
-          }
-        }
-      } else {
-        nparts = 4;
-        if (warp < 4) {  // stream q = warp: TMEM lanes 32 q .., columns 48 q .. 48 q + 47
-          float dv[48];
-          if (nch > 0) {
-            wait_local(X, &tl->d_full, lb & 1);
-            tc_fence_after();
-#pragma unroll
-            for (int k = 0; k < 6; ++k)
-              tc_ld_x8(tmem + ((uint32_t)(32 * warp) << 16) + kColD + 48 * warp + 8 * k, dv + 8 * k);
-          } else {
-#pragma unroll
-            for (int k = 0; k < 48; ++k) dv[k] = 0.f;
-          }
-          float* r0 = buf + ((size_t)warp * kBM + lane) * 24;
-#pragma unroll
-          for (int k = 0; k < 24; ++k) r0[k] = dv[k] + dv[24 + k];
-        }
-      }
-      tc_fence_before();
-      named_bar_sync(1, kComputeThreads);
-      for (int idx = tid; idx < kBM * 24; idx += kComputeThreads) {
-        const int tok = idx / 24, k = idx - tok * 24;
-        float sum = 0.f;
-        for (int w = 0; w < nparts; ++w) sum += buf[((size_t)w * kBM + tok) * 24 + k];
-        tl->dmat[k][tok] = sum;
-      }
-      named_bar_sync(1, kComputeThreads);
       const int par = lb & 1;
-      if (tid < kBM * (kPartPad / 4)) {  // one 16-byte remote store per (token, 4 parts)
-        const int tok = tid / (kPartPad / 4), k0 = 4 * (tid - tok * (kPartPad / 4));
-        float v[4];
+      tl->red[par][warp][lane] = make_float2(sR2.x + sR2.y, sx2.x + sx2.y);
+      named_bar_sync(1, kComputeThreads);
+      if (warp == 4) {
+        // s_x of the 32 tokens to every CTA of the cluster: each one forms
+        // rstd_x from the four partials itself (one hop, no owner round trip)
+        float sx = 0.f;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int k = k0 + e;
-          if (k < 24) {
-            v[e] = tl->dmat[k][tok];
-          } else if (k < kParts) {
-            float sum = 0.f;
+        for (int w = 0; w < 8; ++w) sx += tl->red[par][w][lane].y;
+        if (lane == 0) mbar_arrive_expect_tx(&tl->xs_full[par], kXsBytes);
+        const uint32_t xa = smem_u32(&tl->xs[par][rank][lane]), xb = smem_u32(&tl->xs_full[par]);
 #pragma unroll
-            for (int w = 0; w < 8; ++w) sum += tl->red[w][tok][k - 24];
-            v[e] = sum;
-          } else {
-            v[e] = 0.f;
+        for (int dst = 0; dst < kCl; ++dst) st_async_f32(mapa_shared(xa, (uint32_t)dst), sx, mapa_shared(xb, (uint32_t)dst));
+      }
+      if (MS) {  // warps w and w + 4 both hold stream w % 4: fold them into dbuf[w % 4]
+        const int g = lane >> 2, t4 = lane & 3;
+        if (warp >= 4) {
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {
+#pragma unroll
+            for (int n = 0; n < 3; ++n) {
+              float* r0 = &tl->dbuf[warp - 4][16 * m + g][8 * n + 2 * t4];
+              r0[0] = acc[m][n][0];
+              r0[1] = acc[m][n][1];
+              r0[8 * kDPad] = acc[m][n][2];
+              r0[8 * kDPad + 1] = acc[m][n][3];
+            }
+          }
+          named_bar_arrive(2, kComputeThreads);
+        } else {
+          named_bar_sync(2, kComputeThreads);
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {
+#pragma unroll
+            for (int n = 0; n < 3; ++n) {
+              float* r0 = &tl->dbuf[warp][16 * m + g][8 * n + 2 * t4];
+              r0[0] += acc[m][n][0];
+              r0[1] += acc[m][n][1];
+              r0[8 * kDPad] += acc[m][n][2];
+              r0[8 * kDPad + 1] += acc[m][n][3];
+            }
           }
         }
-        st_cluster_v4(mapa_shared(smem_u32(&tl->recv[par][rank][tok / kCl][k0]), tok % kCl),
-                      make_float4(v[0], v[1], v[2], v[3]));
+      } else if (warp < 4) {  // stream q = warp: TMEM lanes 32 q .., columns 48 q .. 48 q + 47
+        float dv[48];
+        if (nch > 0) {
+          wait_local(X, &tl->d_full, lb & 1);
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 6; ++k)
+            tc_ld_x8(tmem + ((uint32_t)(32 * warp) << 16) + kColD + 48 * warp + 8 * k, dv + 8 * k);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 48; ++k) dv[k] = 0.f;
+        }
+        float* r0 = &tl->dbuf[warp][lane][0];
+#pragma unroll
+        for (int k = 0; k < 24; ++k) r0[k] = dv[k] + dv[24 + k];
+        tc_fence_before();  // the reads of D precede the next block's first MMA
       }
-      fence_acq_rel_cluster();
-      named_bar_sync(1, kComputeThreads);
-      if (tid < kCl) mbar_arrive_remote(mapa_shared(smem_u32(&tl->recv_full[par]), tid));
+      if (warp < 4) {
+        named_bar_sync(3, 4 * 32);
+        // the 24 projections (warp w: logits 6 w .. 6 w + 5) and s_R of each
+        // token to its owner CTA (token % 4), once the owners have read the
+        // partials of block lb - 2 out of this parity's slot
+        if (lb >= 2) wait_remote(X, &tl->recv_free[par], ((lb >> 1) & 1) ^ 1);
+        const int tok = lane, g6 = 6 * warp;
+        float v[6];
+#pragma unroll
+        for (int e = 0; e < 6; ++e) {
+          float s = tl->dbuf[0][tok][g6 + e];
+#pragma unroll
+          for (int q = 1; q < 4; ++q) s += tl->dbuf[q][tok][g6 + e];
+          v[e] = s;
+        }
+        const uint32_t dst = (uint32_t)(tok % kCl);
+        const uint32_t ra = mapa_shared(smem_u32(&tl->recv[par][rank][tok / kCl][g6]), dst);
+        const uint32_t rb = mapa_shared(smem_u32(&tl->recv_full[par]), dst);
+        st_async_v2(ra, v[0], v[1], rb);
+        st_async_v2(ra + 8, v[2], v[3], rb);
+        st_async_v2(ra + 16, v[4], v[5], rb);
+        if (warp == 0) {
+          float sR = 0.f;
+#pragma unroll
+          for (int w = 0; w < 8; ++w) sR += tl->red[par][w][tok].x;
+          st_async_f32(mapa_shared(smem_u32(&tl->recv[par][rank][tok / kCl][24]), dst), sR, rb);
+        }
+      }
     }
   }
 
