@@ -161,6 +161,22 @@ __device__ __forceinline__ void tc_st_x8(uint32_t taddr, const float* v) {
 }
 __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// TMEM load without the wait: tc_wait_ld_x8 on the same registers must come
+// before any use of them.
+__device__ __forceinline__ void tc_ld_x8_issue(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
+}
+// Wait for this thread's TMEM loads; the registers pass through the asm, so
+// no use of them can move above the wait.
+__device__ __forceinline__ void tc_wait_ld_x8(uint32_t* r) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])
+               :
+               : "memory");
+}
 // Load and wait in one block, so no use of the registers can move above the wait.
 __device__ __forceinline__ void tc_ld_x8(uint32_t taddr, float* v) {
   uint32_t r0, r1, r2, r3, r4, r5, r6, r7;

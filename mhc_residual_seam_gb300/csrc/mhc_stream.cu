@@ -4,7 +4,9 @@
 // columns [r W, (r+1) W) of H for all four streams (W = H / 4) and the cluster
 // walks blocks of 32 tokens.  Per 64-column chunk:
 //  - an input producer warp TMA-loads the four R tiles and the Y tile into a
-//    ring of 5 input stages (128-byte swizzle, L2 evict-first);
+//    ring of 5 input stages (128-byte swizzle, L2 evict-first), and each
+//    block's carried gates (comb, pre, post) into a double buffer as it
+//    starts the block, so they wait in shared memory when compute gets there;
 //  - an fn producer warp TMA-loads the four hi/lo-packed fn tiles [48 x 64]
 //    into a ring of 2 fn stages (L2 evict-last: every cluster reuses them);
 //  - eight compute warps (thread = token, warp = 8-column slice; the swizzle
@@ -58,7 +60,7 @@ constexpr uint32_t kFnStage = 4 * kFnTile;             // 24 KB: [192 x 64] bf16
 constexpr uint32_t kInStage = 5 * kRTile;              // 20 KB: R tiles 0-3, Y tile 4
 constexpr uint32_t kOffNormT = 4 * kRTile;             // output stage: R' tiles 0-3, then the norm tile,
 constexpr uint32_t kOffCodesT = 5 * kRTile;            //   then the codes tile [32 x 64] u8
-constexpr uint32_t kOutStage = 6 * kRTile;             // 24 KB
+constexpr uint32_t kOutStage = 5 * kRTile + kBM * 64;  // 22 KB (a multiple of 1 KB: swizzled tiles)
 constexpr uint32_t kOffFn = 0;
 constexpr uint32_t kOffOut = kOffFn + kNF * kFnStage;
 constexpr uint32_t kOffIn = kOffOut + kNO * kOutStage;
@@ -76,9 +78,18 @@ constexpr int kDPad = 25;                              // odd row stride: confli
 constexpr uint32_t kXsBytes = kCl * kBM * 4;           // s_x partials landing in each CTA per block
 constexpr uint32_t kRecvBytes = kCl * kSlots * kOwnerParts * 4;  // owner partials per CTA per block
 
+// Carried gates of one block, TMA-loaded a block ahead: comb [32 x 16],
+// pre [32 x 4], post [32 x 4] fp32.
+struct alignas(128) GateTile {
+  float comb[kBM][16];
+  float pre[kBM][4];
+  float post[kBM][4];
+};
+
 struct Tail {
+  GateTile gates[2];                     // [block parity]
   uint64_t in_full[kNI], in_empty[kNI], fn_full[kNF], fn_empty[kNF], out_full[kNO], out_empty[kNO];
-  uint64_t d_full, xs_full[2], recv_full[2], recv_free[2];
+  uint64_t d_full, xs_full[2], recv_full[2], recv_free[2], gates_full[2], gates_empty[2];
   uint32_t tmem_base;
   volatile int err;
   float2 red[2][8][kBM];                 // [block parity][compute warp][token]: s_R, s_x partials
@@ -141,7 +152,9 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
     stream_seam_kernel(const SeamArgs a, const __grid_constant__ CUtensorMap tmR,
                        const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmRo,
                        const __grid_constant__ CUtensorMap tmFn, const __grid_constant__ CUtensorMap tmN,
-                       const __grid_constant__ CUtensorMap tmC, int W, int n_blocks, unsigned long long limit_ns) {
+                       const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmGc,
+                       const __grid_constant__ CUtensorMap tmGp, const __grid_constant__ CUtensorMap tmGq, int W,
+                       int n_blocks, unsigned long long limit_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Tail* tl = reinterpret_cast<Tail*>(sm + kOffTail);
@@ -174,6 +187,8 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&tl->xs_full[p], 1);    // + kXsBytes of st.async from the cluster
       mbar_init(&tl->recv_full[p], 1);  // + kRecvBytes of st.async from the cluster
       mbar_init(&tl->recv_free[p], kCl);
+      mbar_init(&tl->gates_full[p], 1);
+      mbar_init(&tl->gates_empty[p], 8);
     }
     tl->err = 0;
     mbar_fence_init();
@@ -181,6 +196,9 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 8 && lane == 0) {
     prefetch_tmap(&tmR);
     if (POST) prefetch_tmap(&tmY);
+    prefetch_tmap(&tmGc);
+    prefetch_tmap(&tmGp);
+    if (POST) prefetch_tmap(&tmGq);
   }
   if (warp == 10 && lane == 0) prefetch_tmap(&tmFn);
   if (warp == 12 && lane == 0) {
@@ -206,6 +224,14 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
       int j = 0;
       for (int lb = 0; lb < nblk; ++lb) {
         const int t0 = (cid + lb * ncl) * kBM;
+        {  // the block's carried gates, consumed at the top of its compute
+          const int gp = lb & 1;
+          wait_local(X, &tl->gates_empty[gp], ((lb >> 1) & 1) ^ 1);
+          mbar_arrive_expect_tx(&tl->gates_full[gp], (POST ? 24 : 20) * kBM * 4);
+          tma_load_2d(&tl->gates[gp].comb[0][0], &tmGc, &tl->gates_full[gp], 0, t0, pol);
+          tma_load_2d(&tl->gates[gp].pre[0][0], &tmGp, &tl->gates_full[gp], 0, t0, pol);
+          if (POST) tma_load_2d(&tl->gates[gp].post[0][0], &tmGq, &tl->gates_full[gp], 0, t0, pol);
+        }
         for (int c = 0; c < nch; ++c, ++j) {
           const int s = j % kNI;
           wait_local(X, &tl->in_empty[s], ((j / kNI) & 1) ^ 1);
@@ -397,21 +423,6 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
       }
     };
 
-    // carried gates of the next block, fetched one block ahead
-    float4 gc[4], gp = make_float4(0.f, 0.f, 0.f, 0.f), gq = make_float4(0.f, 0.f, 0.f, 0.f);
-    auto fetch_gates = [&](int lb) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k) gc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-      gp = gq = make_float4(0.f, 0.f, 0.f, 0.f);
-      const int64_t t = (int64_t)(cid + lb * ncl) * kBM + lane;
-      if (lb < nblk && t < T) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) gc[k] = __ldg(reinterpret_cast<const float4*>(a.comb_prev + t * 16) + k);
-        gp = __ldg(reinterpret_cast<const float4*>(a.pre_prev + t * 4));
-        if (POST) gq = __ldg(reinterpret_cast<const float4*>(a.post_prev + t * 4));
-      }
-    };
-    fetch_gates(0);
 
     float rprev = 0.f;
     // rstd_x of block lbp from the s_x partials the four CTAs sent (same sum
@@ -430,15 +441,31 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
     for (int lb = 0; lb <= nblk; ++lb) {  // the last pass only normalises the last block
       const bool real = lb < nblk, prev = lb > 0;
       float2 comb2[16], post2[4], pre2[4];  // each gate duplicated for the fp32x2 FMAs
+      {
+        float4 gc[4], gp = make_float4(0.f, 0.f, 0.f, 0.f), gq = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        comb2[4 * k] = make_float2(gc[k].x, gc[k].x); comb2[4 * k + 1] = make_float2(gc[k].y, gc[k].y);
-        comb2[4 * k + 2] = make_float2(gc[k].z, gc[k].z); comb2[4 * k + 3] = make_float2(gc[k].w, gc[k].w);
+        for (int k = 0; k < 4; ++k) gc[k] = gp;
+        if (real) {  // rows past T arrive as zeros
+          const int p = lb & 1;
+          wait_local(X, &tl->gates_full[p], (lb >> 1) & 1);
+          const GateTile& gt = tl->gates[p];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) gc[k] = *reinterpret_cast<const float4*>(&gt.comb[lane][4 * k]);
+          gp = *reinterpret_cast<const float4*>(&gt.pre[lane][0]);
+          if (POST) gq = *reinterpret_cast<const float4*>(&gt.post[lane][0]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tl->gates_empty[p]);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          comb2[4 * k] = make_float2(gc[k].x, gc[k].x); comb2[4 * k + 1] = make_float2(gc[k].y, gc[k].y);
+          comb2[4 * k + 2] = make_float2(gc[k].z, gc[k].z); comb2[4 * k + 3] = make_float2(gc[k].w, gc[k].w);
+        }
+        pre2[0] = make_float2(gp.x, gp.x); pre2[1] = make_float2(gp.y, gp.y);
+        pre2[2] = make_float2(gp.z, gp.z); pre2[3] = make_float2(gp.w, gp.w);
+        post2[0] = make_float2(gq.x, gq.x); post2[1] = make_float2(gq.y, gq.y);
+        post2[2] = make_float2(gq.z, gq.z); post2[3] = make_float2(gq.w, gq.w);
       }
-      pre2[0] = make_float2(gp.x, gp.x); pre2[1] = make_float2(gp.y, gp.y);
-      pre2[2] = make_float2(gp.z, gp.z); pre2[3] = make_float2(gp.w, gp.w);
-      post2[0] = make_float2(gq.x, gq.x); post2[1] = make_float2(gq.y, gq.y);
-      post2[2] = make_float2(gq.z, gq.z); post2[3] = make_float2(gq.w, gq.w);
       float2 sR2 = make_float2(0.f, 0.f), sx2 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int m = 0; m < 2; ++m)
@@ -451,6 +478,14 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
         const int o = j % kNO;
         uint32_t ow[4][4];
         float x[8];
+        // the previous block's x and gamma of these columns, fetched now so
+        // their latency hides behind this chunk's post-mix
+        uint32_t xr[8];
+        uint4 gv = make_uint4(0, 0, 0, 0);
+        if (prev) {
+          tc_ld_x8_issue(xaddr + 16 * c, xr);
+          gv = __ldg(reinterpret_cast<const uint4*>(a.gamma + hbase + c * kChunk + 8 * warp));
+        }
         if (real) {
           const int s = ji % kNI;
           wait_local(X, &tl->in_full[s], (ji / kNI) & 1);
@@ -497,8 +532,10 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (prev) {  // norm of the previous block's x in these columns, before x is overwritten
           float xv[8], gm[8];
-          tc_ld_x8(xaddr + 16 * c, xv);
-          unpack8(__ldg(reinterpret_cast<const uint4*>(a.gamma + hbase + c * kChunk + 8 * warp)), gm);
+          tc_wait_ld_x8(xr);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) xv[e] = __uint_as_float(xr[e]);
+          unpack8(gv, gm);
           uint4 nv;
           nv.x = pack_bf16x2(xv[0] * rprev * gm[0], xv[1] * rprev * gm[1]);
           nv.y = pack_bf16x2(xv[2] * rprev * gm[2], xv[3] * rprev * gm[3]);
@@ -522,7 +559,6 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
       if (!real) break;
       if (MS && nch > 0) mma_chunk(j - 1, ji - 1);
       tc_wait_st();
-      fetch_gates(lb + 1);
 
       // ------------------------------------------ block finish: partials --
       const int par = lb & 1;
@@ -734,6 +770,14 @@ cudaError_t stream_launch(const SeamArgs& a, bool tcgen05_proj, cudaStream_t str
                       CU_TENSOR_MAP_SWIZZLE_128B);
   if (ok) ok = encode(&mC, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.codes ? (const void*)a.codes : (const void*)a.norm, d2,
                       sC, b2, CU_TENSOR_MAP_SWIZZLE_NONE);
+  // carried gates: comb [T, 16], pre and post [T, 4] fp32, 32 token rows per box
+  CUtensorMap mGc, mGp, mGq;
+  const cuuint64_t dG16[2] = {16, T}, sG16[1] = {64}, dG4[2] = {4, T}, sG4[1] = {16};
+  const cuuint32_t bG16[2] = {16, kBM}, bG4[2] = {4, kBM};
+  if (ok) ok = encode(&mGc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.comb_prev, dG16, sG16, bG16, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+               encode(&mGp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.pre_prev, dG4, sG4, bG4, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+               encode(&mGq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.post_prev ? a.post_prev : a.pre_prev, dG4, sG4, bG4,
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
   if (!ok) return cudaErrorInvalidValue;
   void* k = stream_kernel_ptr(a.Y != nullptr, a.codes != nullptr, !tcgen05_proj);
   const int n_blocks = (int)((a.T + kBM - 1) / kBM);
@@ -746,7 +790,7 @@ cudaError_t stream_launch(const SeamArgs& a, bool tcgen05_proj, cudaStream_t str
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
   int Wi = W, nb = n_blocks;
-  void* args[] = {const_cast<SeamArgs*>(&a), &mR, &mY, &mRo, &mFn, &mN, &mC, &Wi, &nb, &limit_ns};
+  void* args[] = {const_cast<SeamArgs*>(&a), &mR, &mY, &mRo, &mFn, &mN, &mC, &mGc, &mGp, &mGq, &Wi, &nb, &limit_ns};
   cudaError_t e = cudaLaunchKernelExC(&cfg, k, args);
   if (e == cudaSuccess) ++*launches;
   return e;
