@@ -1,8 +1,9 @@
 // Streaming path of the delayed mHC seam: bandwidth-tuned for large T.
 //
 // Persistent clusters of 4 CTAs (one CTA per SM).  CTA r of a cluster owns
-// columns [r W, (r+1) W) of H for all four streams (W = H / 4) and the cluster
-// walks blocks of 32 tokens.  Per 64-column chunk:
+// the 64-column chunks r, r + 4, r + 8, ... of H for all four streams (the
+// cluster reads each row in 512-byte runs) and the cluster walks blocks of 32
+// tokens.  Per 64-column chunk:
 //  - an input producer warp TMA-loads the four R tiles and the Y tile into a
 //    ring of 5 input stages (128-byte swizzle, L2 evict-first), and each
 //    block's carried gates (comb, pre, post) into a double buffer as it
@@ -153,7 +154,7 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmRo,
                        const __grid_constant__ CUtensorMap tmFn, const __grid_constant__ CUtensorMap tmN,
                        const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmGc,
-                       const __grid_constant__ CUtensorMap tmGp, const __grid_constant__ CUtensorMap tmGq, int W,
+                       const __grid_constant__ CUtensorMap tmGp, const __grid_constant__ CUtensorMap tmGq,
                        int n_blocks, unsigned long long limit_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -164,8 +165,10 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t rank = cluster_ctarank();
   const int H = a.H;
   const int64_t T = a.T;
-  const int hbase = (int)rank * W;
-  const int nch = (max(0, min(W, H - hbase)) + kChunk - 1) / kChunk;
+  // CTA r owns the 64-column chunks r, r + 4, r + 8, ... of H: at any time the
+  // four CTAs of a cluster touch adjacent 128-byte pieces of the same rows
+  const int n64 = H / kChunk;
+  const int nch = n64 > (int)rank ? (n64 - (int)rank + kCl - 1) / kCl : 0;
   const int cid = blockIdx.x / kCl, ncl = gridDim.x / kCl;
   const int nblk = cid < n_blocks ? (n_blocks - cid + ncl - 1) / ncl : 0;  // blocks of this cluster
 
@@ -236,7 +239,7 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
           const int s = j % kNI;
           wait_local(X, &tl->in_empty[s], ((j / kNI) & 1) ^ 1);
           uint8_t* st = sm + kOffIn + s * kInStage;
-          const int h = hbase + c * kChunk;
+          const int h = (c * kCl + (int)rank) * kChunk;
           mbar_arrive_expect_tx(&tl->in_full[s], bytes);
 #pragma unroll
           for (int i = 0; i < 4; ++i) tma_load_3d(st + i * kRTile, &tmR, &tl->in_full[s], h, i, t0, pol);
@@ -258,7 +261,7 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
           const int f = j % kNF;
           wait_local(X, &tl->fn_empty[f], ((j / kNF) & 1) ^ 1);
           uint8_t* st = sm + kOffFn + f * kFnStage;
-          const int h = hbase + c * kChunk;
+          const int h = (c * kCl + (int)rank) * kChunk;
           mbar_arrive_expect_tx(&tl->fn_full[f], kFnStage);
 #pragma unroll
           for (int i = 0; i < 4; ++i) tma_load_3d(st + i * kFnTile, &tmFn, &tl->fn_full[f], h, i, 0, pol);
@@ -305,7 +308,7 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
       for (int c = 0; c < nch; ++c, ++j) {
         const int o = j % kNO;
         uint8_t* ost = sm + kOffOut + o * kOutStage;
-        const int h = hbase + c * kChunk;
+        const int h = (c * kCl + (int)rank) * kChunk;
         wait_local(X, &tl->out_full[o], (j / kNO) & 1);
         if (MXFP8 && prev) {  // lane = token; two 32-column groups each
 #pragma unroll
@@ -484,7 +487,7 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
         uint4 gv = make_uint4(0, 0, 0, 0);
         if (prev) {
           tc_ld_x8_issue(xaddr + 16 * c, xr);
-          gv = __ldg(reinterpret_cast<const uint4*>(a.gamma + hbase + c * kChunk + 8 * warp));
+          gv = __ldg(reinterpret_cast<const uint4*>(a.gamma + (c * kCl + (int)rank) * kChunk + 8 * warp));
         }
         if (real) {
           const int s = ji % kNI;
@@ -684,7 +687,8 @@ cudaError_t stream_init() {
   return cudaSuccess;
 }
 
-// Columns per CTA for width H, or 0 when the streaming path cannot take H.
+// Most columns one CTA handles at width H (its chunk count times 64), or 0
+// when the streaming path cannot take H.
 int stream_cols(int H) {
   if (H % kChunk != 0 || H < 512) return 0;
   const int chunks = (H / kChunk + kCl - 1) / kCl;
@@ -789,8 +793,8 @@ cudaError_t stream_launch(const SeamArgs& a, bool tcgen05_proj, cudaStream_t str
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
-  int Wi = W, nb = n_blocks;
-  void* args[] = {const_cast<SeamArgs*>(&a), &mR, &mY, &mRo, &mFn, &mN, &mC, &mGc, &mGp, &mGq, &Wi, &nb, &limit_ns};
+  int nb = n_blocks;
+  void* args[] = {const_cast<SeamArgs*>(&a), &mR, &mY, &mRo, &mFn, &mN, &mC, &mGc, &mGp, &mGq, &nb, &limit_ns};
   cudaError_t e = cudaLaunchKernelExC(&cfg, k, args);
   if (e == cudaSuccess) ++*launches;
   return e;
