@@ -91,6 +91,7 @@ struct Tail {
   GateTile gates[2];                     // [block parity]
   uint64_t in_full[kNI], in_empty[kNI], fn_full[kNF], fn_empty[kNF], out_full[kNO], out_empty[kNO];
   uint64_t d_full, xs_full[2], recv_full[2], recv_free[2], gates_full[2], gates_empty[2];
+  uint64_t red_full[2], dbuf_full, dbuf_free;
   uint32_t tmem_base;
   volatile int err;
   float2 red[2][8][kBM];                 // [block parity][compute warp][token]: s_R, s_x partials
@@ -186,12 +187,15 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&tl->out_empty[s], MS ? 9 : 2);
     }
     mbar_init(&tl->d_full, 1);
+    mbar_init(&tl->dbuf_full, 4);  // the four D readers (or folders)
+    mbar_init(&tl->dbuf_free, 1);  // the exchange warp
     for (int p = 0; p < 2; ++p) {
       mbar_init(&tl->xs_full[p], 1);    // + kXsBytes of st.async from the cluster
       mbar_init(&tl->recv_full[p], 1);  // + kRecvBytes of st.async from the cluster
       mbar_init(&tl->recv_free[p], kCl);
       mbar_init(&tl->gates_full[p], 1);
       mbar_init(&tl->gates_empty[p], 8);
+      mbar_init(&tl->red_full[p], 8);
     }
     tl->err = 0;
     mbar_fence_init();
@@ -349,12 +353,52 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
     }
     if (lane == 0) tma_store_wait_all();
   } else if (warp == 11) {
-    // ---------------------------------------- finisher: gates of 8 tokens --
-    // The owner partials of block lb land by st.async on recv_full[lb & 1];
-    // once read, every CTA is told the slot is free (recv_free) so that the
-    // partials of block lb + 2 may overwrite it.
+    // ------------------------------------ exchange and gate finish warp --
+    // Per block: (1) this CTA's s_x partials to every CTA of the cluster (each
+    // forms rstd_x itself), (2) the 24 projections and s_R of each token to
+    // its owner CTA (token % 4), (3) the gates of the 8 tokens this CTA owns.
+    // Sends are st.async completing bytes on the receiver's mbarrier; the
+    // compute warps only hand their partials over and go on.  recv_free keeps
+    // the partials of block lb + 2 out of a slot until every owner has read
+    // block lb from it.
     for (int lb = 0; lb < nblk; ++lb) {
       const int b = cid + lb * ncl, par = lb & 1;
+      wait_local(X, &tl->red_full[par], (lb >> 1) & 1);
+      float sx = 0.f, sR = 0.f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        const float2 v = tl->red[par][w][lane];
+        sR += v.x;
+        sx += v.y;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&tl->xs_full[par], kXsBytes);
+      {
+        const uint32_t xa = smem_u32(&tl->xs[par][rank][lane]), xb = smem_u32(&tl->xs_full[par]);
+#pragma unroll
+        for (int dst = 0; dst < kCl; ++dst)
+          st_async_f32(mapa_shared(xa, (uint32_t)dst), sx, mapa_shared(xb, (uint32_t)dst));
+      }
+      wait_local(X, &tl->dbuf_full, lb & 1);
+      if (lb >= 2) wait_remote(X, &tl->recv_free[par], ((lb >> 1) & 1) ^ 1);
+      {
+        const uint32_t dst = (uint32_t)(lane % kCl);
+        const uint32_t ra = mapa_shared(smem_u32(&tl->recv[par][rank][lane / kCl][0]), dst);
+        const uint32_t rb = mapa_shared(smem_u32(&tl->recv_full[par]), dst);
+#pragma unroll
+        for (int k = 0; k < 24; k += 2) {
+          float s0 = tl->dbuf[0][lane][k], s1 = tl->dbuf[0][lane][k + 1];
+#pragma unroll
+          for (int q = 1; q < 4; ++q) {
+            s0 += tl->dbuf[q][lane][k];
+            s1 += tl->dbuf[q][lane][k + 1];
+          }
+          st_async_v2(ra + 4 * k, s0, s1, rb);
+        }
+        st_async_f32(ra + 4 * 24, sR, rb);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tl->dbuf_free);
+
       if (lane == 0) mbar_arrive_expect_tx(&tl->recv_full[par], kRecvBytes);
       wait_local(X, &tl->recv_full[par], (lb >> 1) & 1);
       float p[kOwnerParts];
@@ -563,24 +607,15 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
       if (MS && nch > 0) mma_chunk(j - 1, ji - 1);
       tc_wait_st();
 
-      // ------------------------------------------ block finish: partials --
+      // ------------ block finish: hand the partials to the exchange warp --
       const int par = lb & 1;
       tl->red[par][warp][lane] = make_float2(sR2.x + sR2.y, sx2.x + sx2.y);
-      named_bar_sync(1, kComputeThreads);
-      if (warp == 4) {
-        // s_x of the 32 tokens to every CTA of the cluster: each one forms
-        // rstd_x from the four partials itself (one hop, no owner round trip)
-        float sx = 0.f;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) sx += tl->red[par][w][lane].y;
-        if (lane == 0) mbar_arrive_expect_tx(&tl->xs_full[par], kXsBytes);
-        const uint32_t xa = smem_u32(&tl->xs[par][rank][lane]), xb = smem_u32(&tl->xs_full[par]);
-#pragma unroll
-        for (int dst = 0; dst < kCl; ++dst) st_async_f32(mapa_shared(xa, (uint32_t)dst), sx, mapa_shared(xb, (uint32_t)dst));
-      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tl->red_full[par]);
       if (MS) {  // warps w and w + 4 both hold stream w % 4: fold them into dbuf[w % 4]
         const int g = lane >> 2, t4 = lane & 3;
         if (warp >= 4) {
+          wait_local(X, &tl->dbuf_free, (lb & 1) ^ 1);
 #pragma unroll
           for (int m = 0; m < 2; ++m) {
 #pragma unroll
@@ -606,6 +641,8 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
               r0[8 * kDPad + 1] += acc[m][n][3];
             }
           }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tl->dbuf_full);
         }
       } else if (warp < 4) {  // stream q = warp: TMEM lanes 32 q .., columns 48 q .. 48 q + 47
         float dv[48];
@@ -619,38 +656,13 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 48; ++k) dv[k] = 0.f;
         }
+        tc_fence_before();  // the reads of D precede the next block's first MMA
+        wait_local(X, &tl->dbuf_free, (lb & 1) ^ 1);
         float* r0 = &tl->dbuf[warp][lane][0];
 #pragma unroll
         for (int k = 0; k < 24; ++k) r0[k] = dv[k] + dv[24 + k];
-        tc_fence_before();  // the reads of D precede the next block's first MMA
-      }
-      if (warp < 4) {
-        named_bar_sync(3, 4 * 32);
-        // the 24 projections (warp w: logits 6 w .. 6 w + 5) and s_R of each
-        // token to its owner CTA (token % 4), once the owners have read the
-        // partials of block lb - 2 out of this parity's slot
-        if (lb >= 2) wait_remote(X, &tl->recv_free[par], ((lb >> 1) & 1) ^ 1);
-        const int tok = lane, g6 = 6 * warp;
-        float v[6];
-#pragma unroll
-        for (int e = 0; e < 6; ++e) {
-          float s = tl->dbuf[0][tok][g6 + e];
-#pragma unroll
-          for (int q = 1; q < 4; ++q) s += tl->dbuf[q][tok][g6 + e];
-          v[e] = s;
-        }
-        const uint32_t dst = (uint32_t)(tok % kCl);
-        const uint32_t ra = mapa_shared(smem_u32(&tl->recv[par][rank][tok / kCl][g6]), dst);
-        const uint32_t rb = mapa_shared(smem_u32(&tl->recv_full[par]), dst);
-        st_async_v2(ra, v[0], v[1], rb);
-        st_async_v2(ra + 8, v[2], v[3], rb);
-        st_async_v2(ra + 16, v[4], v[5], rb);
-        if (warp == 0) {
-          float sR = 0.f;
-#pragma unroll
-          for (int w = 0; w < 8; ++w) sR += tl->red[par][w][tok].x;
-          st_async_f32(mapa_shared(smem_u32(&tl->recv[par][rank][tok / kCl][24]), dst), sR, rb);
-        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tl->dbuf_full);
       }
     }
   }
