@@ -91,7 +91,7 @@ struct Tail {
   GateTile gates[2];                     // [block parity]
   uint64_t in_full[kNI], in_empty[kNI], fn_full[kNF], fn_empty[kNF], out_full[kNO], out_empty[kNO];
   uint64_t d_full, xs_full[2], recv_full[2], recv_free[2], gates_full[2], gates_empty[2];
-  uint64_t red_full[2], dbuf_full, dbuf_free;
+  uint64_t red_full[2], dbuf_full, dbuf_free, d_free;
   uint32_t tmem_base;
   volatile int err;
   float2 red[2][8][kBM];                 // [block parity][compute warp][token]: s_R, s_x partials
@@ -189,6 +189,7 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&tl->d_full, 1);
     mbar_init(&tl->dbuf_full, 4);  // the four D readers (or folders)
     mbar_init(&tl->dbuf_free, 1);  // the exchange warp
+    mbar_init(&tl->d_free, 4);     // the four D readers
     for (int p = 0; p < 2; ++p) {
       mbar_init(&tl->xs_full[p], 1);    // + kXsBytes of st.async from the cluster
       mbar_init(&tl->recv_full[p], 1);  // + kRecvBytes of st.async from the cluster
@@ -289,6 +290,8 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
             continue;
           }
           const int f = jr % kNF;
+          // the first MMA of a block overwrites D: the previous block's D must have been read
+          if (c == 0 && lb > 0) wait_local(X, &tl->d_free, (lb - 1) & 1);
           wait_local(X, &tl->fn_full[f], (jr / kNF) & 1);
           tc_fence_after();
           const uint32_t ra = smem_u32(sm + kOffOut + o * kOutStage);   // R' of the 4 streams [128 x 64]
@@ -484,6 +487,33 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
       rprev = tt < T ? 1.0f / sqrtf(sx / (float)H + a.eps) : 0.f;
     };
 
+    // tcgen05 projection: warp q reads stream q's diagonal block of block
+    // lbp's D (TMEM lanes 32 q .., columns 48 q .. 48 q + 47) during the next
+    // block's first chunk, frees D for that block's MMAs, and hands the
+    // hi + lo sums to the exchange warp through dbuf.
+    auto read_d = [&](int lbp) {
+      float dv[48];
+      if (nch > 0) {
+        wait_local(X, &tl->d_full, lbp & 1);
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 6; ++k)
+          tc_ld_x8(tmem + ((uint32_t)(32 * warp) << 16) + kColD + 48 * warp + 8 * k, dv + 8 * k);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 48; ++k) dv[k] = 0.f;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tl->d_free);
+      wait_local(X, &tl->dbuf_free, (lbp & 1) ^ 1);
+      float* r0 = &tl->dbuf[warp][lane][0];
+#pragma unroll
+      for (int k = 0; k < 24; ++k) r0[k] = dv[k] + dv[24 + k];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tl->dbuf_full);
+    };
+
     int j = 0, ji = 0;
     for (int lb = 0; lb <= nblk; ++lb) {  // the last pass only normalises the last block
       const bool real = lb < nblk, prev = lb > 0;
@@ -594,6 +624,7 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tl->out_full[o]);
+        if (!MS && prev && c == 0 && warp < 4) read_d(lb - 1);
         if (MS) {
           if (real && c > 0) mma_chunk(j - 1, ji - 2);
           if (!real) {  // no projection in the normalise-only pass: release the stage
@@ -602,7 +633,10 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (prev && nch == 0) take_rstd(lb - 1);  // no columns here: only consume the phase
+      if (prev && nch == 0) {  // no columns here: only consume the phases
+        take_rstd(lb - 1);
+        if (!MS && warp < 4) read_d(lb - 1);
+      }
       if (!real) break;
       if (MS && nch > 0) mma_chunk(j - 1, ji - 1);
       tc_wait_st();
@@ -644,25 +678,6 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&tl->dbuf_full);
         }
-      } else if (warp < 4) {  // stream q = warp: TMEM lanes 32 q .., columns 48 q .. 48 q + 47
-        float dv[48];
-        if (nch > 0) {
-          wait_local(X, &tl->d_full, lb & 1);
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < 6; ++k)
-            tc_ld_x8(tmem + ((uint32_t)(32 * warp) << 16) + kColD + 48 * warp + 8 * k, dv + 8 * k);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 48; ++k) dv[k] = 0.f;
-        }
-        tc_fence_before();  // the reads of D precede the next block's first MMA
-        wait_local(X, &tl->dbuf_free, (lb & 1) ^ 1);
-        float* r0 = &tl->dbuf[warp][lane][0];
-#pragma unroll
-        for (int k = 0; k < 24; ++k) r0[k] = dv[k] + dv[24 + k];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tl->dbuf_full);
       }
     }
   }
