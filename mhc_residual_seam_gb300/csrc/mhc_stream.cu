@@ -98,6 +98,7 @@ struct Tail {
   float dbuf[4][kBM][kDPad];             // the block's projection per stream (hi + lo): [stream][token][logit]
   float xs[2][kCl][kBM];                 // [block parity][source CTA][token]: s_x partial
   float recv[2][kCl][kSlots][kPartPad];  // [block parity][source CTA][owned token][part]
+  uint4 gam[kMaxChunksTC][8];            // gamma of this CTA's chunks (8 bf16 per compute warp)
 };
 
 constexpr size_t kSmemBytes = kOffTail + sizeof(Tail) + 1024;
@@ -214,6 +215,9 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmN);
     if (MXFP8) prefetch_tmap(&tmC);
   }
+  // gamma of this CTA's first chunks, staged once (read by every block)
+  for (int i = tid; i < min(nch, kMaxChunksTC) * 8; i += kThreads)
+    tl->gam[i >> 3][i & 7] = __ldg(reinterpret_cast<const uint4*>(a.gamma + ((i >> 3) * kCl + (int)rank) * kChunk) + (i & 7));
   if (warp == 9) {
     tmem_alloc(&tl->tmem_base, kTmemCols);
     tmem_relinquish();
@@ -561,7 +565,8 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
         uint4 gv = make_uint4(0, 0, 0, 0);
         if (prev) {
           tc_ld_x8_issue(xaddr + 16 * c, xr);
-          gv = __ldg(reinterpret_cast<const uint4*>(a.gamma + (c * kCl + (int)rank) * kChunk + 8 * warp));
+          gv = c < kMaxChunksTC ? tl->gam[c][warp]
+                                : __ldg(reinterpret_cast<const uint4*>(a.gamma + (c * kCl + (int)rank) * kChunk + 8 * warp));
         }
         if (real) {
           const int s = ji % kNI;
