@@ -118,7 +118,7 @@ __device__ __forceinline__ void flag_error(const Ctx& x) {
 }
 // Bounded wait on a CTA-local barrier; returns at once after an earlier error.
 __device__ __forceinline__ void wait_local(const Ctx& x, uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity, 0)) return;
+  if (mbar_test_wait(bar, parity)) return;
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity, 20000)) {
     if (x.tl->err) return;
