@@ -157,7 +157,7 @@ def run_ours(args, w: dict, rank: int, world: int, local_rank: int) -> dict | No
     B.mhc_pack_fn(g["fn"], g["fn_packed"], stream=stream)  # once per weight update, outside the timed region
 
     cfg = B.MhcConfig(projection={"auto": 0, "mma": 1, "tcgen05": 2}[args.projection],
-                      path={"auto": 0, "split": 1, "stream": 2}[args.path])
+                      path={"auto": 0, "split": 1, "stream": 2, "stream16": 3}[args.path])
     out = B.alloc_outputs(T, H, mode, device, cfg)
 
     def step():
@@ -298,7 +298,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--projection", choices=["auto", "mma", "tcgen05"], default="auto",
                     help="streaming path's gate projection (auto = the library's policy)")
-    ap.add_argument("--path", choices=["auto", "split", "stream"], default="auto",
+    ap.add_argument("--path", choices=["auto", "split", "stream", "stream16"], default="auto",
                     help="kernel path (auto = the library's policy)")
     ap.add_argument("--graph", action="store_true",
                     help="time replays of a CUDA graph holding one seam call (as the pages time small T)")

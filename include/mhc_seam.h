@@ -69,10 +69,15 @@ typedef enum {
 
 /* Launch choices.  Zero in any field means "the policy decides". */
 typedef struct {
-    int path;            /* 0 auto; 1 split path (H spread over many small CTAs, CUDA-core
-                            projection, global split-K with a last-arriving-CTA finish:
-                            latency-tuned); 2 streaming path (TMA-staged streams, tcgen05
-                            projection, cluster split-K: bandwidth-tuned) */
+    int path;            /* 0 auto: 2 from 1024 tokens; below that 3 when H >= 1024 and
+                            fn_packed is given, else 1; 1 whenever the streaming path
+                            cannot take H or block_m / cols_per_cta is set; 1 split path (H spread
+                            over many small CTAs, CUDA-core projection, global split-K
+                            with a last-arriving-CTA finish); 2 streaming path (TMA-staged
+                            streams, tensor-core projection, split-K over a cluster of 4
+                            CTAs: bandwidth-tuned); 3 streaming path over clusters of 16
+                            CTAs (a quarter of the columns per CTA: latency-tuned for
+                            small T; tcgen05 projection only) */
     int block_m;         /* tokens per CTA: path 1: 1, 2, 4, 8, 16 or 32; 0 = policy */
     int cols_per_cta;    /* path 1: columns of H per CTA, a multiple of 32; 0 = policy */
     int sinkhorn_iters;  /* Sinkhorn rounds; 0 = 20 */
@@ -121,7 +126,7 @@ int mhc_pack_fn(const float* fn, void* fn_packed, int H, void* stream);
  *   comb_prev   [T,4,4] fp32, row i mixes into output stream i
  *   pre_prev    [T,4]   fp32, the carried pre used for x
  *   fn          [4H,24] fp32, row i*H + h; 16-byte aligned
- *   fn_packed   mhc_pack_fn(fn) output, or NULL; required by path 2
+ *   fn_packed   mhc_pack_fn(fn) output, or NULL; required by paths 2 and 3
  *   bias [24], alpha [3] fp32;  gamma [H] bf16 (16-byte aligned)
  *   eps         added to both mean squares
  *   residual_out[T,4,H] bf16 (R'), 16-byte aligned; may be R itself (in place)
@@ -156,7 +161,7 @@ int mhc_quant_ue8m0(const void* x, int64_t rows, int H, float amax_floor, uint8_
  * equal the seam's). */
 int mhc_copy(const void* src, void* dst, size_t bytes, void* stream);
 
-/* mhc_seam() on the split path (cfg->path 0 or 1; path 2 is refused) for
+/* mhc_seam() on the split path (cfg->path 0 or 1; paths 2 and 3 are refused) for
  * callers that cannot allocate device memory: a plug-in inside a host program
  * that owns every device allocation, code running inside an allocator
  * callback, or a loop that must never block in the allocator.  The paper has

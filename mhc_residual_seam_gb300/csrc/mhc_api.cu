@@ -20,8 +20,8 @@ cudaError_t split_launch(const SeamArgs& a, int BT, int Wd, int64_t groups_per_l
 cudaError_t stream_init();
 int stream_cols(int H);
 bool stream_tc_fits(int H);
-cudaError_t stream_launch(const SeamArgs& a, bool tcgen05_proj, cudaStream_t stream, unsigned long long limit_ns,
-                          int* launches);
+cudaError_t stream_launch(const SeamArgs& a, bool tcgen05_proj, int kcl, cudaStream_t stream,
+                          unsigned long long limit_ns, int* launches);
 // mhc_aux.cu
 cudaError_t pack_fn_launch(const float* fn, void* out, int H, cudaStream_t s);
 cudaError_t quant_launch(const void* x, int64_t rows, int H, float floor_, uint8_t* codes, uint8_t* scales,
@@ -35,7 +35,7 @@ constexpr size_t kHeaderBytes = 256;  // status word + padding, at the start of 
 constexpr long long kDefaultSpin = 10000000LL;
 constexpr int kMaxDevices = 64;
 constexpr size_t kSplitMaxSmem = 160 * 1024;
-constexpr int64_t kStreamMinT = 1024;  // auto policy: streaming path from this many tokens
+constexpr int64_t kStreamMinT = 1024;  // auto policy: clusters of 4 from this many tokens, of 16 below
 
 thread_local std::string g_err;
 thread_local int g_launches = 0;
@@ -87,7 +87,7 @@ int ensure_device(cudaStream_t stream, DeviceState** out) {
 }
 
 struct Plan {
-  int path = 1;
+  int path = 1;          // 1 split, 2 streaming (clusters of 4), 3 streaming (clusters of 16)
   bool tc_proj = false;  // streaming path: tcgen05 projection instead of warp-level MMA
   int BT = 8;   // tokens per CTA (split path)
   int Wd = 64;  // columns per CTA (split path)
@@ -99,11 +99,13 @@ int next_pow2(int64_t v) {
   return p;
 }
 
-// Launch policy: a pure function of (T, H, cfg).
-int make_plan(int64_t T, int H, const mhc_config* cfg, Plan* p) {
+// Launch policy: a pure function of (T, H, cfg, whether fn_packed is given).
+// Workspace sizing asks with have_packed = false, so a workspace sized for the
+// automatic policy also fits the split path it falls back to without fn_packed.
+int make_plan(int64_t T, int H, const mhc_config* cfg, bool have_packed, Plan* p) {
   mhc_config c = {};
   if (cfg) c = *cfg;
-  if (c.path < 0 || c.path > 2) return fail(MHC_ERR_CONFIG, "cfg.path must be 0, 1 or 2");
+  if (c.path < 0 || c.path > 3) return fail(MHC_ERR_CONFIG, "cfg.path must be 0, 1, 2 or 3");
   if (c.block_m != 0 && (c.block_m < 0 || c.block_m > 32 || (c.block_m & (c.block_m - 1)) != 0))
     return fail(MHC_ERR_CONFIG, "cfg.block_m must be 0 or a power of two <= 32");
   if (c.cols_per_cta != 0 && (c.cols_per_cta < 32 || c.cols_per_cta % 32 != 0 || c.cols_per_cta > 16384))
@@ -112,11 +114,22 @@ int make_plan(int64_t T, int H, const mhc_config* cfg, Plan* p) {
   if (!(c.amax_floor >= 0.f) || c.amax_floor > 1e30f) return fail(MHC_ERR_CONFIG, "cfg.amax_floor out of range");
   if (c.spin_limit < 0) return fail(MHC_ERR_CONFIG, "cfg.spin_limit must be >= 0");
   if (c.projection < 0 || c.projection > 2) return fail(MHC_ERR_CONFIG, "cfg.projection must be 0, 1 or 2");
-  p->tc_proj = c.projection == 2 || (c.projection == 0 && mhc::stream_tc_fits(H));
-  p->path = (c.path == 2 || (c.path == 0 && T >= kStreamMinT && mhc::stream_cols(H) > 0)) ? 2 : 1;
-  if (p->path == 2) {
-    if (mhc::stream_cols(H) == 0)
-      return fail(MHC_ERR_SHAPE, "the streaming path needs H a multiple of 64 with 512 <= H <= 8192");
+  const bool stream_ok = mhc::stream_cols(H) > 0;
+  p->path = c.path;
+  if (p->path == 0) {  // a split-path knob (block_m, cols_per_cta) picks the split path
+    if (!stream_ok || c.block_m || c.cols_per_cta) p->path = 1;
+    else if (T >= kStreamMinT) p->path = 2;
+    else p->path = (H >= 1024 && have_packed) ? 3 : 1;
+  }
+  if (p->path == 2 || p->path == 3) {
+    if (!stream_ok) return fail(MHC_ERR_SHAPE, "the streaming path needs H a multiple of 64 with 512 <= H <= 8192");
+    if (p->path == 3) {  // at most 8 chunks per CTA: the tcgen05 projection always fits
+      if (c.projection == 1)
+        return fail(MHC_ERR_CONFIG, "the streaming path with clusters of 16 runs the tcgen05 projection only");
+      p->tc_proj = true;
+      return MHC_OK;
+    }
+    p->tc_proj = c.projection == 2 || (c.projection == 0 && mhc::stream_tc_fits(H));
     if (c.projection == 2 && !mhc::stream_tc_fits(H))
       return fail(MHC_ERR_CONFIG, "the tcgen05 projection needs H <= 5120 (tensor memory holds x and the accumulator)");
     return MHC_OK;
@@ -165,7 +178,7 @@ extern "C" {
 
 size_t mhc_workspace_bytes(int64_t T, int H, const mhc_config* cfg) {
   Plan p;
-  if (T < 0 || H <= 0 || make_plan(T, H, cfg, &p) != MHC_OK) return kHeaderBytes;
+  if (T < 0 || H <= 0 || make_plan(T, H, cfg, false, &p) != MHC_OK) return kHeaderBytes;
   return plan_workspace(T, H, p);
 }
 
@@ -211,7 +224,7 @@ int mhc_seam(const void* R, const void* Y, const float* post_prev, const float* 
   if (mx && H % 32 != 0) return fail(MHC_ERR_SHAPE, "mxfp8 output needs H % 32 == 0");
   if (!(eps >= 0.f) || eps > 1e30f) return fail(MHC_ERR_CONFIG, "eps must be finite and >= 0");
   Plan plan;
-  int rc = make_plan(T, H, cfg, &plan);
+  int rc = make_plan(T, H, cfg, fn_packed != nullptr, &plan);
   if (rc != MHC_OK) return rc;
   if (T == 0) return MHC_OK;
   if ((Y == nullptr) != (post_prev == nullptr))
@@ -280,10 +293,11 @@ int mhc_seam(const void* R, const void* Y, const float* post_prev, const float* 
   a.spin_limit = (cfg && cfg->spin_limit) ? cfg->spin_limit : kDefaultSpin;
 
   int launches = 0;
-  if (plan.path == 2) {
+  if (plan.path == 2 || plan.path == 3) {
     if (!fn_packed) return fail(MHC_ERR_NULL, "the streaming path needs fn_packed (mhc_pack_fn) or cfg.path = 1");
     if (T >= ((int64_t)1 << 31)) return fail(MHC_ERR_SHAPE, "the streaming path takes T < 2^31");
-    cudaError_t e = mhc::stream_launch(a, plan.tc_proj, s, (unsigned long long)a.spin_limit * 100ull, &launches);
+    cudaError_t e = mhc::stream_launch(a, plan.tc_proj, plan.path == 3 ? 16 : 4, s,
+                                       (unsigned long long)a.spin_limit * 100ull, &launches);
     if (e == cudaErrorInvalidValue) return fail(MHC_ERR_CUDA, "tensor map encoding failed (streaming path)");
     if (e != cudaSuccess) return cuda_fail(e, "seam launch (streaming path)");
     g_launches = launches;

@@ -57,7 +57,8 @@ int mhc_seam_noalloc(const void* R, const void* Y, const float* post_prev, const
                      float* comb_out, const mhc_config* cfg, void* stream) {
   mhc_config c = {};
   if (cfg) c = *cfg;
-  if (c.path == 2) return noalloc_fail(MHC_ERR_CONFIG, "mhc_seam_noalloc runs the split path only (cfg.path 0 or 1)");
+  if (c.path == 2 || c.path == 3)
+    return noalloc_fail(MHC_ERR_CONFIG, "mhc_seam_noalloc runs the split path only (cfg.path 0 or 1)");
   c.path = 1;
   if (T < 0 || H <= 0) return mhc_seam(R, Y, post_prev, comb_prev, pre_prev, fn, nullptr, bias, alpha, gamma, eps, T,
                                        H, out_mode, residual_out, norm, fp8_codes, e8m0_scales, pre_out, post_out,

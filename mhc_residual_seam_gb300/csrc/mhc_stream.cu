@@ -48,10 +48,9 @@ namespace mhc {
 
 namespace {
 
-constexpr int kCl = 4;                 // CTAs per cluster
 constexpr int kBM = 32;                // tokens per block
 constexpr int kChunk = 64;             // columns per chunk
-constexpr int kNI = 5, kNF = 2, kNO = 2;
+constexpr int kNF = 2, kNO = 2;
 constexpr int kComputeThreads = 256;   // warps 0-7
 constexpr int kThreads = 416;          // + 8 input producer, 9 MMA issuer, 10 fn producer, 11 finisher, 12 store
 constexpr int kFnRows = 48;
@@ -64,20 +63,15 @@ constexpr uint32_t kOffCodesT = 5 * kRTile;            //   then the codes tile 
 constexpr uint32_t kOutStage = 5 * kRTile + kBM * 64;  // 22 KB (a multiple of 1 KB: swizzled tiles)
 constexpr uint32_t kOffFn = 0;
 constexpr uint32_t kOffOut = kOffFn + kNF * kFnStage;
-constexpr uint32_t kOffIn = kOffOut + kNO * kOutStage;
-constexpr uint32_t kOffTail = kOffIn + kNI * kInStage;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColD = 0;                          // tcgen05 accumulator D[128 x 192]
 constexpr uint32_t kDCols = 4 * kFnRows;
 constexpr int kMaxChunksTC = (int)((kTmemCols - kDCols) / 16);  // x: 16 columns per chunk
 constexpr int kMaxChunks = (int)(kTmemCols / 16);
 constexpr uint32_t kIdesc = idesc_bf16_f32(128, kDCols);
-constexpr int kSlots = kBM / kCl;                      // tokens owned per CTA and block
 constexpr int kOwnerParts = 25;                        // sent to a token's owner: 24 projections, s_R
 constexpr int kPartPad = 26;                           // rows of 8-byte aligned pairs
 constexpr int kDPad = 25;                              // odd row stride: conflict-free columns
-constexpr uint32_t kXsBytes = kCl * kBM * 4;           // s_x partials landing in each CTA per block
-constexpr uint32_t kRecvBytes = kCl * kSlots * kOwnerParts * 4;  // owner partials per CTA per block
 
 // Carried gates of one block, TMA-loaded a block ahead: comb [32 x 16],
 // pre [32 x 4], post [32 x 4] fp32.
@@ -87,32 +81,44 @@ struct alignas(128) GateTile {
   float post[kBM][4];
 };
 
-struct Tail {
-  GateTile gates[2];                     // [block parity]
-  uint64_t in_full[kNI], in_empty[kNI], fn_full[kNF], fn_empty[kNF], out_full[kNO], out_empty[kNO];
-  uint64_t d_full, xs_full[2], recv_full[2], recv_free[2], gates_full[2], gates_empty[2];
-  uint64_t red_full[2], dbuf_full, dbuf_free, d_free;
-  uint32_t tmem_base;
-  volatile int err;
-  float2 red[2][8][kBM];                 // [block parity][compute warp][token]: s_R, s_x partials
-  float dbuf[4][kBM][kDPad];             // the block's projection per stream (hi + lo): [stream][token][logit]
-  float xs[2][kCl][kBM];                 // [block parity][source CTA][token]: s_x partial
-  float recv[2][kCl][kSlots][kPartPad];  // [block parity][source CTA][owned token][part]
-  uint4 gam[kMaxChunksTC][8];            // gamma of this CTA's chunks (8 bf16 per compute warp)
+// Geometry of a cluster of KCL CTAs: 4 for large T (bandwidth), 16 for small T
+// (each CTA takes a quarter of the columns it would take in a cluster of 4).
+template <int KCL>
+struct Geo {
+  static constexpr int kCl = KCL;
+  static constexpr int kNI = KCL == 4 ? 5 : 4;          // input stages
+  static constexpr int kSlots = kBM / KCL;              // tokens owned per CTA and block
+  static constexpr int kGamChunks = KCL == 4 ? kMaxChunksTC : (kMaxChunks * 4) / KCL;  // gamma staged in smem
+  static constexpr uint32_t kXsBytes = KCL * kBM * 4;   // s_x partials landing in each CTA per block
+  static constexpr uint32_t kRecvBytes = KCL * kSlots * kOwnerParts * 4;  // owner partials per CTA per block
+  static constexpr uint32_t kOffIn = kOffOut + kNO * kOutStage;
+  static constexpr uint32_t kOffTail = kOffIn + kNI * kInStage;
+  struct Tail {
+    GateTile gates[2];                     // [block parity]
+    uint64_t in_full[kNI], in_empty[kNI], fn_full[kNF], fn_empty[kNF], out_full[kNO], out_empty[kNO];
+    uint64_t d_full, xs_full[2], recv_full[2], recv_free[2], gates_full[2], gates_empty[2];
+    uint64_t red_full[2], dbuf_full, dbuf_free, d_free;
+    uint32_t tmem_base;
+    volatile int err;
+    float2 red[2][8][kBM];                 // [block parity][compute warp][token]: s_R, s_x partials
+    float dbuf[4][kBM][kDPad];             // the block's projection per stream (hi + lo): [stream][token][logit]
+    float xs[2][KCL][kBM];                 // [block parity][source CTA][token]: s_x partial
+    float recv[2][KCL][kSlots][kPartPad];  // [block parity][source CTA][owned token][part]
+    uint4 gam[kGamChunks][8];              // gamma of this CTA's first chunks (8 bf16 per compute warp)
+  };
+  static constexpr size_t kSmemBytes = kOffTail + sizeof(Tail) + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory of the streaming kernel exceeds 227 KB");
 };
-
-constexpr size_t kSmemBytes = kOffTail + sizeof(Tail) + 1024;
-static_assert(kSmemBytes <= 232448, "shared memory of the streaming kernel exceeds 227 KB");
 
 struct Ctx {
   const SeamArgs* a;
-  Tail* tl;
+  volatile int* err;  // the CTA's error flag in shared memory
   uint64_t limit_ns;
 };
 
 __device__ __forceinline__ void flag_error(const Ctx& x) {
-  if (!x.tl->err) {
-    x.tl->err = 1;
+  if (!*x.err) {
+    *x.err = 1;
     atomicOr(x.a->status, 2u);
   }
 }
@@ -121,7 +127,7 @@ __device__ __forceinline__ void wait_local(const Ctx& x, uint64_t* bar, uint32_t
   if (mbar_test_wait(bar, parity)) return;
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity, 20000)) {
-    if (x.tl->err) return;
+    if (*x.err) return;
     if (globaltimer_ns() - t0 > x.limit_ns) {
       flag_error(x);
       return;
@@ -132,7 +138,7 @@ __device__ __forceinline__ void wait_remote(const Ctx& x, uint64_t* bar, uint32_
   if (mbar_try_wait_cluster(bar, parity, 0)) return;
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait_cluster(bar, parity, 20000)) {
-    if (x.tl->err) return;
+    if (*x.err) return;
     if (globaltimer_ns() - t0 > x.limit_ns) {
       flag_error(x);
       return;
@@ -150,8 +156,8 @@ __device__ __noinline__ void finish_store_gates(const SeamArgs& a, int64_t t, co
   store_gates(a, t, pre, post, cb);
 }
 
-template <bool POST, bool MXFP8, bool MS>
-__global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
+template <bool POST, bool MXFP8, bool MS, int KCL>
+__global__ void __launch_bounds__(kThreads, 1)
     stream_seam_kernel(const SeamArgs a, const __grid_constant__ CUtensorMap tmR,
                        const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmRo,
                        const __grid_constant__ CUtensorMap tmFn, const __grid_constant__ CUtensorMap tmN,
@@ -160,8 +166,11 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
                        int n_blocks, unsigned long long limit_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Tail* tl = reinterpret_cast<Tail*>(sm + kOffTail);
-  const Ctx X{&a, tl, limit_ns};
+  using G = Geo<KCL>;
+  constexpr int kCl = G::kCl, kNI = G::kNI, kSlots = G::kSlots;
+  constexpr uint32_t kOffIn = G::kOffIn, kXsBytes = G::kXsBytes, kRecvBytes = G::kRecvBytes;
+  typename G::Tail* tl = reinterpret_cast<typename G::Tail*>(sm + G::kOffTail);
+  const Ctx X{&a, &tl->err, limit_ns};
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_ctarank();
@@ -216,7 +225,7 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
     if (MXFP8) prefetch_tmap(&tmC);
   }
   // gamma of this CTA's first chunks, staged once (read by every block)
-  for (int i = tid; i < min(nch, kMaxChunksTC) * 8; i += kThreads)
+  for (int i = tid; i < min(nch, G::kGamChunks) * 8; i += kThreads)
     tl->gam[i >> 3][i & 7] = __ldg(reinterpret_cast<const uint4*>(a.gamma + ((i >> 3) * kCl + (int)rank) * kChunk) + (i & 7));
   if (warp == 9) {
     tmem_alloc(&tl->tmem_base, kTmemCols);
@@ -565,7 +574,7 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
         uint4 gv = make_uint4(0, 0, 0, 0);
         if (prev) {
           tc_ld_x8_issue(xaddr + 16 * c, xr);
-          gv = c < kMaxChunksTC ? tl->gam[c][warp]
+          gv = c < G::kGamChunks ? tl->gam[c][warp]
                                 : __ldg(reinterpret_cast<const uint4*>(a.gamma + (c * kCl + (int)rank) * kChunk + 8 * warp));
         }
         if (real) {
@@ -697,23 +706,26 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------- host side --
-template <bool MS>
-static void* stream_kernel_ptr_(bool post, bool mxfp8) {
-  if (post) return mxfp8 ? (void*)stream_seam_kernel<true, true, MS> : (void*)stream_seam_kernel<true, false, MS>;
-  return mxfp8 ? (void*)stream_seam_kernel<false, true, MS> : (void*)stream_seam_kernel<false, false, MS>;
+template <bool MS, int KCL>
+static void* kptr_(bool post, bool mxfp8) {
+  if (post) return mxfp8 ? (void*)stream_seam_kernel<true, true, MS, KCL> : (void*)stream_seam_kernel<true, false, MS, KCL>;
+  return mxfp8 ? (void*)stream_seam_kernel<false, true, MS, KCL> : (void*)stream_seam_kernel<false, false, MS, KCL>;
 }
-static void* stream_kernel_ptr(bool post, bool mxfp8, bool ms) {
-  return ms ? stream_kernel_ptr_<true>(post, mxfp8) : stream_kernel_ptr_<false>(post, mxfp8);
+// Clusters of 16 run only the tcgen05 projection (at most 8 chunks per CTA).
+static void* stream_kernel_ptr(bool post, bool mxfp8, bool ms, int kcl) {
+  if (kcl == 16) return kptr_<false, 16>(post, mxfp8);
+  return ms ? kptr_<true, 4>(post, mxfp8) : kptr_<false, 4>(post, mxfp8);
 }
-
-size_t stream_smem_bytes() { return kSmemBytes; }
+static size_t smem_bytes(int kcl) { return kcl == 16 ? Geo<16>::kSmemBytes : Geo<4>::kSmemBytes; }
 
 cudaError_t stream_init() {
   for (int p = 0; p < 2; ++p)
     for (int m = 0; m < 2; ++m)
-      for (int v = 0; v < 2; ++v) {
-        cudaError_t e = cudaFuncSetAttribute(stream_kernel_ptr(p, m, v), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSmemBytes);
+      for (int v = 0; v < 3; ++v) {  // v: 0 tcgen05 / 4, 1 warp MMA / 4, 2 tcgen05 / 16
+        const int kcl = v == 2 ? 16 : 4;
+        void* k = stream_kernel_ptr(p, m, v == 1, kcl);
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes(kcl));
+        if (e == cudaSuccess && kcl == 16) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
       }
   return cudaSuccess;
@@ -723,7 +735,7 @@ cudaError_t stream_init() {
 // when the streaming path cannot take H.
 int stream_cols(int H) {
   if (H % kChunk != 0 || H < 512) return 0;
-  const int chunks = (H / kChunk + kCl - 1) / kCl;
+  const int chunks = (H / kChunk + 3) / 4;
   if (chunks > kMaxChunks) return 0;
   return chunks * kChunk;
 }
@@ -760,33 +772,37 @@ static bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void*
              sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Clusters that fit at once, per device (queried once).
-static int max_clusters(void* kernel) {
-  static int cache[2][64] = {};
+// Clusters that fit at once, per device and kernel variant (queried once).
+static int max_clusters(bool post, bool mxfp8, bool ms, int kcl) {
+  static int cache[12][64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  const int v = (kernel == stream_kernel_ptr(true, false, true) || kernel == stream_kernel_ptr(true, true, true) ||
-                 kernel == stream_kernel_ptr(false, false, true) || kernel == stream_kernel_ptr(false, true, true))
-                    ? 0
-                    : 1;
+  const int v = (post ? 1 : 0) + (mxfp8 ? 2 : 0) + 4 * (kcl == 16 ? 2 : (ms ? 1 : 0));
   if (cache[v][dev] > 0) return cache[v][dev];
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(kCl, 1, 1);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)kcl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)kcl, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem_bytes(kcl);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveClusters(&n, stream_kernel_ptr(post, mxfp8, ms, kcl), &cfg) != cudaSuccess) return 0;
   cache[v][dev] = n;
   return n;
 }
 
 // Returns cudaSuccess, or cudaErrorInvalidValue when a tensor map cannot be
-// encoded or no cluster fits (the caller reports it).
-cudaError_t stream_launch(const SeamArgs& a, bool tcgen05_proj, cudaStream_t stream, unsigned long long limit_ns,
-                          int* launches) {
+// encoded or no cluster fits (the caller reports it).  kcl: CTAs per cluster
+// (4, or 16 with the tcgen05 projection).
+cudaError_t stream_launch(const SeamArgs& a, bool tcgen05_proj, int kcl, cudaStream_t stream,
+                          unsigned long long limit_ns, int* launches) {
   const int H = a.H;
-  const int W = stream_cols(H);
-  if (W == 0) return cudaErrorInvalidValue;
+  if (stream_cols(H) == 0 || (kcl != 4 && kcl != 16) || (kcl == 16 && !tcgen05_proj)) return cudaErrorInvalidValue;
   const cuuint64_t T = (cuuint64_t)a.T;
   CUtensorMap mR, mY, mRo, mFn, mN, mC;
   const cuuint64_t d3[3] = {(cuuint64_t)H, 4, T};
@@ -815,16 +831,24 @@ cudaError_t stream_launch(const SeamArgs& a, bool tcgen05_proj, cudaStream_t str
                encode(&mGq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.post_prev ? a.post_prev : a.pre_prev, dG4, sG4, bG4,
                       CU_TENSOR_MAP_SWIZZLE_NONE);
   if (!ok) return cudaErrorInvalidValue;
-  void* k = stream_kernel_ptr(a.Y != nullptr, a.codes != nullptr, !tcgen05_proj);
+  const bool post = a.Y != nullptr, mx = a.codes != nullptr, ms = !tcgen05_proj;
+  void* k = stream_kernel_ptr(post, mx, ms, kcl);
   const int n_blocks = (int)((a.T + kBM - 1) / kBM);
-  const int fit = max_clusters(k);
+  const int fit = max_clusters(post, mx, ms, kcl);
   if (fit <= 0) return cudaErrorInvalidValue;
   const int ncl = n_blocks < fit ? n_blocks : fit;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(ncl * kCl), 1, 1);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)kcl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)(ncl * kcl), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem_bytes(kcl);
   cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   int nb = n_blocks;
   void* args[] = {const_cast<SeamArgs*>(&a), &mR, &mY, &mRo, &mFn, &mN, &mC, &mGc, &mGp, &mGq, &nb, &limit_ns};
   cudaError_t e = cudaLaunchKernelExC(&cfg, k, args);

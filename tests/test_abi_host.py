@@ -92,19 +92,26 @@ def test_workspace_rules(L):
 
 
 def test_config_validation(L):
-    for bad in (dict(path=5), dict(block_m=3), dict(block_m=64), dict(cols_per_cta=48), dict(spin_limit=-1),
+    for bad in (dict(path=5), dict(path=-1), dict(block_m=3), dict(block_m=64), dict(cols_per_cta=48), dict(spin_limit=-1),
                 dict(sinkhorn_iters=-2), dict(amax_floor=-1.0), dict(projection=3)):
         cfg = B.MhcConfig(**bad)
         assert _seam(L, cfg=C.byref(cfg)) == -10, bad
+    cfg = B.MhcConfig(path=3, projection=1)     # clusters of 16 run the tcgen05 projection only
+    assert _seam(L, H=5120, fn_packed=FAKE + 0xF00000, cfg=C.byref(cfg)) == -10
 
 
 def test_workspace_grows_with_tokens_and_columns(L):
-    a = L.mhc_workspace_bytes(4, 5120, None)
-    b = L.mhc_workspace_bytes(64, 5120, None)
-    c = L.mhc_workspace_bytes(1024, 5120, None)          # streaming path: status word only
     p1 = B.MhcConfig(path=1)
-    d = L.mhc_workspace_bytes(1024, 5120, C.byref(p1))   # split path forced
+    a = L.mhc_workspace_bytes(4, 5120, C.byref(p1))      # split path forced
+    b = L.mhc_workspace_bytes(64, 5120, C.byref(p1))
+    c = L.mhc_workspace_bytes(1024, 5120, None)          # streaming path: status word only
+    d = L.mhc_workspace_bytes(1024, 5120, C.byref(p1))
     assert 256 < a < b < d and c == 256
+    # small T: the automatic policy's workspace also covers the split path it
+    # takes without fn_packed; clusters of 16 need only the status word
+    assert L.mhc_workspace_bytes(4, 5120, None) == a
+    p3 = B.MhcConfig(path=3)
+    assert L.mhc_workspace_bytes(4, 5120, C.byref(p3)) == 256
     cfg = B.MhcConfig(block_m=8, cols_per_cta=64)
     assert L.mhc_workspace_bytes(64, 5120, C.byref(cfg)) == 256 + 8 * (((64 + 128 + 80 * 8 * 128) + 255) // 256 * 256)
 

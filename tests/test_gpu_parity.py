@@ -309,6 +309,50 @@ def test_stream_requires_packed_fn_and_supported_width():
     assert e.value.code == -2
 
 
+# ------------------------------------- streaming path, clusters of 16 (path 3) --
+STREAM16 = dict(path=3)
+
+
+@pytest.mark.parametrize("T", [1, 31, 32, 33, 257, 1000, 1100])
+def test_stream16_ragged_tokens(T):
+    d = make_case(T, 5120, 7800 + T)
+    compare(d, to_host(run_gpu(d, cfg=B.MhcConfig(**STREAM16))))
+
+
+@pytest.mark.parametrize("H", [512, 576, 1024, 4096, 7168, 8192])
+@pytest.mark.parametrize("mx", [False, True])
+def test_stream16_widths(H, mx):
+    # H = 512 and 576 leave CTAs of the cluster without a chunk
+    d = make_case(45, H, 7900 + H, mxfp8=mx)
+    compare(d, to_host(run_gpu(d, cfg=B.MhcConfig(**STREAM16))))
+
+
+def test_stream16_no_post_in_place_and_crafted():
+    d = make_case(100, 5120, 8000, post=False)
+    compare(d, to_host(run_gpu(d, cfg=B.MhcConfig(**STREAM16), inplace=True)))
+    d = make_case(128, 5120, 8001, mxfp8=True, craft=True)
+    h = to_host(run_gpu(d, cfg=B.MhcConfig(**STREAM16)))
+    compare(d, h)
+    g = I.bf16_bits(d["gamma"])
+    for t in d["crafted_rows"]:
+        for grp in d["crafted_groups"]:
+            sl = slice(32 * grp, 32 * grp + 32)
+            assert np.array_equal(h["norm"][t, sl], g[sl]), (t, grp)
+
+
+def test_stream16_refuses_warp_mma():
+    d = make_case(8, 5120, 8002)
+    with pytest.raises(B.MhcError) as e:
+        run_gpu(d, cfg=B.MhcConfig(path=3, projection=1))
+    assert e.value.code == -10
+
+
+@pytest.mark.parametrize("T,post", [(4, True), (64, True), (64, False)])
+def test_split_path_on_the_decode_configs(T, post):
+    d = make_case(T, 5120, 8100 + T, post=post)
+    compare(d, to_host(run_gpu(d, cfg=B.MhcConfig(path=1))))
+
+
 @pytest.mark.parametrize("proj", [1, 2])
 @pytest.mark.parametrize("T,H,mx,post", [(300, 5120, False, True), (97, 4096, True, True), (64, 7168, False, False)])
 def test_stream_projection_variants(proj, T, H, mx, post):
