@@ -121,11 +121,19 @@ __device__ __forceinline__ uint8_t quant_group32(const uint32_t* nb, uint32_t* c
 }
 
 // ---------------------------------------------------------------- finish --
+// Hardware reciprocal (rcp.approx.ftz.f32, within about 1 ulp): the shortest
+// dependent step of the Sinkhorn chain.
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
 // Gate finish of one token from its reduced partial sums (s_R over 4H, the
 // 24 projections d[k]).  Logit order [pre 0..3 | post 4..7 | comb 8..23
 // row-major], alpha[0] pre, alpha[1] post, alpha[2] comb.  The Sinkhorn runs
 // on exp(l - rowmax): the row scale cancels in the first row normalisation.
-// Reciprocals use the hardware approximation (__fdividef, a few ulp): the 160
+// Reciprocals use the hardware approximation (about 1 ulp): the 160
 // normalisations of the Sinkhorn are a serial chain per token, and the gates
 // are checked to 1e-3.
 __device__ __forceinline__ void finish_gates(float sR, const float* d, const float* alpha,
@@ -135,8 +143,8 @@ __device__ __forceinline__ void finish_gates(float sR, const float* d, const flo
   float a0 = alpha[0] * rstdR, a1 = alpha[1] * rstdR, a2 = alpha[2] * rstdR;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    pre[i] = __fdividef(1.0f, 1.0f + expf(-(a0 * d[i] + bias[i])));
-    post[i] = __fdividef(2.0f, 1.0f + expf(-(a1 * d[4 + i] + bias[4 + i])));
+    pre[i] = rcp_approx(1.0f + expf(-(a0 * d[i] + bias[i])));
+    post[i] = 2.0f * rcp_approx(1.0f + expf(-(a1 * d[4 + i] + bias[4 + i])));
   }
   float M[16];
 #pragma unroll
@@ -153,13 +161,13 @@ __device__ __forceinline__ void finish_gates(float sR, const float* d, const flo
   for (int it = 0; it < iters; ++it) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      float s = __fdividef(1.0f, (M[4 * i] + M[4 * i + 1]) + (M[4 * i + 2] + M[4 * i + 3]));
+      float s = rcp_approx((M[4 * i] + M[4 * i + 1]) + (M[4 * i + 2] + M[4 * i + 3]));
 #pragma unroll
       for (int j = 0; j < 4; ++j) M[4 * i + j] *= s;
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      float s = __fdividef(1.0f, (M[j] + M[4 + j]) + (M[8 + j] + M[12 + j]));
+      float s = rcp_approx((M[j] + M[4 + j]) + (M[8 + j] + M[12 + j]));
 #pragma unroll
       for (int i = 0; i < 4; ++i) M[4 * i + j] *= s;
     }
