@@ -1,11 +1,12 @@
-// Streaming path of the delayed mHC seam: bandwidth-tuned for large T.
+// Streaming path of the delayed mHC seam: bandwidth-tuned for large T, and
+// latency-tuned for small T with larger clusters.
 //
-// Persistent clusters of 4 CTAs (one CTA per SM).  CTA r of a cluster owns
-// the 64-column chunks r, r + 4, r + 8, ... of H for all four streams (the
-// cluster reads each row in 512-byte runs) and the cluster walks blocks of 32
-// tokens.  Per 64-column chunk:
+// Persistent clusters of KCL CTAs (4, or 16 for small T; one CTA per SM).
+// CTA r of a cluster owns the 64-column chunks r, r + KCL, r + 2 KCL, ... of H
+// for all four streams (the cluster reads each row in long runs) and the
+// cluster walks blocks of 32 tokens.  Per 64-column chunk:
 //  - an input producer warp TMA-loads the four R tiles and the Y tile into a
-//    ring of 5 input stages (128-byte swizzle, L2 evict-first), and each
+//    ring of input stages (128-byte swizzle, L2 evict-first), and each
 //    block's carried gates (comb, pre, post) into a double buffer as it
 //    starts the block, so they wait in shared memory when compute gets there;
 //  - an fn producer warp TMA-loads the four hi/lo-packed fn tiles [48 x 64]
@@ -26,13 +27,15 @@
 //    MMAs in the compute warps;
 //  - a store warp TMA-stores the R' tiles and the norm tile of each stage
 //    (and computes the ue8m0 codes of the norm tile).
-// After the last chunk of a block each CTA sends, through distributed shared
-// memory (st.async completing bytes on the receiver's mbarrier):
-//  - its per-token s_x partials to all four CTAs, which each sum the four in
-//    the same order into rstd_x, needed by the first chunk of the next block;
-//  - its 24 projection partials and s_R of each token to the token's owner
-//    CTA (token % 4), whose finisher warp computes the gates off the critical
-//    path.
+// After the last chunk of a block the compute warps hand their partial sums
+// over in shared memory and go on; an exchange warp sends, through
+// distributed shared memory (st.async completing bytes on the receiver's
+// mbarrier):
+//  - the CTA's per-token s_x partials to every CTA of the cluster, which each
+//    sum them in the same order into rstd_x, needed by the next block's first
+//    chunk;
+//  - the 24 projection sums and s_R of each token to the token's owner CTA
+//    (token % KCL), whose exchange warp then computes the gates.
 // ("[FlyDSL] Single-launch Mega-mHC on gfx950", Kernel Architecture: split-K
 // with a distributed finish; here the cluster launch makes every CTA of a
 // split co-resident.)
