@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tmFn, const __grid_constant__ CUtensorMap tmN,
                        const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmGc,
                        const __grid_constant__ CUtensorMap tmGp, const __grid_constant__ CUtensorMap tmGq,
-                       int n_blocks, unsigned long long limit_ns) {
+                       int block0, int n_blocks, unsigned long long limit_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   using G = Geo<KCL>;
@@ -186,7 +186,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n64 = H / kChunk;
   const int nch = n64 > (int)rank ? (n64 - (int)rank + kCl - 1) / kCl : 0;
   const int cid = blockIdx.x / kCl, ncl = gridDim.x / kCl;
-  const int nblk = cid < n_blocks ? (n_blocks - cid + ncl - 1) / ncl : 0;  // blocks of this cluster
+  // this launch's blocks are block0 .. block0 + n_blocks - 1; cluster cid takes
+  // every ncl-th of them, starting with its own index
+  const int nblk = cid < n_blocks ? (n_blocks - cid + ncl - 1) / ncl : 0;
+  const int bb = block0 + cid;
 
   if (tid == 0) {
     for (int s = 0; s < kNI; ++s) {
@@ -249,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t bytes = (POST ? 5 : 4) * kRTile;
       int j = 0;
       for (int lb = 0; lb < nblk; ++lb) {
-        const int t0 = (cid + lb * ncl) * kBM;
+        const int t0 = (bb + lb * ncl) * kBM;
         {  // the block's carried gates, consumed at the top of its compute
           const int gp = lb & 1;
           wait_local(X, &tl->gates_empty[gp], ((lb >> 1) & 1) ^ 1);
@@ -329,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int j = 0;
     for (int lb = 0; lb <= nblk; ++lb) {
       const bool real = lb < nblk, prev = lb > 0;
-      const int t0 = (cid + lb * ncl) * kBM, tp = (cid + (lb - 1) * ncl) * kBM;
+      const int t0 = (bb + lb * ncl) * kBM, tp = (bb + (lb - 1) * ncl) * kBM;
       for (int c = 0; c < nch; ++c, ++j) {
         const int o = j % kNO;
         uint8_t* ost = sm + kOffOut + o * kOutStage;
@@ -385,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane < 27) tl->ab[lane] = lane < 3 ? a.alpha[lane] : a.bias[lane - 3];
     __syncwarp();
     for (int lb = 0; lb < nblk; ++lb) {
-      const int b = cid + lb * ncl, par = lb & 1;
+      const int b = bb + lb * ncl, par = lb & 1;
       wait_local(X, &tl->red_full[par], (lb >> 1) & 1);
       float sx = 0.f, sR = 0.f;
 #pragma unroll
@@ -501,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float sx = 0.f;
 #pragma unroll
       for (int src = 0; src < kCl; ++src) sx += tl->xs[pp][src][lane];
-      const int64_t tt = (int64_t)(cid + lbp * ncl) * kBM + lane;
+      const int64_t tt = (int64_t)(bb + lbp * ncl) * kBM + lane;
       rprev = tt < T ? 1.0f / sqrtf(sx / (float)H + a.eps) : 0.f;
     };
 
@@ -805,6 +808,8 @@ static int max_clusters(bool post, bool mxfp8, bool ms, int kcl) {
 
 static cudaError_t launch_with_maps(const SeamArgs& a, const CUtensorMap* m, bool tcgen05_proj, int kcl,
                                     cudaStream_t stream, unsigned long long limit_ns, int* launches);
+static cudaError_t launch_range(const SeamArgs& a, const CUtensorMap* m, bool tcgen05_proj, int kcl, int block0,
+                                int n_blocks, cudaStream_t stream, unsigned long long limit_ns, int* launches);
 
 // Returns cudaSuccess, or cudaErrorInvalidValue when a tensor map cannot be
 // encoded or no cluster fits (the caller reports it).  kcl: CTAs per cluster
@@ -868,11 +873,34 @@ cudaError_t stream_launch(const SeamArgs& a, bool tcgen05_proj, int kcl, cudaStr
   return launch_with_maps(a, c.m, tcgen05_proj, kcl, stream, limit_ns, launches);
 }
 
+// One seam call: a single launch, or, when the clusters of 4 would end with a
+// partial round of at most as many blocks as clusters of 16 fit, the full
+// rounds over clusters of 4 and that last round as a second launch over
+// clusters of 16 (a quarter of the columns per CTA, so it takes about a
+// quarter of the time).
 static cudaError_t launch_with_maps(const SeamArgs& a, const CUtensorMap* m, bool tcgen05_proj, int kcl,
                                     cudaStream_t stream, unsigned long long limit_ns, int* launches) {
+  const int n_blocks = (int)((a.T + kBM - 1) / kBM);
+  if (kcl == 4) {
+    const bool post = a.Y != nullptr, mx = a.codes != nullptr;
+    const int fit4 = max_clusters(post, mx, !tcgen05_proj, 4);
+    const int fit16 = max_clusters(post, mx, false, 16);
+    if (fit4 > 0 && fit16 > 0) {
+      const int full = n_blocks / fit4 * fit4, rest = n_blocks - full;
+      if (full > 0 && rest > 0 && rest <= fit16) {
+        cudaError_t e = launch_range(a, m, tcgen05_proj, 4, 0, full, stream, limit_ns, launches);
+        if (e != cudaSuccess) return e;
+        return launch_range(a, m, true, 16, full, rest, stream, limit_ns, launches);
+      }
+    }
+  }
+  return launch_range(a, m, tcgen05_proj, kcl, 0, n_blocks, stream, limit_ns, launches);
+}
+
+static cudaError_t launch_range(const SeamArgs& a, const CUtensorMap* m, bool tcgen05_proj, int kcl, int block0,
+                                int n_blocks, cudaStream_t stream, unsigned long long limit_ns, int* launches) {
   const bool post = a.Y != nullptr, mx = a.codes != nullptr, ms = !tcgen05_proj;
   void* k = stream_kernel_ptr(post, mx, ms, kcl);
-  const int n_blocks = (int)((a.T + kBM - 1) / kBM);
   const int fit = max_clusters(post, mx, ms, kcl);
   if (fit <= 0) return cudaErrorInvalidValue;
   const int ncl = n_blocks < fit ? n_blocks : fit;
@@ -888,11 +916,11 @@ static cudaError_t launch_with_maps(const SeamArgs& a, const CUtensorMap* m, boo
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  int nb = n_blocks;
+  int b0 = block0, nb = n_blocks;
   void* args[] = {const_cast<SeamArgs*>(&a),    const_cast<CUtensorMap*>(m),     const_cast<CUtensorMap*>(m + 1),
                   const_cast<CUtensorMap*>(m + 2), const_cast<CUtensorMap*>(m + 3), const_cast<CUtensorMap*>(m + 4),
                   const_cast<CUtensorMap*>(m + 5), const_cast<CUtensorMap*>(m + 6), const_cast<CUtensorMap*>(m + 7),
-                  const_cast<CUtensorMap*>(m + 8), &nb, &limit_ns};
+                  const_cast<CUtensorMap*>(m + 8), &b0, &nb, &limit_ns};
   cudaError_t e = cudaLaunchKernelExC(&cfg, k, args);
   if (e == cudaSuccess) ++*launches;
   return e;
