@@ -64,6 +64,11 @@ constexpr uint32_t kInStage = 5 * kRTile;              // 20 KB: R tiles 0-3, Y 
 constexpr uint32_t kOffNormT = 4 * kRTile;             // output stage: R' tiles 0-3, then the norm tile,
 constexpr uint32_t kOffCodesT = 5 * kRTile;            //   then the codes tile [32 x 64] u8
 constexpr uint32_t kOutStage = 5 * kRTile + kBM * 64;  // 22 KB (a multiple of 1 KB: swizzled tiles)
+// The normalise-only pass after a cluster's last block puts the norm tiles of
+// kNormGroup chunks in one output stage (in the R' tile slots; with mxfp8 the
+// codes tiles go where the norm tile sits in the other passes).
+template <bool MXFP8>
+__host__ __device__ constexpr int norm_group() { return MXFP8 ? 2 : 4; }
 constexpr uint32_t kOffFn = 0;
 constexpr uint32_t kOffOut = kOffFn + kNF * kFnStage;
 constexpr uint32_t kTmemCols = 512;
@@ -301,15 +306,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------- tcgen05 projection (one thread) --
     if (!MS && lane == 0) {
       int j = 0, jr = 0;
-      for (int lb = 0; lb <= nblk; ++lb) {  // the last pass only normalises (no R')
-        const bool real = lb < nblk;
+      for (int lb = 0; lb <= nblk; ++lb) {
+        if (lb == nblk) {  // the normalise-only pass: one stage per group of chunks, no MMA
+          for (int c0 = 0; c0 < nch; c0 += norm_group<MXFP8>(), ++j) {
+            wait_local(X, &tl->out_full[j % kNO], (j / kNO) & 1);
+            mbar_arrive(&tl->out_empty[j % kNO]);
+          }
+          break;
+        }
         for (int c = 0; c < nch; ++c, ++j) {
           const int o = j % kNO;
           wait_local(X, &tl->out_full[o], (j / kNO) & 1);
-          if (!real) {
-            mbar_arrive(&tl->out_empty[o]);
-            continue;
-          }
           const int f = jr % kNF;
           // the first MMA of a block overwrites D: the previous block's D must have been read
           if (c == 0 && lb > 0) wait_local(X, &tl->d_free, (lb - 1) & 1);
@@ -330,32 +337,63 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 12) {
     // ---------------------------- stores: R' tiles, norm tile, ue8m0 codes --
     int j = 0;
+    // lane = token: the ue8m0 codes of one norm tile (two 32-column groups)
+    auto quant_tile = [&](const uint8_t* nt, uint8_t* ct, int64_t tp, int h) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t nb[16];
+#pragma unroll
+        for (int jq = 0; jq < 4; ++jq) {
+          const int ch = 4 * half + jq;
+          uint4 v = *reinterpret_cast<const uint4*>(nt + lane * 128 + ((ch ^ (lane & 7)) << 4));
+          nb[4 * jq] = v.x; nb[4 * jq + 1] = v.y; nb[4 * jq + 2] = v.z; nb[4 * jq + 3] = v.w;
+        }
+        uint32_t cw[8];
+        const uint8_t sb = quant_group32(nb, cw, a.amax_floor);
+        uint4* cd = reinterpret_cast<uint4*>(ct + lane * 64 + 32 * half);
+        cd[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+        cd[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+        const int64_t tt = tp + lane;
+        if (tt < T) a.scales[tt * (H / 32) + (h + 32 * half) / 32] = sb;
+      }
+    };
     for (int lb = 0; lb <= nblk; ++lb) {
       const bool real = lb < nblk, prev = lb > 0;
       const int t0 = (bb + lb * ncl) * kBM, tp = (bb + (lb - 1) * ncl) * kBM;
+      if (!real) {  // the normalise-only pass: the norm tiles of a group of chunks per stage
+        constexpr int G = norm_group<MXFP8>();
+        for (int c0 = 0; c0 < nch && prev; c0 += G, ++j) {
+          const int o = j % kNO;
+          uint8_t* ost = sm + kOffOut + o * kOutStage;
+          wait_local(X, &tl->out_full[o], (j / kNO) & 1);
+          const int ng = min(G, nch - c0);
+          if (MXFP8) {
+            for (int g = 0; g < ng; ++g)
+              quant_tile(ost + g * kRTile, ost + kOffNormT + g * 2048, tp, ((c0 + g) * kCl + (int)rank) * kChunk);
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+          if (lane == 0) {
+            for (int g = 0; g < ng; ++g) {
+              const int h = ((c0 + g) * kCl + (int)rank) * kChunk;
+              tma_store_2d(&tmN, ost + g * kRTile, h, tp);
+              if (MXFP8) tma_store_2d(&tmC, ost + kOffNormT + g * 2048, h, tp);
+            }
+            tma_store_commit();
+            tma_store_wait_read_all();
+            mbar_arrive(&tl->out_empty[o]);
+          }
+          __syncwarp();
+        }
+        break;
+      }
       for (int c = 0; c < nch; ++c, ++j) {
         const int o = j % kNO;
         uint8_t* ost = sm + kOffOut + o * kOutStage;
         const int h = (c * kCl + (int)rank) * kChunk;
         wait_local(X, &tl->out_full[o], (j / kNO) & 1);
-        if (MXFP8 && prev) {  // lane = token; two 32-column groups each
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t nb[16];
-#pragma unroll
-            for (int jq = 0; jq < 4; ++jq) {
-              const int ch = 4 * half + jq;
-              uint4 v = *reinterpret_cast<const uint4*>(ost + kOffNormT + lane * 128 + ((ch ^ (lane & 7)) << 4));
-              nb[4 * jq] = v.x; nb[4 * jq + 1] = v.y; nb[4 * jq + 2] = v.z; nb[4 * jq + 3] = v.w;
-            }
-            uint32_t cw[8];
-            const uint8_t sb = quant_group32(nb, cw, a.amax_floor);
-            uint4* cd = reinterpret_cast<uint4*>(ost + kOffCodesT + lane * 64 + 32 * half);
-            cd[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-            cd[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-            const int64_t tt = (int64_t)tp + lane;
-            if (tt < T) a.scales[tt * (H / 32) + (h + 32 * half) / 32] = sb;
-          }
+        if (MXFP8 && prev) {
+          quant_tile(ost + kOffNormT, ost + kOffCodesT, tp, h);
           fence_proxy_async_smem();
           __syncwarp();
         }
@@ -538,6 +576,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     int j = 0, ji = 0;
     for (int lb = 0; lb <= nblk; ++lb) {  // the last pass only normalises the last block
       const bool real = lb < nblk, prev = lb > 0;
+      if (!real) {  // the normalise-only pass: the norm tiles of a group of chunks per output stage
+        if (prev) {
+          take_rstd(lb - 1);
+          constexpr int NG = norm_group<MXFP8>();
+          for (int c0 = 0; c0 < nch; c0 += NG, ++j) {
+            const int o = j % kNO;
+            wait_local(X, &tl->out_empty[o], ((j / kNO) & 1) ^ 1);
+            uint8_t* ost = sm + kOffOut + o * kOutStage;
+            const int ng = min(NG, nch - c0);
+            for (int g = 0; g < ng; ++g) {
+              const int c = c0 + g;
+              uint32_t xr[8];
+              tc_ld_x8_issue(xaddr + 16 * c, xr);
+              const uint4 gv = c < G::kGamChunks
+                                   ? tl->gam[c][warp]
+                                   : __ldg(reinterpret_cast<const uint4*>(a.gamma + (c * kCl + (int)rank) * kChunk + 8 * warp));
+              tc_wait_ld_x8(xr);
+              float xv[8], gm[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) xv[e] = __uint_as_float(xr[e]);
+              unpack8(gv, gm);
+              uint4 nv;
+              nv.x = pack_bf16x2(xv[0] * rprev * gm[0], xv[1] * rprev * gm[1]);
+              nv.y = pack_bf16x2(xv[2] * rprev * gm[2], xv[3] * rprev * gm[3]);
+              nv.z = pack_bf16x2(xv[4] * rprev * gm[4], xv[5] * rprev * gm[5]);
+              nv.w = pack_bf16x2(xv[6] * rprev * gm[6], xv[7] * rprev * gm[7]);
+              *reinterpret_cast<uint4*>(ost + g * kRTile + off) = nv;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tl->out_full[o]);
+            if (MS) {  // the warp-level projection warps count in the stage's release
+              __syncwarp();
+              if (lane == 0 && warp < 8) mbar_arrive(&tl->out_empty[o]);
+            }
+          }
+        }
+        break;
+      }
       float2 comb2[16], post2[4], pre2[4];  // each gate duplicated for the fp32x2 FMAs
       {
         float4 gc[4], gp = make_float4(0.f, 0.f, 0.f, 0.f), gq = make_float4(0.f, 0.f, 0.f, 0.f);
