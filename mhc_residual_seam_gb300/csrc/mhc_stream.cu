@@ -6,15 +6,15 @@
 // for all four streams (the cluster reads each row in long runs) and the
 // cluster walks blocks of 32 tokens.  Per 64-column chunk:
 //  - an input producer warp TMA-loads the four R tiles and the Y tile into a
-//    ring of input stages (128-byte swizzle), and each
-//    block's carried gates (comb, pre, post) into a double buffer as it
-//    starts the block, so they wait in shared memory when compute gets there;
+//    ring of 4 input stages (128-byte swizzle), and each block's carried
+//    gates (comb, pre, post) into a buffer as it starts the block, so they
+//    wait in shared memory when compute gets there;
 //  - an fn producer warp TMA-loads the four hi/lo-packed fn tiles [48 x 64]
 //    into a ring of 2 fn stages (L2 evict-last: every cluster reuses them);
 //  - eight compute warps (thread = token, warp = 8-column slice; the swizzle
 //    makes the column reads conflict-free) read their inputs, release the
 //    input stage, post-mix in fp32 (packed fp32x2 FMAs), round R' to bf16 into
-//    a ring of 2 output stages, accumulate s_R and s_x, keep x in tensor
+//    a ring of 3 output stages, accumulate s_R and s_x, keep x in tensor
 //    memory, and normalise the previous block's x of the same chunk into the
 //    same output stage;
 //  - the gate projection runs on the tensor cores, in one of two forms:
@@ -53,7 +53,7 @@ namespace {
 
 constexpr int kBM = 32;                // tokens per block
 constexpr int kChunk = 64;             // columns per chunk
-constexpr int kNF = 2, kNO = 2;
+constexpr int kNF = 2, kNO = 3;
 constexpr int kComputeThreads = 256;   // warps 0-7
 constexpr int kThreads = 416;          // + 8 input producer, 9 MMA issuer, 10 fn producer, 11 finisher, 12 store
 constexpr int kFnRows = 48;
@@ -94,7 +94,7 @@ struct alignas(128) GateTile {
 template <int KCL>
 struct Geo {
   static constexpr int kCl = KCL;
-  static constexpr int kNI = KCL == 4 ? 5 : 4;          // input stages
+  static constexpr int kNI = 4;                         // input stages
   static constexpr int kSlots = kBM / KCL;              // tokens owned per CTA and block
   static constexpr int kGamChunks = KCL == 4 ? kMaxChunksTC : (kMaxChunks * 4) / KCL;  // gamma staged in smem
   static constexpr uint32_t kXsBytes = KCL * kBM * 4;   // s_x partials landing in each CTA per block
@@ -102,9 +102,9 @@ struct Geo {
   static constexpr uint32_t kOffIn = kOffOut + kNO * kOutStage;
   static constexpr uint32_t kOffTail = kOffIn + kNI * kInStage;
   struct Tail {
-    GateTile gates[2];                     // [block parity]
+    GateTile gates;                        // one block's carried gates (the producer loads the next once compute has read them)
     uint64_t in_full[kNI], in_empty[kNI], fn_full[kNF], fn_empty[kNF], out_full[kNO], out_empty[kNO];
-    uint64_t d_full, xs_full[2], recv_full[2], recv_free[2], gates_full[2], gates_empty[2];
+    uint64_t d_full, xs_full[2], recv_full[2], recv_free[2], gates_full, gates_empty;
     uint64_t red_full[2], dbuf_full, dbuf_free, d_free;
     uint32_t tmem_base;
     volatile int err;
@@ -210,6 +210,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tl->out_empty[s], MS ? 9 : 2);
     }
     mbar_init(&tl->d_full, 1);
+    mbar_init(&tl->gates_full, 1);
+    mbar_init(&tl->gates_empty, 8);
     mbar_init(&tl->dbuf_full, 4);  // the four D readers (or folders)
     mbar_init(&tl->dbuf_free, 1);  // the exchange warp
     mbar_init(&tl->d_free, 4);     // the four D readers
@@ -217,8 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tl->xs_full[p], 1);    // + kXsBytes of st.async from the cluster
       mbar_init(&tl->recv_full[p], 1);  // + kRecvBytes of st.async from the cluster
       mbar_init(&tl->recv_free[p], kCl);
-      mbar_init(&tl->gates_full[p], 1);
-      mbar_init(&tl->gates_empty[p], 8);
+
       mbar_init(&tl->red_full[p], 8);
     }
     tl->err = 0;
@@ -262,12 +263,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int lb = 0; lb < nblk; ++lb) {
         const int t0 = (bb + lb * ncl) * kBM;
         {  // the block's carried gates, consumed at the top of its compute
-          const int gp = lb & 1;
-          wait_local(X, &tl->gates_empty[gp], ((lb >> 1) & 1) ^ 1);
-          mbar_arrive_expect_tx(&tl->gates_full[gp], (POST ? 24 : 20) * kBM * 4);
-          tma_load_2d(&tl->gates[gp].comb[0][0], &tmGc, &tl->gates_full[gp], 0, t0, pol);
-          tma_load_2d(&tl->gates[gp].pre[0][0], &tmGp, &tl->gates_full[gp], 0, t0, pol);
-          if (POST) tma_load_2d(&tl->gates[gp].post[0][0], &tmGq, &tl->gates_full[gp], 0, t0, pol);
+          wait_local(X, &tl->gates_empty, (lb & 1) ^ 1);
+          mbar_arrive_expect_tx(&tl->gates_full, (POST ? 24 : 20) * kBM * 4);
+          tma_load_2d(&tl->gates.comb[0][0], &tmGc, &tl->gates_full, 0, t0, pol);
+          tma_load_2d(&tl->gates.pre[0][0], &tmGp, &tl->gates_full, 0, t0, pol);
+          if (POST) tma_load_2d(&tl->gates.post[0][0], &tmGq, &tl->gates_full, 0, t0, pol);
         }
         for (int c = 0; c < nch; ++c, ++j) {
           const int s = j % kNI;
@@ -624,15 +624,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < 4; ++k) gc[k] = gp;
         if (real) {  // rows past T arrive as zeros
-          const int p = lb & 1;
-          wait_local(X, &tl->gates_full[p], (lb >> 1) & 1);
-          const GateTile& gt = tl->gates[p];
+          wait_local(X, &tl->gates_full, lb & 1);
+          const GateTile& gt = tl->gates;
 #pragma unroll
           for (int k = 0; k < 4; ++k) gc[k] = *reinterpret_cast<const float4*>(&gt.comb[lane][4 * k]);
           gp = *reinterpret_cast<const float4*>(&gt.pre[lane][0]);
           if (POST) gq = *reinterpret_cast<const float4*>(&gt.post[lane][0]);
           __syncwarp();
-          if (lane == 0) mbar_arrive(&tl->gates_empty[p]);
+          if (lane == 0) mbar_arrive(&tl->gates_empty);
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
