@@ -952,27 +952,11 @@ cudaError_t stream_launch(const SeamArgs& a, bool tcgen05_proj, int kcl, cudaStr
   return launch_with_maps(a, c.m, tcgen05_proj, kcl, stream, limit_ns, launches);
 }
 
-// One seam call: a single launch, or, when the clusters of 4 would end with a
-// partial round of at most as many blocks as clusters of 16 fit, the full
-// rounds over clusters of 4 and that last round as a second launch over
-// clusters of 16 (a quarter of the columns per CTA, so it takes about a
-// quarter of the time).
+// One seam call, one launch.  (Running a partial last round as a second
+// launch over larger clusters was measured slower than the partial round.)
 static cudaError_t launch_with_maps(const SeamArgs& a, const CUtensorMap* m, bool tcgen05_proj, int kcl,
                                     cudaStream_t stream, unsigned long long limit_ns, int* launches) {
   const int n_blocks = (int)((a.T + kBM - 1) / kBM);
-  if (kcl == 4) {
-    const bool post = a.Y != nullptr, mx = a.codes != nullptr;
-    const int fit4 = max_clusters(post, mx, !tcgen05_proj, 4);
-    const int fit16 = max_clusters(post, mx, false, 16);
-    if (fit4 > 0 && fit16 > 0) {
-      const int full = n_blocks / fit4 * fit4, rest = n_blocks - full;
-      if (full > 0 && rest > 0 && rest <= fit16) {
-        cudaError_t e = launch_range(a, m, tcgen05_proj, 4, 0, full, stream, limit_ns, launches);
-        if (e != cudaSuccess) return e;
-        return launch_range(a, m, true, 16, full, rest, stream, limit_ns, launches);
-      }
-    }
-  }
   return launch_range(a, m, tcgen05_proj, kcl, 0, n_blocks, stream, limit_ns, launches);
 }
 
