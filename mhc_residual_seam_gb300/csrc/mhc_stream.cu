@@ -401,10 +401,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
         }
         if (lane == 0) {
-          if (real) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) tma_store_3d(&tmRo, ost + i * kRTile, h, i, t0);
-          }
+          for (int i = 0; i < 4; ++i) tma_store_3d(&tmRo, ost + i * kRTile, h, i, t0);
           if (prev) {
             tma_store_2d(&tmN, ost + kOffNormT, h, tp);
             if (MXFP8) tma_store_2d(&tmC, ost + kOffCodesT, h, tp);
@@ -623,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float4 gc[4], gp = make_float4(0.f, 0.f, 0.f, 0.f), gq = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < 4; ++k) gc[k] = gp;
-        if (real) {  // rows past T arrive as zeros
+        {  // rows past T arrive as zeros
           wait_local(X, &tl->gates_full, lb & 1);
           const GateTile& gt = tl->gates;
 #pragma unroll
@@ -664,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           gv = c < G::kGamChunks ? tl->gam[c][warp]
                                 : __ldg(reinterpret_cast<const uint4*>(a.gamma + (c * kCl + (int)rank) * kChunk + 8 * warp));
         }
-        if (real) {
+        {
           const int s = ji % kNI;
           wait_local(X, &tl->in_full[s], (ji / kNI) & 1);
           const uint8_t* st = sm + kOffIn + s * kInStage;
@@ -703,11 +701,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (prev && c == 0) take_rstd(lb - 1);
         wait_local(X, &tl->out_empty[o], ((j / kNO) & 1) ^ 1);
         uint8_t* ost = sm + kOffOut + o * kOutStage;
-        if (real) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            *reinterpret_cast<uint4*>(ost + i * kRTile + off) = make_uint4(ow[i][0], ow[i][1], ow[i][2], ow[i][3]);
-        }
+        for (int i = 0; i < 4; ++i)
+          *reinterpret_cast<uint4*>(ost + i * kRTile + off) = make_uint4(ow[i][0], ow[i][1], ow[i][2], ow[i][3]);
         if (prev) {  // norm of the previous block's x in these columns, before x is overwritten
           float xv[8], gm[8];
           tc_wait_ld_x8(xr);
@@ -721,24 +717,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           nv.w = pack_bf16x2(xv[6] * rprev * gm[6], xv[7] * rprev * gm[7]);
           *reinterpret_cast<uint4*>(ost + kOffNormT + off) = nv;
         }
-        if (real) tc_st_x8(xaddr + 16 * c, x);
+        tc_st_x8(xaddr + 16 * c, x);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tl->out_full[o]);
-        if (!MS && prev && real && c == 0 && warp < 4) read_d(lb - 1);
-        if (MS) {
-          if (real && c > 0) mma_chunk(j - 1, ji - 2);
-          if (!real) {  // no projection in the normalise-only pass: release the stage
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tl->out_empty[o]);
-          }
-        }
+        if (!MS && prev && c == 0 && warp < 4) read_d(lb - 1);
+        if (MS && c > 0) mma_chunk(j - 1, ji - 2);
       }
       if (prev && nch == 0) {  // no columns here: only consume the phases
         take_rstd(lb - 1);
-        if (!MS && real && warp < 4) read_d(lb - 1);
+        if (!MS && warp < 4) read_d(lb - 1);
       }
-      if (!real) break;
       if (MS && nch > 0) mma_chunk(j - 1, ji - 1);
       tc_wait_st();
 
