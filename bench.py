@@ -49,6 +49,9 @@ WORKLOADS = {
     "seam_T64_H5120_post_bf16": dict(T=64, H=5120, post=True, out="bf16", seed=1001),
     "seam_T64_H5120_nopost_bf16": dict(T=64, H=5120, post=False, out="bf16", seed=1001),
     "seam_T4_H5120_post_bf16": dict(T=4, H=5120, post=True, out="bf16", seed=1000),
+    # the T sweep of the pages' single-launch table (config 4 inputs)
+    **{f"seam_T{t}_H5120_post_bf16": dict(T=t, H=5120, post=True, out="bf16", seed=1004)
+       for t in (1, 32, 384, 2048, 8192)},
 }
 DEFAULT = "seam_T16384_H5120_post_bf16"
 UNIQUE_TOKENS = 2048  # distinct tokens drawn; repeated along T (the device streams all T)
