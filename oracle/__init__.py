@@ -55,6 +55,10 @@ def bind(cdll):
     L.mhc_oracle_ue8m0_exponent.argtypes = [C.c_double, C.c_double]
     L.mhc_oracle_quant_ue8m0.restype = C.c_int
     L.mhc_oracle_quant_ue8m0.argtypes = [P, C.c_int64, C.c_int, C.c_double, P, P]
+    L.mhc_oracle_e4m3_decode.restype = C.c_double
+    L.mhc_oracle_e4m3_decode.argtypes = [C.c_uint8]
+    L.mhc_oracle_grid_ue8m0.restype = C.c_int
+    L.mhc_oracle_grid_ue8m0.argtypes = [P, C.c_int64, C.c_int, C.c_double, P]
     L.mhc_oracle_sinkhorn.restype = None
     L.mhc_oracle_sinkhorn.argtypes = [C.c_int, P, C.c_int]
     L.mhc_oracle_sigmoid.restype = C.c_double
@@ -137,6 +141,23 @@ def quant_ue8m0(x, amax_floor: float = 1e-10):
     if rc != 0:
         raise ValueError("H must be a multiple of 32")
     return codes, scales
+
+
+def e4m3_decode(code: int) -> float:
+    """Value of one e4m3fn code (NaN for 0x7F / 0xFF)."""
+    return float(lib().mhc_oracle_e4m3_decode(int(code)))
+
+
+def grid_ue8m0(x, amax_floor: float = 1e-10) -> np.ndarray:
+    """fp8_grid output of bf16 rows: per 32-group, bf16(decode(code) * 2^e) as
+    uint16 bits [rows, H]."""
+    xb = _u16(x)
+    rows, H = xb.shape
+    grid = np.zeros((rows, H), np.uint16)
+    rc = lib().mhc_oracle_grid_ue8m0(_ptr(xb), rows, H, float(amax_floor), _ptr(grid))
+    if rc != 0:
+        raise ValueError("H must be a multiple of 32")
+    return grid
 
 
 def seam(R, Y, post_prev, comb_prev, pre_prev, fn, bias, alpha, gamma, eps: float,

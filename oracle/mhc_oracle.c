@@ -153,6 +153,40 @@ int mhc_oracle_quant_ue8m0(const uint16_t* x, int64_t rows, int H, double amax_f
     return 0;
 }
 
+/* Value of an e4m3fn code under the definition above: S.0000.fff is
+ * f * 2^-9, S.EEEE.fff (E = 1..15) is (1 + f/8) * 2^(E-7), S.1111.111 is NaN. */
+double mhc_oracle_e4m3_decode(uint8_t c) {
+    int E = (c >> 3) & 0xF, f = c & 7;
+    if (E == 0xF && f == 7) return NAN;
+    double v = E == 0 ? ldexp((double)f, -9) : ldexp(1.0 + f / 8.0, E - 7);
+    return (c & 0x80) ? -v : v;
+}
+
+/* fp8_grid output: per 32-element group, the values a consumer of the ue8m0
+ * quantisation reconstructs, decode(code) * 2^e, rounded to bf16 (RNE; the
+ * product has at most 4 significant bits, so it is exact unless it leaves
+ * the bf16 range).  Returns 0, or -1 when H is not a multiple of 32. */
+int mhc_oracle_grid_ue8m0(const uint16_t* x, int64_t rows, int H, double amax_floor, uint16_t* grid) {
+    if (H % 32 != 0) return -1;
+    int G = H / 32;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int g = 0; g < G; ++g) {
+            const uint16_t* src = x + r * H + g * 32;
+            double amax = 0.0;
+            for (int j = 0; j < 32; ++j) {
+                double a = fabs(mhc_oracle_bf16_to_double(src[j]));
+                if (a > amax) amax = a;
+            }
+            int e = mhc_oracle_ue8m0_exponent(amax, amax_floor);
+            for (int j = 0; j < 32; ++j) {
+                uint8_t code = mhc_oracle_e4m3_rne_satfinite(ldexp(mhc_oracle_bf16_to_double(src[j]), -e));
+                grid[r * H + g * 32 + j] = mhc_oracle_bf16_rne(ldexp(mhc_oracle_e4m3_decode(code), e));
+            }
+        }
+    }
+    return 0;
+}
+
 /* ----------------------------------------------------------- Sinkhorn ---- */
 
 /* n x n Sinkhorn normalisation of a positive matrix (row-major, in place):

@@ -29,9 +29,15 @@ MUTATIONS = {
     "e4m3_one_bit_short": ("spacing = ldexp(1.0, (e - 1) - 3);", "spacing = ldexp(1.0, (e - 1) - 2);"),
     "e8m0_bias_off_by_one": ("scales[r * G + g] = (uint8_t)(e + 127);", "scales[r * G + g] = (uint8_t)(e + 128);"),
     "x_uses_equal_weights": ("v += (double)pre[i] * rp[i * H + h];", "v += 0.25 * rp[i * H + h];"),
+    "grid_scale_off_by_one": ("mhc_oracle_bf16_rne(ldexp(mhc_oracle_e4m3_decode(code), e))",
+                              "mhc_oracle_bf16_rne(ldexp(mhc_oracle_e4m3_decode(code), e + 1))"),
+    "e4m3_decode_bias_8": ("ldexp(1.0 + f / 8.0, E - 7)", "ldexp(1.0 + f / 8.0, E - 8)"),
 }
 
 PINS = [
+    P.test_e4m3_decode_matches_format_definition,
+    P.test_grid_exact_on_the_e4m3_lattice,
+    P.test_grid_is_the_dequantised_mxfp8_output,
     P.test_bf16_rne_matches_torch_cast_on_float32_inputs,
     P.test_e4m3_golden_codes_from_ocp_spec,
     P.test_ue8m0_exponent_exhaustive_over_bf16_amax,

@@ -482,3 +482,47 @@ def test_oracle_rejects_half_present_post(oracle):
     d = seam_inputs(1, 8, 40, oracle=oracle)
     with pytest.raises(ValueError):
         run(oracle, dict(d, post_prev=None))
+
+
+# ------------------------------------------------------------ fp8_grid ----
+def test_e4m3_decode_matches_format_definition(oracle):
+    # every finite code decodes to its value in the OCP definition (the golden
+    # file's listed code points and the table built from the bit fields)
+    rows = [l.split() for l in open(os.path.join(GOLDEN, "e4m3fn_ocp.txt")) if l.strip() and not l.startswith("#")]
+    for v, code in rows:
+        assert oracle.e4m3_decode(int(code, 16)) == float(v), (v, code)
+    for code, v in e4m3_table().items():
+        assert oracle.e4m3_decode(code) == v, code
+        assert oracle.e4m3(v) == code or (v == 0.0 and code in (0x00, 0x80)), code
+    assert math.isnan(oracle.e4m3_decode(0x7F)) and math.isnan(oracle.e4m3_decode(0xFF))
+
+
+def test_grid_exact_on_the_e4m3_lattice(oracle):
+    # a group whose amax is 448 * 2^k and whose values are e4m3 values times
+    # 2^k reconstructs exactly (the grid is the identity on its own lattice)
+    table = e4m3_table()
+    codes = sorted(c for c in table if c not in (0x7F, 0xFF))
+    rng = np.random.default_rng(7)
+    for k in (-30, -5, 0, 3, 20):
+        vals = np.array([table[c] for c in rng.choice(codes, 32)]) * 2.0 ** k
+        vals[0] = 448.0 * 2.0 ** k
+        x = I.to_bf16(vals).reshape(1, 32)
+        grid = oracle.grid_ue8m0(x)
+        assert np.array_equal(grid, I.bf16_bits(x)), k
+
+
+def test_grid_is_the_dequantised_mxfp8_output(oracle):
+    # grid = decode(code) * 2^(scale - 127) from the quantiser's own outputs,
+    # decoded by the table above, within the e4m3 rounding bound of the input
+    x, _ = I.crafted_quant_tensor(8, 256, seed=1005, frac=0.2)
+    grid = oracle.grid_ue8m0(x)
+    codes, scales = oracle.quant_ue8m0(x)
+    table = e4m3_table()
+    xv = x.to(torch.float64).numpy()
+    for r in range(8):
+        for h in range(256):
+            e = int(scales[r, h // 32]) - 127
+            want = I.bf16_bits(I.to_bf16(np.array([table[int(codes[r, h])] * 2.0 ** e])))[0]
+            assert grid[r, h] == want, (r, h)
+            g = bf16_val(grid[r, h])
+            assert abs(g - xv[r, h]) <= max(abs(xv[r, h]) * 2.0 ** -4, 2.0 ** (e - 10)), (r, h)
