@@ -46,6 +46,7 @@ WORKLOADS = {
     "seam_T16384_H5120_nopost_bf16": dict(T=16384, H=5120, post=False, out="bf16", seed=1004),
     "seam_T4160_H5120_post_bf16": dict(T=4160, H=5120, post=True, out="bf16", seed=1003),
     "seam_T1024_H5120_post_mxfp8": dict(T=1024, H=5120, post=True, out="mxfp8", seed=1002),
+    "seam_T16384_H5120_post_fp8grid": dict(T=16384, H=5120, post=True, out="fp8_grid", seed=1004),
     "seam_T64_H5120_post_bf16": dict(T=64, H=5120, post=True, out="bf16", seed=1001),
     "seam_T64_H5120_nopost_bf16": dict(T=64, H=5120, post=False, out="bf16", seed=1001),
     "seam_T4_H5120_post_bf16": dict(T=4, H=5120, post=True, out="bf16", seed=1000),
@@ -158,7 +159,7 @@ def run_ours(args, w: dict, rank: int, world: int, local_rank: int) -> dict | No
     g, host = wl["dev"], wl["host"]
     T, H = w["T"], w["H"]
     mx = w["out"] == "mxfp8"
-    mode = B.MHC_OUT_MXFP8 if mx else B.MHC_OUT_BF16
+    mode = {"bf16": B.MHC_OUT_BF16, "mxfp8": B.MHC_OUT_MXFP8, "fp8_grid": B.MHC_OUT_FP8_GRID}[w["out"]]
     stream = torch.cuda.current_stream(device)
     g["fn_packed"] = torch.empty(B.mhc_packed_fn_bytes(H) // 2, dtype=torch.bfloat16, device=device)
     B.mhc_pack_fn(g["fn"], g["fn_packed"], stream=stream)  # once per weight update, outside the timed region
@@ -220,7 +221,8 @@ def run_ours(args, w: dict, rank: int, world: int, local_rank: int) -> dict | No
     if not args.no_e2e:
         pin = {k: (None if v is None else v.pin_memory()) for k, v in host.items()
                if k in ("R", "Y", "post_prev", "comb_prev", "pre_prev")}
-        outs = ["residual_out", "norm", "pre_out", "post_out", "comb_out"] + (["fp8_codes", "e8m0_scales"] if mx else [])
+        outs = ["residual_out", "norm", "pre_out", "post_out", "comb_out"] + (
+            ["fp8_codes", "e8m0_scales"] if mx else (["fp8_codes"] if mode == B.MHC_OUT_FP8_GRID else []))
         pout = {k: torch.empty(out[k].shape, dtype=out[k].dtype).pin_memory() for k in outs}
         bi = sum(v.numel() * v.element_size() for v in pin.values() if v is not None)
         bo = sum(v.numel() * v.element_size() for v in pout.values())
@@ -295,6 +297,8 @@ def cpu_baseline(w: dict, wl: dict | None, budget_s: float = 15.0, steps: int = 
                    pre[:n], d["fn"], d["bias"], d["alpha"], d["gamma"], d["eps"])
         if w["out"] == "mxfp8":
             O.quant_ue8m0(o["norm"])
+        elif w["out"] == "fp8_grid":
+            O.grid_ue8m0(o["norm"])
         times.append(time.perf_counter() - t0)
     sec = statistics.median(times)
     b = ACC.seam_bytes(n, w["H"], post=w["post"], out=w["out"])

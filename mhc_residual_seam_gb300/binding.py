@@ -16,6 +16,7 @@ from . import build as _build
 
 MHC_OUT_BF16 = 0
 MHC_OUT_MXFP8 = 1
+MHC_OUT_FP8_GRID = 2
 STATUS_NAMES = {
     0: "MHC_OK", -1: "MHC_ERR_NULL", -2: "MHC_ERR_SHAPE", -3: "MHC_ERR_ALIGN", -4: "MHC_ERR_INCOMPLETE_POST",
     -5: "MHC_ERR_WORKSPACE", -6: "MHC_ERR_CAPTURE", -7: "MHC_ERR_TIMEOUT", -8: "MHC_ERR_CUDA", -9: "MHC_ERR_ALIAS",
@@ -188,7 +189,10 @@ def alloc_outputs(T: int, H: int, out_mode: int, device, cfg=None) -> dict:
     o = {
         "residual_out": torch.empty((T, 4, H), dtype=torch.bfloat16, device=device),
         "norm": torch.empty((T, H), dtype=torch.bfloat16, device=device),
-        "fp8_codes": torch.empty((T, H), dtype=torch.uint8, device=device) if out_mode == MHC_OUT_MXFP8 else None,
+        # mxfp8: e4m3 codes; fp8_grid: the bf16 grid (written through the same argument)
+        "fp8_codes": (torch.empty((T, H), dtype=torch.uint8, device=device) if out_mode == MHC_OUT_MXFP8 else
+                      torch.empty((T, H), dtype=torch.bfloat16, device=device) if out_mode == MHC_OUT_FP8_GRID
+                      else None),
         "e8m0_scales": torch.empty((T, H // 32), dtype=torch.uint8, device=device) if out_mode == MHC_OUT_MXFP8 else None,
         "pre_out": torch.empty((T, 4), dtype=torch.float32, device=device),
         "post_out": torch.empty((T, 4), dtype=torch.float32, device=device),

@@ -218,10 +218,11 @@ int mhc_seam(const void* R, const void* Y, const float* post_prev, const float* 
              size_t ws_bytes, const mhc_config* cfg, void* stream) {
   g_launches = 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (out_mode != MHC_OUT_BF16 && out_mode != MHC_OUT_MXFP8) return fail(MHC_ERR_CONFIG, "unknown out_mode");
-  const bool mx = out_mode == MHC_OUT_MXFP8;
+  if (out_mode != MHC_OUT_BF16 && out_mode != MHC_OUT_MXFP8 && out_mode != MHC_OUT_FP8_GRID)
+    return fail(MHC_ERR_CONFIG, "unknown out_mode");
+  const bool mx = out_mode == MHC_OUT_MXFP8, gridm = out_mode == MHC_OUT_FP8_GRID;
   if (T < 0 || H <= 0 || H % 8 != 0) return fail(MHC_ERR_SHAPE, "need T >= 0 and H a positive multiple of 8");
-  if (mx && H % 32 != 0) return fail(MHC_ERR_SHAPE, "mxfp8 output needs H % 32 == 0");
+  if ((mx || gridm) && H % 32 != 0) return fail(MHC_ERR_SHAPE, "mxfp8 and fp8_grid outputs need H % 32 == 0");
   if (!(eps >= 0.f) || eps > 1e30f) return fail(MHC_ERR_CONFIG, "eps must be finite and >= 0");
   Plan plan;
   int rc = make_plan(T, H, cfg, fn_packed != nullptr, &plan);
@@ -233,9 +234,12 @@ int mhc_seam(const void* R, const void* Y, const float* post_prev, const float* 
       !post_out || !comb_out)
     return fail(MHC_ERR_NULL, "a required pointer is NULL");
   if (mx && (!fp8_codes || !e8m0_scales)) return fail(MHC_ERR_NULL, "mxfp8 output needs fp8_codes and e8m0_scales");
+  if (gridm && !fp8_codes) return fail(MHC_ERR_NULL, "fp8_grid output needs fp8_codes (the bf16 grid)");
+  if (gridm && plan.path == 1)
+    return fail(MHC_ERR_CONFIG, "fp8_grid runs on the streaming path (cfg.path 2 or 3, fn_packed, 512 <= H <= 8192)");
   if (!workspace) return fail(MHC_ERR_WORKSPACE, "workspace is NULL");
   const void* a16[] = {R, Y, post_prev, comb_prev, pre_prev, fn, fn_packed, gamma, residual_out, norm,
-                       mx ? fp8_codes : nullptr, pre_out, post_out, comb_out, workspace};
+                       (mx || gridm) ? fp8_codes : nullptr, pre_out, post_out, comb_out, workspace};
   for (const void* p : a16)
     if (p && !aligned16(p)) return fail(MHC_ERR_ALIGN, "a pointer that must be 16-byte aligned is not");
   if (reinterpret_cast<uintptr_t>(bias) % 4 || reinterpret_cast<uintptr_t>(alpha) % 4)
@@ -249,7 +253,7 @@ int mhc_seam(const void* R, const void* Y, const float* post_prev, const float* 
                 rng(comb_prev, (size_t)T * 64), rng(pre_prev, (size_t)T * 16), rng(fn, (size_t)H * 4 * 24 * 4),
                 rng(fn_packed, fn_packed ? mhc_packed_fn_bytes(H) : 0), rng(bias, 96), rng(alpha, 12),
                 rng(gamma, (size_t)H * 2)};
-  Range out[] = {rng(residual_out, TH * 8), rng(norm, TH * 2), rng(fp8_codes, mx ? TH : 0),
+  Range out[] = {rng(residual_out, TH * 8), rng(norm, TH * 2), rng(fp8_codes, mx ? TH : (gridm ? TH * 2 : 0)),
                  rng(e8m0_scales, mx ? TH / 32 : 0), rng(pre_out, (size_t)T * 16), rng(post_out, (size_t)T * 16),
                  rng(comb_out, (size_t)T * 64), rng(workspace, need)};
   const int n_in = sizeof in / sizeof in[0], n_out = sizeof out / sizeof out[0];
@@ -284,6 +288,7 @@ int mhc_seam(const void* R, const void* Y, const float* post_prev, const float* 
   a.norm = static_cast<__nv_bfloat16*>(norm);
   a.codes = mx ? fp8_codes : nullptr;
   a.scales = mx ? e8m0_scales : nullptr;
+  a.grid = gridm ? reinterpret_cast<__nv_bfloat16*>(fp8_codes) : nullptr;
   a.pre_out = pre_out;
   a.post_out = post_out;
   a.comb_out = comb_out;

@@ -8,6 +8,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -37,6 +38,7 @@ struct SeamArgs {
   __nv_bfloat16* norm;             // [T,H]
   uint8_t* codes;                  // [T,H]   (mxfp8)
   uint8_t* scales;                 // [T,H/32] (mxfp8)
+  __nv_bfloat16* grid;             // [T,H]   (fp8_grid: the quantisation dequantised to bf16)
   float* pre_out;                  // [T,4]
   float* post_out;                 // [T,4]
   float* comb_out;                 // [T,4,4]
@@ -118,6 +120,30 @@ __device__ __forceinline__ uint8_t quant_group32(const uint32_t* nb, uint32_t* c
     codes[q] = (uint32_t)lo | ((uint32_t)hi << 16);
   }
   return (uint8_t)(e + 127);
+}
+
+// 2^e as an fp32 (e in [-127, 127] -> normal or the one subnormal 2^-127).
+__device__ __forceinline__ float exp2_pos(int e) {
+  return e > -127 ? __uint_as_float((uint32_t)(127 + e) << 23) : __uint_as_float(0x00400000u);
+}
+
+// fp8_grid of one 32-group: the ue8m0 exponent and e4m3 codes as in
+// quant_group32, then each code's value times 2^e rounded to bf16 (the e4m3
+// value is exact in fp16 and the product by a power of two is exact in fp32
+// unless it leaves the range).  Writes 32 bf16 values as 16 words.
+__device__ __forceinline__ void grid_group32(const uint32_t* nb, uint32_t* gw, float floor_) {
+  float amax = 0.f;
+#pragma unroll
+  for (int q = 0; q < 16; ++q) amax = fmaxf(amax, fmaxf(fabsf(bf16lo(nb[q])), fabsf(bf16hi(nb[q]))));
+  const int e = ue8m0_exponent(amax, floor_);
+  const float s = exp2_neg(e), up = exp2_pos(e);
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    const uint16_t c2 = e4m3x2(__fmul_rn(bf16lo(nb[q]), s), __fmul_rn(bf16hi(nb[q]), s));
+    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)c2, __NV_E4M3);
+    const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+    gw[q] = pack_bf16x2(__fmul_rn(v.x, up), __fmul_rn(v.y, up));
+  }
 }
 
 // ---------------------------------------------------------------- finish --

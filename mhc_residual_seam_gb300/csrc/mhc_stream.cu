@@ -65,10 +65,11 @@ constexpr uint32_t kOffNormT = 4 * kRTile;             // output stage: R' tiles
 constexpr uint32_t kOffCodesT = 5 * kRTile;            //   then the codes tile [32 x 64] u8
 constexpr uint32_t kOutStage = 5 * kRTile + kBM * 64;  // 22 KB (a multiple of 1 KB: swizzled tiles)
 // The normalise-only pass after a cluster's last block puts the norm tiles of
-// kNormGroup chunks in one output stage (in the R' tile slots; with mxfp8 the
-// codes tiles go where the norm tile sits in the other passes).
-template <bool MXFP8>
-__host__ __device__ constexpr int norm_group() { return MXFP8 ? 2 : 4; }
+// norm_group() chunks in one output stage (in the R' tile slots; with mxfp8
+// the codes tiles go where the norm tile sits in the other passes, with
+// fp8_grid the grid tiles take R' slots 2 and 3).
+template <bool QUANT>
+__host__ __device__ constexpr int norm_group() { return QUANT ? 2 : 4; }
 constexpr uint32_t kOffFn = 0;
 constexpr uint32_t kOffOut = kOffFn + kNF * kFnStage;
 constexpr uint32_t kTmemCols = 512;
@@ -166,7 +167,9 @@ __device__ __noinline__ void finish_store_gates(const SeamArgs& a, int64_t t, co
   store_gates(a, t, pre, post, cb);
 }
 
-template <bool POST, bool MXFP8, bool MS, int KCL>
+// OUT: 0 bf16 norm, 1 mxfp8 (+ e4m3 codes, e8m0 scales), 2 fp8_grid (+ the
+// quantisation dequantised to bf16)
+template <bool POST, int OUT, bool MS, int KCL>
 __global__ void __launch_bounds__(kThreads, 1)
     stream_seam_kernel(const SeamArgs a, const __grid_constant__ CUtensorMap tmR,
                        const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmRo,
@@ -177,6 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   using G = Geo<KCL>;
+  constexpr bool QUANT = OUT != 0;
   constexpr int kCl = G::kCl, kNI = G::kNI, kSlots = G::kSlots;
   constexpr uint32_t kOffIn = G::kOffIn, kXsBytes = G::kXsBytes, kRecvBytes = G::kRecvBytes;
   typename G::Tail* tl = reinterpret_cast<typename G::Tail*>(sm + G::kOffTail);
@@ -236,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 12 && lane == 0) {
     prefetch_tmap(&tmRo);
     prefetch_tmap(&tmN);
-    if (MXFP8) prefetch_tmap(&tmC);
+    if (OUT == 1) prefetch_tmap(&tmC);
   }
   // gamma of this CTA's first chunks, staged once (read by every block)
   for (int i = tid; i < min(nch, G::kGamChunks) * 8; i += kThreads)
@@ -311,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int j = 0, jr = 0;
       for (int lb = 0; lb <= nblk; ++lb) {
         if (lb == nblk) {  // the normalise-only pass: one stage per group of chunks, no MMA
-          for (int c0 = 0; c0 < nch; c0 += norm_group<MXFP8>(), ++j) {
+          for (int c0 = 0; c0 < nch; c0 += norm_group<QUANT>(), ++j) {
             wait_local(X, &tl->out_full[j % kNO], (j / kNO) & 1);
             mbar_arrive(&tl->out_empty[j % kNO]);
           }
@@ -340,6 +344,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 12) {
     // ---------------------------- stores: R' tiles, norm tile, ue8m0 codes --
     int j = 0;
+    // lane = token: the fp8_grid values of one norm tile row into registers,
+    // and their store as a swizzled bf16 tile like the norm tile
+    auto grid_regs = [&](const uint8_t* nt, uint32_t* gw) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t nb[16];
+#pragma unroll
+        for (int jq = 0; jq < 4; ++jq) {
+          const int ch = 4 * half + jq;
+          uint4 v = *reinterpret_cast<const uint4*>(nt + lane * 128 + ((ch ^ (lane & 7)) << 4));
+          nb[4 * jq] = v.x; nb[4 * jq + 1] = v.y; nb[4 * jq + 2] = v.z; nb[4 * jq + 3] = v.w;
+        }
+        grid_group32(nb, gw + 16 * half, a.amax_floor);
+      }
+    };
+    // the grid row of token tp + lane, columns h .. h + 63, straight from
+    // registers: each lane writes its own 128 contiguous bytes
+    auto store_grid = [&](int64_t tp, int h, const uint32_t* gw) {
+      const int64_t tt = tp + lane;
+      if (tt < T) {
+        uint4* dst = reinterpret_cast<uint4*>(a.grid + tt * H + h);
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) st_stream(dst + ch, make_uint4(gw[4 * ch], gw[4 * ch + 1], gw[4 * ch + 2], gw[4 * ch + 3]));
+      }
+    };
     // lane = token: the ue8m0 codes of one norm tile (two 32-column groups)
     auto quant_tile = [&](const uint8_t* nt, uint8_t* ct, int64_t tp, int h) {
 #pragma unroll
@@ -364,23 +393,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool real = lb < nblk, prev = lb > 0;
       const int t0 = (bb + lb * ncl) * kBM, tp = (bb + (lb - 1) * ncl) * kBM;
       if (!real) {  // the normalise-only pass: the norm tiles of a group of chunks per stage
-        constexpr int G = norm_group<MXFP8>();
+        constexpr int G = norm_group<QUANT>();
         for (int c0 = 0; c0 < nch && prev; c0 += G, ++j) {
           const int o = j % kNO;
           uint8_t* ost = sm + kOffOut + o * kOutStage;
           wait_local(X, &tl->out_full[o], (j / kNO) & 1);
           const int ng = min(G, nch - c0);
-          if (MXFP8) {
+          if (OUT == 1) {  // codes tiles in stage slot 4
             for (int g = 0; g < ng; ++g)
               quant_tile(ost + g * kRTile, ost + kOffNormT + g * 2048, tp, ((c0 + g) * kCl + (int)rank) * kChunk);
             fence_proxy_async_smem();
             __syncwarp();
           }
+          if (OUT == 2) {
+            for (int g = 0; g < ng; ++g) {
+              uint32_t gw[32];
+              grid_regs(ost + g * kRTile, gw);
+              store_grid(tp, ((c0 + g) * kCl + (int)rank) * kChunk, gw);
+            }
+          }
           if (lane == 0) {
             for (int g = 0; g < ng; ++g) {
               const int h = ((c0 + g) * kCl + (int)rank) * kChunk;
               tma_store_2d(&tmN, ost + g * kRTile, h, tp);
-              if (MXFP8) tma_store_2d(&tmC, ost + kOffNormT + g * 2048, h, tp);
+              if (OUT == 1) tma_store_2d(&tmC, ost + kOffNormT + g * 2048, h, tp);
             }
             tma_store_commit();
             tma_store_wait_read_all();
@@ -395,23 +431,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* ost = sm + kOffOut + o * kOutStage;
         const int h = (c * kCl + (int)rank) * kChunk;
         wait_local(X, &tl->out_full[o], (j / kNO) & 1);
-        if (MXFP8 && prev) {
+        uint32_t gw[OUT == 2 ? 32 : 1];
+        if (OUT == 1 && prev) {
           quant_tile(ost + kOffNormT, ost + kOffCodesT, tp, h);
           fence_proxy_async_smem();
           __syncwarp();
         }
+        if (OUT == 2 && prev) grid_regs(ost + kOffNormT, gw);
         if (lane == 0) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) tma_store_3d(&tmRo, ost + i * kRTile, h, i, t0);
           if (prev) {
             tma_store_2d(&tmN, ost + kOffNormT, h, tp);
-            if (MXFP8) tma_store_2d(&tmC, ost + kOffCodesT, h, tp);
+            if (OUT == 1) tma_store_2d(&tmC, ost + kOffCodesT, h, tp);
           }
           tma_store_commit();
           tma_store_wait_read_all();
-          mbar_arrive(&tl->out_empty[o]);
         }
+        if (lane == 0) mbar_arrive(&tl->out_empty[o]);
         __syncwarp();
+        if (OUT == 2 && prev) store_grid(tp, h, gw);
       }
     }
     if (lane == 0) tma_store_wait_all();
@@ -580,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!real) {  // the normalise-only pass: the norm tiles of a group of chunks per output stage
         if (prev) {
           take_rstd(lb - 1);
-          constexpr int NG = norm_group<MXFP8>();
+          constexpr int NG = norm_group<QUANT>();
           for (int c0 = 0; c0 < nch; c0 += NG, ++j) {
             const int o = j % kNO;
             wait_local(X, &tl->out_empty[o], ((j / kNO) & 1) ^ 1);
@@ -785,20 +824,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------- host side --
 template <bool MS, int KCL>
-static void* kptr_(bool post, bool mxfp8) {
-  if (post) return mxfp8 ? (void*)stream_seam_kernel<true, true, MS, KCL> : (void*)stream_seam_kernel<true, false, MS, KCL>;
-  return mxfp8 ? (void*)stream_seam_kernel<false, true, MS, KCL> : (void*)stream_seam_kernel<false, false, MS, KCL>;
+static void* kptr_(bool post, int out) {
+  if (post)
+    return out == 2 ? (void*)stream_seam_kernel<true, 2, MS, KCL>
+                    : out == 1 ? (void*)stream_seam_kernel<true, 1, MS, KCL> : (void*)stream_seam_kernel<true, 0, MS, KCL>;
+  return out == 2 ? (void*)stream_seam_kernel<false, 2, MS, KCL>
+                  : out == 1 ? (void*)stream_seam_kernel<false, 1, MS, KCL> : (void*)stream_seam_kernel<false, 0, MS, KCL>;
 }
 // Clusters of 16 run only the tcgen05 projection (at most 8 chunks per CTA).
-static void* stream_kernel_ptr(bool post, bool mxfp8, bool ms, int kcl) {
-  if (kcl == 16) return kptr_<false, 16>(post, mxfp8);
-  return ms ? kptr_<true, 4>(post, mxfp8) : kptr_<false, 4>(post, mxfp8);
+static void* stream_kernel_ptr(bool post, int out, bool ms, int kcl) {
+  if (kcl == 16) return kptr_<false, 16>(post, out);
+  return ms ? kptr_<true, 4>(post, out) : kptr_<false, 4>(post, out);
 }
 static size_t smem_bytes(int kcl) { return kcl == 16 ? Geo<16>::kSmemBytes : Geo<4>::kSmemBytes; }
 
 cudaError_t stream_init() {
   for (int p = 0; p < 2; ++p)
-    for (int m = 0; m < 2; ++m)
+    for (int m = 0; m < 3; ++m)      // out mode
       for (int v = 0; v < 3; ++v) {  // v: 0 tcgen05 / 4, 1 warp MMA / 4, 2 tcgen05 / 16
         const int kcl = v == 2 ? 16 : 4;
         void* k = stream_kernel_ptr(p, m, v == 1, kcl);
@@ -851,11 +893,11 @@ static bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void*
 }
 
 // Clusters that fit at once, per device and kernel variant (queried once).
-static int max_clusters(bool post, bool mxfp8, bool ms, int kcl) {
-  static int cache[12][64] = {};
+static int max_clusters(bool post, int out, bool ms, int kcl) {
+  static int cache[18][64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  const int v = (post ? 1 : 0) + (mxfp8 ? 2 : 0) + 4 * (kcl == 16 ? 2 : (ms ? 1 : 0));
+  const int v = (post ? 1 : 0) + 2 * out + 6 * (kcl == 16 ? 2 : (ms ? 1 : 0));
   if (cache[v][dev] > 0) return cache[v][dev];
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -869,7 +911,7 @@ static int max_clusters(bool post, bool mxfp8, bool ms, int kcl) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, stream_kernel_ptr(post, mxfp8, ms, kcl), &cfg) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveClusters(&n, stream_kernel_ptr(post, out, ms, kcl), &cfg) != cudaSuccess) return 0;
   cache[v][dev] = n;
   return n;
 }
@@ -898,7 +940,8 @@ cudaError_t stream_launch(const SeamArgs& a, bool tcgen05_proj, int kcl, cudaStr
   };
   thread_local MapSet cache[4];
   thread_local int cache_next = 0;
-  const void* key[9] = {a.R, a.Y, a.res_out, a.fn_packed, a.norm, a.codes, a.comb_prev, a.pre_prev, a.post_prev};
+  const void* key[9] = {a.R, a.Y, a.res_out, a.fn_packed, a.norm, a.grid ? (const void*)a.grid : (const void*)a.codes,
+                        a.comb_prev, a.pre_prev, a.post_prev};
   for (const MapSet& c : cache) {
     bool hit = c.T == a.T && c.H == H;
     for (int i = 0; hit && i < 9; ++i) hit = c.key[i] == key[i];
@@ -920,8 +963,13 @@ cudaError_t stream_launch(const SeamArgs& a, bool tcgen05_proj, int kcl, cudaStr
             encode(&mN, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.norm, d2, s2, b2, CU_TENSOR_MAP_SWIZZLE_128B);
   if (ok) ok = encode(&mY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.Y ? (const void*)a.Y : (const void*)a.R, d2, s2, b2,
                       CU_TENSOR_MAP_SWIZZLE_128B);
-  if (ok) ok = encode(&mC, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.codes ? (const void*)a.codes : (const void*)a.norm, d2,
-                      sC, b2, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (ok) {  // the quantised output: e4m3 codes (u8), or the fp8_grid (bf16, laid out like the norm)
+    if (a.grid)
+      ok = encode(&mC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.grid, d2, s2, b2, CU_TENSOR_MAP_SWIZZLE_128B);
+    else
+      ok = encode(&mC, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.codes ? (const void*)a.codes : (const void*)a.norm, d2, sC,
+                  b2, CU_TENSOR_MAP_SWIZZLE_NONE);
+  }
   // carried gates: comb [T, 16], pre and post [T, 4] fp32, 32 token rows per box
   CUtensorMap mGc, mGp, mGq;
   const cuuint64_t dG16[2] = {16, T}, sG16[1] = {64}, dG4[2] = {4, T}, sG4[1] = {16};
@@ -951,7 +999,8 @@ static cudaError_t launch_with_maps(const SeamArgs& a, const CUtensorMap* m, boo
 
 static cudaError_t launch_range(const SeamArgs& a, const CUtensorMap* m, bool tcgen05_proj, int kcl, int block0,
                                 int n_blocks, cudaStream_t stream, unsigned long long limit_ns, int* launches) {
-  const bool post = a.Y != nullptr, mx = a.codes != nullptr, ms = !tcgen05_proj;
+  const bool post = a.Y != nullptr, ms = !tcgen05_proj;
+  const int mx = a.grid ? 2 : a.codes ? 1 : 0;
   void* k = stream_kernel_ptr(post, mx, ms, kcl);
   const int fit = max_clusters(post, mx, ms, kcl);
   if (fit <= 0) return cudaErrorInvalidValue;

@@ -7,6 +7,7 @@ Acceptance (per output):
   pre, post, comb      within 1e-3 absolute
   fp8 codes, scales    bit-exact against the oracle quantiser applied to the
                        kernel's own norm
+  fp8_grid             bit-exact against the oracle's grid of the kernel's norm
 """
 from __future__ import annotations
 
@@ -22,7 +23,7 @@ GATE_TOL = 1e-3
 
 
 def make_case(T: int, H: int, seed: int, post: bool = True, mxfp8: bool = False, craft: bool = False,
-              unique_tokens: int | None = None) -> dict:
+              unique_tokens: int | None = None, grid: bool = False) -> dict:
     d = I.seam_draws(T, H, seed, post=post, unique_tokens=unique_tokens)
     if craft:
         I.craft_mxfp8(d, seed)
@@ -30,7 +31,7 @@ def make_case(T: int, H: int, seed: int, post: bool = True, mxfp8: bool = False,
     d["pre_prev"] = torch.from_numpy(pre)
     d["post_prev"] = torch.from_numpy(post_g) if post else None
     d["comb_prev"] = torch.from_numpy(comb)
-    d["out_mode"] = B.MHC_OUT_MXFP8 if mxfp8 else B.MHC_OUT_BF16
+    d["out_mode"] = B.MHC_OUT_FP8_GRID if grid else (B.MHC_OUT_MXFP8 if mxfp8 else B.MHC_OUT_BF16)
     return d
 
 
@@ -111,6 +112,11 @@ def compare(d: dict, h: dict, idx: np.ndarray | None = None, check_quant: bool =
         rep["codes_mismatch"] = int(np.sum(codes != h["fp8_codes"]))
         rep["scales_mismatch"] = int(np.sum(scales != h["e8m0_scales"]))
         assert rep["codes_mismatch"] == 0 and rep["scales_mismatch"] == 0, rep
+    if d["out_mode"] == B.MHC_OUT_FP8_GRID and check_quant:
+        # bit-exact against the oracle's fp8_grid of the kernel's own norm (all tokens)
+        grid = O.grid_ue8m0(h["norm"])
+        rep["grid_mismatch"] = int(np.sum(grid != h["fp8_codes"]))
+        assert rep["grid_mismatch"] == 0, rep
     return rep
 
 

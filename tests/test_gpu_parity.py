@@ -420,3 +420,32 @@ def test_three_seams_chained(T, path, post):
                    "comb_prev": o["comb"].astype(np.float32)}
         g_state = {"R": out["residual_out"], "pre_prev": out["pre_out"],
                    "post_prev": out["post_out"] if post else None, "comb_prev": out["comb_out"]}
+
+
+# ------------------------------------------------------ fp8_grid out (f1) --
+@pytest.mark.parametrize("T,path,craft", [(1024, 2, True), (300, 2, False), (64, 3, True), (5, 3, False)])
+def test_fp8_grid(T, path, craft):
+    d = make_case(T, 5120, 8400 + T, grid=True, craft=craft)
+    h = to_host(run_gpu(d, cfg=B.MhcConfig(path=path)))
+    rep = compare(d, h, sample_tokens(T, 24, 8400 + T, must=d.get("crafted_rows")) if T > 256 else None)
+    assert rep["grid_mismatch"] == 0
+    if craft:  # crafted gamma groups: the grid of a 448 * 2^k group is the group itself
+        g = I.bf16_bits(d["gamma"])
+        for t in d["crafted_rows"]:
+            for grp in d["crafted_groups"]:
+                sl = slice(32 * grp, 32 * grp + 32)
+                assert np.array_equal(h["norm"][t, sl], g[sl]), (t, grp)
+
+
+@pytest.mark.parametrize("H", [512, 4096, 7168])
+def test_fp8_grid_widths(H):
+    d = make_case(40, H, 8500 + H, grid=True)
+    compare(d, to_host(run_gpu(d, cfg=B.MhcConfig(path=2))))
+
+
+def test_fp8_grid_no_post_and_split_path_refused():
+    d = make_case(70, 5120, 8600, grid=True, post=False)
+    compare(d, to_host(run_gpu(d, cfg=B.MhcConfig(path=2))))
+    with pytest.raises(B.MhcError) as e:
+        run_gpu(d, cfg=B.MhcConfig(path=1))
+    assert e.value.code == -10
