@@ -166,7 +166,8 @@ def seam(R, Y, post_prev, comb_prev, pre_prev, fn, bias, alpha, gamma, eps: floa
     bit arrays; fp32 inputs may be tensors or arrays.  Returns a dict with
     ``residual_out`` [T,4,H] and ``norm`` [T,H] as uint16 bits, ``pre``,
     ``post`` [T,4], ``comb`` [T,4,4], ``rstd`` [T,2] in float64 and
-    optionally ``x`` [T,H] float64."""
+    optionally ``x`` [T,H] float64.  ``comb_prev`` None (with ``Y`` and
+    ``post_prev`` None) is the identity form of the first block: R' = R."""
     Rb = _u16(R)
     T, n, H = Rb.shape
     assert n == 4
@@ -189,7 +190,7 @@ def seam(R, Y, post_prev, comb_prev, pre_prev, fn, bias, alpha, gamma, eps: floa
                                _ptr(out["residual_out"]), _ptr(out["norm"]), _ptr(out["pre"]),
                                _ptr(out["post"]), _ptr(out["comb"]), _ptr(out["rstd"]), _ptr(x))
     if rc != 0:
-        raise ValueError("oracle rejected the inputs (NULL operand or half-present post inputs)")
+        raise ValueError("oracle rejected the inputs (NULL operand, half-present post inputs, or Y without comb)")
     if want_x:
         out["x"] = x
     return out

@@ -217,12 +217,17 @@ double mhc_oracle_sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
  * [T,H] bf16 bits; post_prev, pre_prev [T,4], comb_prev [T,4,4] fp32; fn
  * [4H,24] fp32 with row i*H + h for stream i, column h; bias [24], alpha [3]
  * fp32; gamma [H] bf16 bits.  Y and post_prev are both NULL for the no_post
- * form (R' = comb . R).  Outputs pre_out, post_out [T,4], comb_out [T,16] in
+ * form (R' = comb . R).  comb_prev NULL as well selects the identity form of
+ * the first block ("[FlyDSL] Single-launch Mega-mHC on gfx950", Correctness,
+ * which compares a "first block" form beside post and no_post; read here as
+ * the seam with nothing to mix in): R' = R bit for bit, and residual_out
+ * receives that copy.  Outputs pre_out, post_out [T,4], comb_out [T,16] in
  * double; rstd_out [T,2] = (rstd over 4H of R', rstd over H of x) and x_out
  * [T,H] are optional.  rprime_unrounded = 1 feeds the unrounded R' (instead
  * of the stored bf16 one) to the sums, the projection and x; it exists to
  * measure how much that reading matters.
- * Returns 0, or -1 on a NULL required pointer or a half-present post input. */
+ * Returns 0, or -1 on a NULL required pointer, a half-present post input, or
+ * a post input given without comb_prev. */
 int mhc_oracle_seam(int64_t T, int H,
                     const uint16_t* R, const uint16_t* Y,
                     const float* post_prev, const float* comb_prev, const float* pre_prev,
@@ -232,7 +237,8 @@ int mhc_oracle_seam(int64_t T, int H,
                     double* pre_out, double* post_out, double* comb_out,
                     double* rstd_out, double* x_out) {
     if ((Y == NULL) != (post_prev == NULL)) return -1;
-    if (!R || !comb_prev || !pre_prev || !fn || !bias || !alpha || !gamma) return -1;
+    if (!comb_prev && Y) return -1;
+    if (!R || !pre_prev || !fn || !bias || !alpha || !gamma) return -1;
     if (!residual_out || !norm || !pre_out || !post_out || !comb_out) return -1;
     const int K = N_HC * H;
     double* rp = (double*)malloc(sizeof(double) * (size_t)K);
@@ -241,11 +247,17 @@ int mhc_oracle_seam(int64_t T, int H,
 
     for (int64_t t = 0; t < T; ++t) {
         const uint16_t* Rt = R + t * K;
-        const float* comb = comb_prev + t * 16;
+        const float* comb = comb_prev ? comb_prev + t * 16 : NULL;
         /* 1. post-mix: R'[i][h] = sum_j comb[i][j] R[j][h] + post[i] Y[h],
-         *    stored as bf16 (round to nearest even). */
+         *    stored as bf16 (round to nearest even); the identity form keeps R. */
         for (int i = 0; i < N_HC; ++i) {
             for (int h = 0; h < H; ++h) {
+                if (!comb) {
+                    const uint16_t b = Rt[i * H + h];
+                    residual_out[t * K + i * H + h] = b;
+                    rp[i * H + h] = mhc_oracle_bf16_to_double(b);
+                    continue;
+                }
                 double v = 0.0;
                 for (int j = 0; j < N_HC; ++j)
                     v += (double)comb[i * 4 + j] * mhc_oracle_bf16_to_double(Rt[j * H + h]);

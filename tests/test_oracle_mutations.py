@@ -32,9 +32,11 @@ MUTATIONS = {
     "grid_scale_off_by_one": ("mhc_oracle_bf16_rne(ldexp(mhc_oracle_e4m3_decode(code), e))",
                               "mhc_oracle_bf16_rne(ldexp(mhc_oracle_e4m3_decode(code), e + 1))"),
     "e4m3_decode_bias_8": ("ldexp(1.0 + f / 8.0, E - 7)", "ldexp(1.0 + f / 8.0, E - 8)"),
+    "identity_form_stream_shifted": ("const uint16_t b = Rt[i * H + h];", "const uint16_t b = Rt[((i + 1) % N_HC) * H + h];"),
 }
 
 PINS = [
+    P.test_identity_form_keeps_signed_zeros_and_subnormals,
     P.test_e4m3_decode_matches_format_definition,
     P.test_grid_exact_on_the_e4m3_lattice,
     P.test_grid_is_the_dequantised_mxfp8_output,

@@ -417,9 +417,9 @@ def _brute_force_seam(d, t=0):
     getcontext().prec = 60
     H = d["H"]
     Rv = d["R"].to(torch.float64).numpy()[t]
-    Yv = d["Y"].to(torch.float64).numpy()[t]
-    comb = d["comb_prev"][t].astype(np.float64)
-    post = d["post_prev"][t].astype(np.float64)
+    Yv = None if d["Y"] is None else d["Y"].to(torch.float64).numpy()[t]
+    comb = None if d["comb_prev"] is None else d["comb_prev"][t].astype(np.float64)
+    post = None if d["post_prev"] is None else d["post_prev"][t].astype(np.float64)
     pre = d["pre_prev"][t].astype(np.float64)
     fn = d["fn"].to(torch.float64).numpy()
     gam = d["gamma"].to(torch.float64).numpy()
@@ -428,8 +428,13 @@ def _brute_force_seam(d, t=0):
     rp = [[None] * H for _ in range(4)]
     for i in range(4):
         for h in range(H):
-            v = sum(Fraction(comb[i, j]) * Fraction(Rv[j, h]) for j in range(4)) + Fraction(post[i]) * Fraction(Yv[h])
-            b = bf16_rne_exact(v)
+            if comb is None:  # the identity form: R' = R, no rounding
+                b = int(I.bf16_bits(d["R"][t])[i, h])
+            else:
+                v = sum(Fraction(comb[i, j]) * Fraction(Rv[j, h]) for j in range(4))
+                if Yv is not None:
+                    v += Fraction(post[i]) * Fraction(Yv[h])
+                b = bf16_rne_exact(v)
             res[i, h] = b
             rp[i][h] = Fraction(bf16_val(b))
     K = 4 * H
@@ -476,6 +481,45 @@ def test_brute_force_T1_H8_asymmetric_comb(oracle, seed):
     assert np.allclose(o["pre"][0], g_pre, atol=1e-13, rtol=0)
     assert np.allclose(o["post"][0], g_post, atol=1e-13, rtol=0)
     assert np.allclose(o["comb"][0], comb, atol=1e-13, rtol=0)
+
+
+@pytest.mark.parametrize("seed", [34, 35])
+def test_brute_force_T1_H8_identity_form(oracle, seed):
+    # the first-block form: nothing mixed in, R' = R; gates and norm from R
+    d = seam_inputs(1, 8, seed, post=False, oracle=oracle)
+    d["comb_prev"] = None
+    d["bias"] = torch.linspace(-0.4, 0.6, 24)
+    d["alpha"] = torch.tensor([1.1, 0.7, 0.9])
+    o = run(oracle, d)
+    res, norm, g_pre, g_post, comb = _brute_force_seam(d)
+    assert np.array_equal(o["residual_out"][0], res)
+    assert np.array_equal(o["residual_out"][0], I.bf16_bits(d["R"][0]))
+    assert np.array_equal(o["norm"][0], norm)
+    assert np.allclose(o["pre"][0], g_pre, atol=1e-13, rtol=0)
+    assert np.allclose(o["post"][0], g_post, atol=1e-13, rtol=0)
+    assert np.allclose(o["comb"][0], comb, atol=1e-13, rtol=0)
+
+
+def test_identity_form_keeps_signed_zeros_and_subnormals(oracle):
+    # R' = R bit for bit, where comb = I would turn -0 into +0 (1 * -0 + 0 * r)
+    d = seam_inputs(2, 64, 36, post=False, oracle=oracle)
+    bits = I.bf16_bits(d["R"]).copy()
+    bits[0, 0, :8] = 0x8000                     # -0
+    bits[0, 1, :8] = 0x0001                     # smallest subnormal
+    bits[1, 2, 5] = 0x8001
+    d["R"] = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+    ident = run(oracle, dict(d, comb_prev=None))
+    assert np.array_equal(ident["residual_out"], bits)
+    eye = run(oracle, dict(d, comb_prev=np.tile(np.eye(4, dtype=np.float32), (2, 1, 1))))
+    assert not np.array_equal(eye["residual_out"], bits)  # the -0 entries differ
+    # away from the signed zeros the two forms agree
+    assert np.array_equal(ident["norm"][1], eye["norm"][1])
+
+
+def test_oracle_rejects_y_without_comb(oracle):
+    d = seam_inputs(1, 8, 41, oracle=oracle)
+    with pytest.raises(ValueError):
+        run(oracle, dict(d, comb_prev=None))
 
 
 def test_oracle_rejects_half_present_post(oracle):
