@@ -47,6 +47,8 @@ WORKLOADS = {
     "seam_T4160_H5120_post_bf16": dict(T=4160, H=5120, post=True, out="bf16", seed=1003),
     "seam_T1024_H5120_post_mxfp8": dict(T=1024, H=5120, post=True, out="mxfp8", seed=1002),
     "seam_T16384_H5120_post_fp8grid": dict(T=16384, H=5120, post=True, out="fp8_grid", seed=1004),
+    # the identity (first-block) form: no Y, no post, no comb; R' = R is not written
+    "seam_T16384_H5120_first_bf16": dict(T=16384, H=5120, post=False, out="bf16", seed=1004, ident=True),
     "seam_T64_H5120_post_bf16": dict(T=64, H=5120, post=True, out="bf16", seed=1001),
     "seam_T64_H5120_nopost_bf16": dict(T=64, H=5120, post=False, out="bf16", seed=1001),
     "seam_T4_H5120_post_bf16": dict(T=4, H=5120, post=True, out="bf16", seed=1000),
@@ -89,7 +91,8 @@ def carried_gates(pre_l, post_l, comb_l, iters: int = 20):
 def make_workload(w: dict, device) -> dict:
     d = I.seam_draws(w["T"], w["H"], w["seed"], post=w["post"], unique_tokens=UNIQUE_TOKENS)
     pre, post, comb = carried_gates(d["pre_logits"], d["post_logits"], d["comb_logits"])
-    host = {"R": d["R"], "Y": d["Y"], "post_prev": post if w["post"] else None, "comb_prev": comb, "pre_prev": pre,
+    host = {"R": d["R"], "Y": d["Y"], "post_prev": post if w["post"] else None,
+            "comb_prev": None if w.get("ident") else comb, "pre_prev": pre,
             "fn": d["fn"], "bias": d["bias"], "alpha": d["alpha"], "gamma": d["gamma"]}
     dev = {k: (None if v is None else v.to(device)) for k, v in host.items()}
     return {"host": host, "dev": dev, "eps": d["eps"], "draws": d}
@@ -167,6 +170,8 @@ def run_ours(args, w: dict, rank: int, world: int, local_rank: int) -> dict | No
     cfg = B.MhcConfig(projection={"auto": 0, "mma": 1, "tcgen05": 2}[args.projection],
                       path={"auto": 0, "split": 1, "stream": 2, "stream16": 3}[args.path])
     out = B.alloc_outputs(T, H, mode, device, cfg)
+    if w.get("ident"):  # the identity form writes no residual
+        out["residual_out"] = None
 
     def step():
         B.mhc_seam(g["R"], g["Y"], g["post_prev"], g["comb_prev"], g["pre_prev"], g["fn"], g["fn_packed"], g["bias"],
@@ -221,7 +226,7 @@ def run_ours(args, w: dict, rank: int, world: int, local_rank: int) -> dict | No
     if not args.no_e2e:
         pin = {k: (None if v is None else v.pin_memory()) for k, v in host.items()
                if k in ("R", "Y", "post_prev", "comb_prev", "pre_prev")}
-        outs = ["residual_out", "norm", "pre_out", "post_out", "comb_out"] + (
+        outs = ([] if w.get("ident") else ["residual_out"]) + ["norm", "pre_out", "post_out", "comb_out"] + (
             ["fp8_codes", "e8m0_scales"] if mx else (["fp8_codes"] if mode == B.MHC_OUT_FP8_GRID else []))
         pout = {k: torch.empty(out[k].shape, dtype=out[k].dtype).pin_memory() for k in outs}
         bi = sum(v.numel() * v.element_size() for v in pin.values() if v is not None)
@@ -248,7 +253,8 @@ def run_ours(args, w: dict, rank: int, world: int, local_rank: int) -> dict | No
                             g[k][t0:t1].copy_(v[t0:t1], non_blocking=True)
                     sl = {k: (None if v is None else v[t0:t1]) for k, v in out.items() if k != "workspace"}
                     B.mhc_seam(g["R"][t0:t1], None if g["Y"] is None else g["Y"][t0:t1],
-                               None if g["post_prev"] is None else g["post_prev"][t0:t1], g["comb_prev"][t0:t1],
+                               None if g["post_prev"] is None else g["post_prev"][t0:t1],
+                               None if g["comb_prev"] is None else g["comb_prev"][t0:t1],
                                g["pre_prev"][t0:t1], g["fn"], g["fn_packed"], g["bias"], g["alpha"], g["gamma"],
                                wl["eps"], mode, sl["residual_out"], sl["norm"], sl["fp8_codes"], sl["e8m0_scales"],
                                sl["pre_out"], sl["post_out"], sl["comb_out"], spaces[i % len(streams)], cfg=cfg,
@@ -285,15 +291,19 @@ def cpu_baseline(w: dict, wl: dict | None, budget_s: float = 15.0, steps: int = 
 
     d = wl["draws"] if wl else I.seam_draws(w["T"], w["H"], w["seed"], post=w["post"], unique_tokens=UNIQUE_TOKENS)
     pre, post, comb = carried_gates(d["pre_logits"], d["post_logits"], d["comb_logits"])
+    if w.get("ident"):
+        comb = None
     t0 = time.perf_counter()
-    O.seam(d["R"][:1], d["Y"][:1] if w["post"] else None, post[:1] if w["post"] else None, comb[:1], pre[:1],
+    O.seam(d["R"][:1], d["Y"][:1] if w["post"] else None, post[:1] if w["post"] else None,
+           None if comb is None else comb[:1], pre[:1],
            d["fn"], d["bias"], d["alpha"], d["gamma"], d["eps"])
     per_tok = max(time.perf_counter() - t0, 1e-4)
     n = int(max(1, min(w["T"], budget_s / per_tok)))
     times = []
     for _ in range(steps):
         t0 = time.perf_counter()
-        o = O.seam(d["R"][:n], d["Y"][:n] if w["post"] else None, post[:n] if w["post"] else None, comb[:n],
+        o = O.seam(d["R"][:n], d["Y"][:n] if w["post"] else None, post[:n] if w["post"] else None,
+                   None if comb is None else comb[:n],
                    pre[:n], d["fn"], d["bias"], d["alpha"], d["gamma"], d["eps"])
         if w["out"] == "mxfp8":
             O.quant_ue8m0(o["norm"])
@@ -301,7 +311,7 @@ def cpu_baseline(w: dict, wl: dict | None, budget_s: float = 15.0, steps: int = 
             O.grid_ue8m0(o["norm"])
         times.append(time.perf_counter() - t0)
     sec = statistics.median(times)
-    b = ACC.seam_bytes(n, w["H"], post=w["post"], out=w["out"])
+    b = ACC.seam_bytes(n, w["H"], post=w["post"], out=w["out"], ident=w.get("ident", False))
     return {"value": b / sec / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle", "seconds": sec,
             "sample": f"first {n} of {w['T']} tokens of the same workload, single-threaded C oracle (fp64)"}
 
@@ -352,13 +362,13 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     config = {"workload": args.workload, "T": w["T"], "H": w["H"], "n_hc": 4,
-              "form": "post" if w["post"] else "no_post", "out": w["out"],
+              "form": "identity" if w.get("ident") else ("post" if w["post"] else "no_post"), "out": w["out"],
               "tokens_per_rank": w["T"], "parallelism": f"token-shard x{args.gpus} (independent)",
               "projection": args.projection, "path": args.path,
               "timing": (f"cuda-graph replay ({GRAPH_CALLS} calls per graph)" if args.graph
                          else "back-to-back launches"),
               "e2e_pipeline": "token slices (8 from T=2048, 4 from T=512) on two streams, copies overlapping seams",
-              "l2": "inputs larger than L2" if ACC.seam_bytes(w["T"], w["H"], w["post"], w["out"]) > 2 * L2_BYTES
+              "l2": "inputs larger than L2" if ACC.seam_bytes(w["T"], w["H"], w["post"], w["out"], ident=w.get("ident", False)) > 2 * L2_BYTES
               else "inputs smaller than L2 (warm)"}
 
     if args.impl == "reference":
@@ -384,7 +394,7 @@ def main():
         torch.distributed.destroy_process_group()
     if rank != 0:
         return
-    step_bytes = ACC.seam_bytes(w["T"], w["H"], post=w["post"], out=w["out"])
+    step_bytes = ACC.seam_bytes(w["T"], w["H"], post=w["post"], out=w["out"], ident=w.get("ident", False))
     value = job_value(world, step_bytes, r["ms"])
     peaks = load_peaks()
     launch_ms = r["ms"] / max(1, r["launches"])

@@ -230,7 +230,12 @@ int mhc_seam(const void* R, const void* Y, const float* post_prev, const float* 
   if (T == 0) return MHC_OK;
   if ((Y == nullptr) != (post_prev == nullptr))
     return fail(MHC_ERR_INCOMPLETE_POST, "Y and post_prev must both be given (post form) or both be NULL (no_post)");
-  if (!R || !comb_prev || !pre_prev || !fn || !bias || !alpha || !gamma || !residual_out || !norm || !pre_out ||
+  // comb_prev NULL: the identity (first-block) form, R' = R; residual_out is
+  // not written (and may be NULL)
+  const bool ident = comb_prev == nullptr;
+  if (ident && Y) return fail(MHC_ERR_INCOMPLETE_POST, "the identity form (comb_prev NULL) takes no Y and no post_prev");
+  if (ident) residual_out = nullptr;
+  if (!R || !pre_prev || !fn || !bias || !alpha || !gamma || (!ident && !residual_out) || !norm || !pre_out ||
       !post_out || !comb_out)
     return fail(MHC_ERR_NULL, "a required pointer is NULL");
   if (mx && (!fp8_codes || !e8m0_scales)) return fail(MHC_ERR_NULL, "mxfp8 output needs fp8_codes and e8m0_scales");
@@ -250,10 +255,10 @@ int mhc_seam(const void* R, const void* Y, const float* post_prev, const float* 
   // Overlap checks: outputs against inputs (R' may be R exactly) and each other.
   const size_t TH = (size_t)T * H;
   Range in[] = {rng(R, TH * 8), rng(Y, Y ? TH * 2 : 0), rng(post_prev, post_prev ? (size_t)T * 16 : 0),
-                rng(comb_prev, (size_t)T * 64), rng(pre_prev, (size_t)T * 16), rng(fn, (size_t)H * 4 * 24 * 4),
+                rng(comb_prev, comb_prev ? (size_t)T * 64 : 0), rng(pre_prev, (size_t)T * 16), rng(fn, (size_t)H * 4 * 24 * 4),
                 rng(fn_packed, fn_packed ? mhc_packed_fn_bytes(H) : 0), rng(bias, 96), rng(alpha, 12),
                 rng(gamma, (size_t)H * 2)};
-  Range out[] = {rng(residual_out, TH * 8), rng(norm, TH * 2), rng(fp8_codes, mx ? TH : (gridm ? TH * 2 : 0)),
+  Range out[] = {rng(residual_out, residual_out ? TH * 8 : 0), rng(norm, TH * 2), rng(fp8_codes, mx ? TH : (gridm ? TH * 2 : 0)),
                  rng(e8m0_scales, mx ? TH / 32 : 0), rng(pre_out, (size_t)T * 16), rng(post_out, (size_t)T * 16),
                  rng(comb_out, (size_t)T * 64), rng(workspace, need)};
   const int n_in = sizeof in / sizeof in[0], n_out = sizeof out / sizeof out[0];

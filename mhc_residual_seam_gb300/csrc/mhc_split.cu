@@ -70,11 +70,13 @@ __global__ void __launch_bounds__(kSplitThreads) split_seam_kernel(SeamArgs a, i
   const int64_t t = t0 + tl;
   const bool tvalid = t < T;
 
+  // no comb: the identity (first-block) form, R' = R and no residual write
+  const bool ident = a.comb_prev == nullptr;
   float comb[16], postg[4], preg[4];
   if (tvalid) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      float4 c = __ldg(reinterpret_cast<const float4*>(a.comb_prev + t * 16) + q);
+      float4 c = ident ? make_float4(0.f, 0.f, 0.f, 0.f) : __ldg(reinterpret_cast<const float4*>(a.comb_prev + t * 16) + q);
       comb[4 * q] = c.x; comb[4 * q + 1] = c.y; comb[4 * q + 2] = c.z; comb[4 * q + 3] = c.w;
     }
     float4 p = __ldg(reinterpret_cast<const float4*>(a.pre_prev + t * 4));
@@ -115,10 +117,12 @@ __global__ void __launch_bounds__(kSplitThreads) split_seam_kernel(SeamArgs a, i
           if (POST) s = fmaf(postg[i], y[e], s);
           v[e] = s;
         }
-        uint4 ov;
-        ov.x = pack_bf16x2(v[0], v[1]); ov.y = pack_bf16x2(v[2], v[3]);
-        ov.z = pack_bf16x2(v[4], v[5]); ov.w = pack_bf16x2(v[6], v[7]);
-        st_stream(a.res_out + (t * kStreams + i) * H + h, ov);
+        uint4 ov = rv[i];
+        if (!ident) {
+          ov.x = pack_bf16x2(v[0], v[1]); ov.y = pack_bf16x2(v[2], v[3]);
+          ov.z = pack_bf16x2(v[4], v[5]); ov.w = pack_bf16x2(v[6], v[7]);
+          st_stream(a.res_out + (t * kStreams + i) * H + h, ov);
+        }
         float rp[8];
         unpack8(ov, rp);
         const float4* f = reinterpret_cast<const float4*>(a.fn + ((size_t)i * H + h) * kLogits);

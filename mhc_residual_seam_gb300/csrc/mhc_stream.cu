@@ -26,7 +26,9 @@
 //    leaves no room for that accumulator in tensor memory, warp-level m16n8k16
 //    MMAs in the compute warps;
 //  - a store warp TMA-stores the R' tiles and the norm tile of each stage
-//    (and computes the ue8m0 codes of the norm tile).
+//    (and computes the e4m3 codes and ue8m0 scales of the norm tile); with
+//    the fp8_grid output three more warps each take every third stage and
+//    write the grid of its norm tile.
 // After the last chunk of a block the compute warps hand their partial sums
 // over in shared memory and go on; an exchange warp sends, through
 // distributed shared memory (st.async completing bytes on the receiver's
@@ -55,7 +57,12 @@ constexpr int kBM = 32;                // tokens per block
 constexpr int kChunk = 64;             // columns per chunk
 constexpr int kNF = 2, kNO = 3;
 constexpr int kComputeThreads = 256;   // warps 0-7
-constexpr int kThreads = 416;          // + 8 input producer, 9 MMA issuer, 10 fn producer, 11 finisher, 12 store
+// + 8 input producer, 9 MMA issuer, 10 fn producer, 11 finisher, 12 store,
+// and with the fp8_grid output 13-15 grid warps (warp 13 + o takes output
+// stage o).  16 warps still leave each thread 128 registers (4 warps per SM
+// sub-partition, as with 13).
+template <int OUT>
+__host__ __device__ constexpr int threads_of() { return OUT == 2 ? 512 : 416; }
 constexpr int kFnRows = 48;
 constexpr uint32_t kRTile = kBM * 128;                 // 4 KB
 constexpr uint32_t kFnTile = kFnRows * 128;            // 6 KB
@@ -66,10 +73,9 @@ constexpr uint32_t kOffCodesT = 5 * kRTile;            //   then the codes tile 
 constexpr uint32_t kOutStage = 5 * kRTile + kBM * 64;  // 22 KB (a multiple of 1 KB: swizzled tiles)
 // The normalise-only pass after a cluster's last block puts the norm tiles of
 // norm_group() chunks in one output stage (in the R' tile slots; with mxfp8
-// the codes tiles go where the norm tile sits in the other passes, with
-// fp8_grid the grid tiles take R' slots 2 and 3).
-template <bool QUANT>
-__host__ __device__ constexpr int norm_group() { return QUANT ? 2 : 4; }
+// the codes tiles go where the norm tile sits in the other passes).
+template <int OUT>
+__host__ __device__ constexpr int norm_group() { return OUT == 1 ? 2 : 4; }
 constexpr uint32_t kOffFn = 0;
 constexpr uint32_t kOffOut = kOffFn + kNF * kFnStage;
 constexpr uint32_t kTmemCols = 512;
@@ -167,10 +173,12 @@ __device__ __noinline__ void finish_store_gates(const SeamArgs& a, int64_t t, co
   store_gates(a, t, pre, post, cb);
 }
 
+// FORM: 0 no_post (R' = comb . R), 1 post (+ post (x) Y), 2 identity: the
+// first block's form, R' = R, no residual write.
 // OUT: 0 bf16 norm, 1 mxfp8 (+ e4m3 codes, e8m0 scales), 2 fp8_grid (+ the
 // quantisation dequantised to bf16)
-template <bool POST, int OUT, bool MS, int KCL>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int FORM, int OUT, bool MS, int KCL>
+__global__ void __launch_bounds__(threads_of<OUT>(), 1)
     stream_seam_kernel(const SeamArgs a, const __grid_constant__ CUtensorMap tmR,
                        const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmRo,
                        const __grid_constant__ CUtensorMap tmFn, const __grid_constant__ CUtensorMap tmN,
@@ -180,7 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   using G = Geo<KCL>;
-  constexpr bool QUANT = OUT != 0;
+  constexpr int kThreads = threads_of<OUT>();
+  constexpr bool POST = FORM == 1, IDENT = FORM == 2;
   constexpr int kCl = G::kCl, kNI = G::kNI, kSlots = G::kSlots;
   constexpr uint32_t kOffIn = G::kOffIn, kXsBytes = G::kXsBytes, kRecvBytes = G::kRecvBytes;
   typename G::Tail* tl = reinterpret_cast<typename G::Tail*>(sm + G::kOffTail);
@@ -211,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < kNO; ++s) {
       mbar_init(&tl->out_full[s], 8);
-      mbar_init(&tl->out_empty[s], MS ? 9 : 2);
+      mbar_init(&tl->out_empty[s], (MS ? 9 : 2) + (OUT == 2 ? 1 : 0));
     }
     mbar_init(&tl->d_full, 1);
     mbar_init(&tl->gates_full, 1);
@@ -232,13 +241,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 8 && lane == 0) {
     prefetch_tmap(&tmR);
     if (POST) prefetch_tmap(&tmY);
-    prefetch_tmap(&tmGc);
+    if (!IDENT) prefetch_tmap(&tmGc);
     prefetch_tmap(&tmGp);
     if (POST) prefetch_tmap(&tmGq);
   }
   if (warp == 10 && lane == 0) prefetch_tmap(&tmFn);
   if (warp == 12 && lane == 0) {
-    prefetch_tmap(&tmRo);
+    if (!IDENT) prefetch_tmap(&tmRo);
     prefetch_tmap(&tmN);
     if (OUT == 1) prefetch_tmap(&tmC);
   }
@@ -268,8 +277,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t0 = (bb + lb * ncl) * kBM;
         {  // the block's carried gates, consumed at the top of its compute
           wait_local(X, &tl->gates_empty, (lb & 1) ^ 1);
-          mbar_arrive_expect_tx(&tl->gates_full, (POST ? 24 : 20) * kBM * 4);
-          tma_load_2d(&tl->gates.comb[0][0], &tmGc, &tl->gates_full, 0, t0, pol);
+          mbar_arrive_expect_tx(&tl->gates_full, (IDENT ? 4 : POST ? 24 : 20) * kBM * 4);
+          if (!IDENT) tma_load_2d(&tl->gates.comb[0][0], &tmGc, &tl->gates_full, 0, t0, pol);
           tma_load_2d(&tl->gates.pre[0][0], &tmGp, &tl->gates_full, 0, t0, pol);
           if (POST) tma_load_2d(&tl->gates.post[0][0], &tmGq, &tl->gates_full, 0, t0, pol);
         }
@@ -315,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int j = 0, jr = 0;
       for (int lb = 0; lb <= nblk; ++lb) {
         if (lb == nblk) {  // the normalise-only pass: one stage per group of chunks, no MMA
-          for (int c0 = 0; c0 < nch; c0 += norm_group<QUANT>(), ++j) {
+          for (int c0 = 0; c0 < nch; c0 += norm_group<OUT>(), ++j) {
             wait_local(X, &tl->out_full[j % kNO], (j / kNO) & 1);
             mbar_arrive(&tl->out_empty[j % kNO]);
           }
@@ -342,33 +351,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 12) {
-    // ---------------------------- stores: R' tiles, norm tile, ue8m0 codes --
+    // ---------------------------- stores: R' tiles, norm tile, e4m3 codes --
     int j = 0;
-    // lane = token: the fp8_grid values of one norm tile row into registers,
-    // and their store as a swizzled bf16 tile like the norm tile
-    auto grid_regs = [&](const uint8_t* nt, uint32_t* gw) {
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t nb[16];
-#pragma unroll
-        for (int jq = 0; jq < 4; ++jq) {
-          const int ch = 4 * half + jq;
-          uint4 v = *reinterpret_cast<const uint4*>(nt + lane * 128 + ((ch ^ (lane & 7)) << 4));
-          nb[4 * jq] = v.x; nb[4 * jq + 1] = v.y; nb[4 * jq + 2] = v.z; nb[4 * jq + 3] = v.w;
-        }
-        grid_group32(nb, gw + 16 * half, a.amax_floor);
-      }
-    };
-    // the grid row of token tp + lane, columns h .. h + 63, straight from
-    // registers: each lane writes its own 128 contiguous bytes
-    auto store_grid = [&](int64_t tp, int h, const uint32_t* gw) {
-      const int64_t tt = tp + lane;
-      if (tt < T) {
-        uint4* dst = reinterpret_cast<uint4*>(a.grid + tt * H + h);
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) st_stream(dst + ch, make_uint4(gw[4 * ch], gw[4 * ch + 1], gw[4 * ch + 2], gw[4 * ch + 3]));
-      }
-    };
     // lane = token: the ue8m0 codes of one norm tile (two 32-column groups)
     auto quant_tile = [&](const uint8_t* nt, uint8_t* ct, int64_t tp, int h) {
 #pragma unroll
@@ -393,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool real = lb < nblk, prev = lb > 0;
       const int t0 = (bb + lb * ncl) * kBM, tp = (bb + (lb - 1) * ncl) * kBM;
       if (!real) {  // the normalise-only pass: the norm tiles of a group of chunks per stage
-        constexpr int G = norm_group<QUANT>();
+        constexpr int G = norm_group<OUT>();
         for (int c0 = 0; c0 < nch && prev; c0 += G, ++j) {
           const int o = j % kNO;
           uint8_t* ost = sm + kOffOut + o * kOutStage;
@@ -404,13 +388,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               quant_tile(ost + g * kRTile, ost + kOffNormT + g * 2048, tp, ((c0 + g) * kCl + (int)rank) * kChunk);
             fence_proxy_async_smem();
             __syncwarp();
-          }
-          if (OUT == 2) {
-            for (int g = 0; g < ng; ++g) {
-              uint32_t gw[32];
-              grid_regs(ost + g * kRTile, gw);
-              store_grid(tp, ((c0 + g) * kCl + (int)rank) * kChunk, gw);
-            }
           }
           if (lane == 0) {
             for (int g = 0; g < ng; ++g) {
@@ -431,16 +408,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* ost = sm + kOffOut + o * kOutStage;
         const int h = (c * kCl + (int)rank) * kChunk;
         wait_local(X, &tl->out_full[o], (j / kNO) & 1);
-        uint32_t gw[OUT == 2 ? 32 : 1];
         if (OUT == 1 && prev) {
           quant_tile(ost + kOffNormT, ost + kOffCodesT, tp, h);
           fence_proxy_async_smem();
           __syncwarp();
         }
-        if (OUT == 2 && prev) grid_regs(ost + kOffNormT, gw);
         if (lane == 0) {
+          if (!IDENT) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) tma_store_3d(&tmRo, ost + i * kRTile, h, i, t0);
+            for (int i = 0; i < 4; ++i) tma_store_3d(&tmRo, ost + i * kRTile, h, i, t0);
+          }
           if (prev) {
             tma_store_2d(&tmN, ost + kOffNormT, h, tp);
             if (OUT == 1) tma_store_2d(&tmC, ost + kOffCodesT, h, tp);
@@ -450,10 +427,75 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (lane == 0) mbar_arrive(&tl->out_empty[o]);
         __syncwarp();
-        if (OUT == 2 && prev) store_grid(tp, h, gw);
       }
     }
     if (lane == 0) tma_store_wait_all();
+  } else if (OUT == 2 && warp >= 13) {
+    // ------------------------------------------------------ grid warps --
+    // fp8_grid: warp 13 + o reads the norm tiles of output stage o and writes
+    // their grid (bf16 of the dequantised e4m3 codes) straight to global
+    // memory; the stage is free again once it has read them.
+    const int me = warp - 13;
+    // lane = token: one norm tile row (64 bf16) into registers, so the stage
+    // can be released before the grid is computed from them
+    auto load_row = [&](const uint8_t* nt, uint32_t* nb) {
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        const uint4 v = *reinterpret_cast<const uint4*>(nt + lane * 128 + ((ch ^ (lane & 7)) << 4));
+        nb[4 * ch] = v.x; nb[4 * ch + 1] = v.y; nb[4 * ch + 2] = v.z; nb[4 * ch + 3] = v.w;
+      }
+    };
+    // the grid row of token tp + lane, columns h .. h + 63, straight from
+    // registers: each lane writes its own 128 contiguous bytes
+    auto store_grid = [&](int64_t tp, int h, const uint32_t* gw) {
+      const int64_t tt = tp + lane;
+      if (tt < T) {
+        uint4* dst = reinterpret_cast<uint4*>(a.grid + tt * H + h);
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) st_stream(dst + ch, make_uint4(gw[4 * ch], gw[4 * ch + 1], gw[4 * ch + 2], gw[4 * ch + 3]));
+      }
+    };
+    int j = 0;
+    for (int lb = 0; lb <= nblk; ++lb) {
+      const bool real = lb < nblk, prev = lb > 0;
+      const int64_t tp = (int64_t)(bb + (lb - 1) * ncl) * kBM;
+      if (!real) {  // the normalise-only pass: the norm tiles of a group of chunks per stage
+        constexpr int G = norm_group<OUT>();
+        for (int c0 = 0; c0 < nch && prev; c0 += G, ++j) {
+          const int o = j % kNO;
+          if (o != me) continue;
+          const uint8_t* ost = sm + kOffOut + o * kOutStage;
+          wait_local(X, &tl->out_full[o], (j / kNO) & 1);
+          const int ng = min(G, nch - c0);
+          for (int g = 0; g < ng; ++g) {
+            uint32_t nb[32], gw[32];
+            load_row(ost + g * kRTile, nb);
+            __syncwarp();
+            if (g == ng - 1 && lane == 0) mbar_arrive(&tl->out_empty[o]);
+            grid_group32(nb, gw, a.amax_floor);
+            grid_group32(nb + 16, gw + 16, a.amax_floor);
+            store_grid(tp, ((c0 + g) * kCl + (int)rank) * kChunk, gw);
+          }
+        }
+        break;
+      }
+      for (int c = 0; c < nch; ++c, ++j) {
+        const int o = j % kNO;
+        if (o != me) continue;
+        const uint8_t* ost = sm + kOffOut + o * kOutStage;
+        wait_local(X, &tl->out_full[o], (j / kNO) & 1);
+        uint32_t nb[32];
+        if (prev) load_row(ost + kOffNormT, nb);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tl->out_empty[o]);
+        if (prev) {
+          uint32_t gw[32];
+          grid_group32(nb, gw, a.amax_floor);
+          grid_group32(nb + 16, gw + 16, a.amax_floor);
+          store_grid(tp, (c * kCl + (int)rank) * kChunk, gw);
+        }
+      }
+    }
   } else if (warp == 11) {
     // ------------------------------------ exchange and gate finish warp --
     // Per block: (1) this CTA's s_x partials to every CTA of the cluster (each
@@ -619,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!real) {  // the normalise-only pass: the norm tiles of a group of chunks per output stage
         if (prev) {
           take_rstd(lb - 1);
-          constexpr int NG = norm_group<QUANT>();
+          constexpr int NG = norm_group<OUT>();
           for (int c0 = 0; c0 < nch; c0 += NG, ++j) {
             const int o = j % kNO;
             wait_local(X, &tl->out_empty[o], ((j / kNO) & 1) ^ 1);
@@ -663,8 +705,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         {  // rows past T arrive as zeros
           wait_local(X, &tl->gates_full, lb & 1);
           const GateTile& gt = tl->gates;
+          if (!IDENT) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) gc[k] = *reinterpret_cast<const float4*>(&gt.comb[lane][4 * k]);
+            for (int k = 0; k < 4; ++k) gc[k] = *reinterpret_cast<const float4*>(&gt.comb[lane][4 * k]);
+          }
           gp = *reinterpret_cast<const float4*>(&gt.pre[lane][0]);
           if (POST) gq = *reinterpret_cast<const float4*>(&gt.post[lane][0]);
           __syncwarp();
@@ -721,12 +765,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             float2 xx = make_float2(0.f, 0.f);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              float2 v = __fmul2_rn(comb2[4 * i], r0);
-              v = __ffma2_rn(comb2[4 * i + 1], r1, v);
-              v = __ffma2_rn(comb2[4 * i + 2], r2, v);
-              v = __ffma2_rn(comb2[4 * i + 3], r3, v);
-              if (POST) v = __ffma2_rn(post2[i], yy, v);
-              const uint32_t w = pack_bf16x2(v.x, v.y);
+              uint32_t w;
+              if (IDENT) {
+                w = (&rin[i].x)[wd];  // R' = R, bit for bit
+              } else {
+                float2 v = __fmul2_rn(comb2[4 * i], r0);
+                v = __ffma2_rn(comb2[4 * i + 1], r1, v);
+                v = __ffma2_rn(comb2[4 * i + 2], r2, v);
+                v = __ffma2_rn(comb2[4 * i + 3], r3, v);
+                if (POST) v = __ffma2_rn(post2[i], yy, v);
+                w = pack_bf16x2(v.x, v.y);
+              }
               ow[i][wd] = w;
               const float2 rr2 = bf16pair(w);
               sR2 = __ffma2_rn(rr2, rr2, sR2);
@@ -823,23 +872,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------- host side --
-template <bool MS, int KCL>
-static void* kptr_(bool post, int out) {
-  if (post)
-    return out == 2 ? (void*)stream_seam_kernel<true, 2, MS, KCL>
-                    : out == 1 ? (void*)stream_seam_kernel<true, 1, MS, KCL> : (void*)stream_seam_kernel<true, 0, MS, KCL>;
-  return out == 2 ? (void*)stream_seam_kernel<false, 2, MS, KCL>
-                  : out == 1 ? (void*)stream_seam_kernel<false, 1, MS, KCL> : (void*)stream_seam_kernel<false, 0, MS, KCL>;
+template <int FORM, bool MS, int KCL>
+static void* kptr_f(int out) {
+  return out == 2 ? (void*)stream_seam_kernel<FORM, 2, MS, KCL>
+                  : out == 1 ? (void*)stream_seam_kernel<FORM, 1, MS, KCL> : (void*)stream_seam_kernel<FORM, 0, MS, KCL>;
 }
-// Clusters of 16 run only the tcgen05 projection (at most 8 chunks per CTA).
-static void* stream_kernel_ptr(bool post, int out, bool ms, int kcl) {
-  if (kcl == 16) return kptr_<false, 16>(post, out);
-  return ms ? kptr_<true, 4>(post, out) : kptr_<false, 4>(post, out);
+template <bool MS, int KCL>
+static void* kptr_(int form, int out) {
+  return form == 2 ? kptr_f<2, MS, KCL>(out) : form == 1 ? kptr_f<1, MS, KCL>(out) : kptr_f<0, MS, KCL>(out);
+}
+// form: 0 no_post, 1 post, 2 identity.  Clusters of 16 run only the tcgen05
+// projection (at most 8 chunks per CTA).
+static void* stream_kernel_ptr(int form, int out, bool ms, int kcl) {
+  if (kcl == 16) return kptr_<false, 16>(form, out);
+  return ms ? kptr_<true, 4>(form, out) : kptr_<false, 4>(form, out);
 }
 static size_t smem_bytes(int kcl) { return kcl == 16 ? Geo<16>::kSmemBytes : Geo<4>::kSmemBytes; }
 
 cudaError_t stream_init() {
-  for (int p = 0; p < 2; ++p)
+  for (int p = 0; p < 3; ++p)        // form
     for (int m = 0; m < 3; ++m)      // out mode
       for (int v = 0; v < 3; ++v) {  // v: 0 tcgen05 / 4, 1 warp MMA / 4, 2 tcgen05 / 16
         const int kcl = v == 2 ? 16 : 4;
@@ -893,11 +944,11 @@ static bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void*
 }
 
 // Clusters that fit at once, per device and kernel variant (queried once).
-static int max_clusters(bool post, int out, bool ms, int kcl) {
-  static int cache[18][64] = {};
+static int max_clusters(int form, int out, bool ms, int kcl) {
+  static int cache[27][64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  const int v = (post ? 1 : 0) + 2 * out + 6 * (kcl == 16 ? 2 : (ms ? 1 : 0));
+  const int v = form + 3 * out + 9 * (kcl == 16 ? 2 : (ms ? 1 : 0));
   if (cache[v][dev] > 0) return cache[v][dev];
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -906,12 +957,12 @@ static int max_clusters(bool post, int out, bool ms, int kcl) {
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3((unsigned)kcl, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(out == 2 ? threads_of<2>() : threads_of<0>(), 1, 1);
   cfg.dynamicSmemBytes = smem_bytes(kcl);
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, stream_kernel_ptr(post, out, ms, kcl), &cfg) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveClusters(&n, stream_kernel_ptr(form, out, ms, kcl), &cfg) != cudaSuccess) return 0;
   cache[v][dev] = n;
   return n;
 }
@@ -958,7 +1009,8 @@ cudaError_t stream_launch(const SeamArgs& a, bool tcgen05_proj, int kcl, cudaStr
   const cuuint32_t bF[3] = {kChunk, 1, kFnRows};
   const cuuint64_t sC[1] = {(cuuint64_t)H};
   bool ok = encode(&mR, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.R, d3, s3, b3, CU_TENSOR_MAP_SWIZZLE_128B) &&
-            encode(&mRo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.res_out, d3, s3, b3, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            encode(&mRo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.res_out ? (const void*)a.res_out : (const void*)a.R, d3, s3,
+                   b3, CU_TENSOR_MAP_SWIZZLE_128B) &&
             encode(&mFn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.fn_packed, dF, s3, bF, CU_TENSOR_MAP_SWIZZLE_128B) &&
             encode(&mN, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.norm, d2, s2, b2, CU_TENSOR_MAP_SWIZZLE_128B);
   if (ok) ok = encode(&mY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.Y ? (const void*)a.Y : (const void*)a.R, d2, s2, b2,
@@ -974,10 +1026,14 @@ cudaError_t stream_launch(const SeamArgs& a, bool tcgen05_proj, int kcl, cudaStr
   CUtensorMap mGc, mGp, mGq;
   const cuuint64_t dG16[2] = {16, T}, sG16[1] = {64}, dG4[2] = {4, T}, sG4[1] = {16};
   const cuuint32_t bG16[2] = {16, kBM}, bG4[2] = {4, kBM};
-  if (ok) ok = encode(&mGc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.comb_prev, dG16, sG16, bG16, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-               encode(&mGp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.pre_prev, dG4, sG4, bG4, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+  if (ok) ok = encode(&mGp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.pre_prev, dG4, sG4, bG4, CU_TENSOR_MAP_SWIZZLE_NONE) &&
                encode(&mGq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.post_prev ? a.post_prev : a.pre_prev, dG4, sG4, bG4,
                       CU_TENSOR_MAP_SWIZZLE_NONE);
+  // the identity form loads no comb: its map slot holds the pre map, never used
+  if (ok && a.comb_prev)
+    ok = encode(&mGc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.comb_prev, dG16, sG16, bG16, CU_TENSOR_MAP_SWIZZLE_NONE);
+  else
+    mGc = mGp;
   if (!ok) return cudaErrorInvalidValue;
   MapSet& c = cache[cache_next];
   cache_next = (cache_next + 1) % 4;
@@ -999,10 +1055,11 @@ static cudaError_t launch_with_maps(const SeamArgs& a, const CUtensorMap* m, boo
 
 static cudaError_t launch_range(const SeamArgs& a, const CUtensorMap* m, bool tcgen05_proj, int kcl, int block0,
                                 int n_blocks, cudaStream_t stream, unsigned long long limit_ns, int* launches) {
-  const bool post = a.Y != nullptr, ms = !tcgen05_proj;
+  const bool ms = !tcgen05_proj;
+  const int form = a.comb_prev == nullptr ? 2 : a.Y != nullptr ? 1 : 0;
   const int mx = a.grid ? 2 : a.codes ? 1 : 0;
-  void* k = stream_kernel_ptr(post, mx, ms, kcl);
-  const int fit = max_clusters(post, mx, ms, kcl);
+  void* k = stream_kernel_ptr(form, mx, ms, kcl);
+  const int fit = max_clusters(form, mx, ms, kcl);
   if (fit <= 0) return cudaErrorInvalidValue;
   const int ncl = n_blocks < fit ? n_blocks : fit;
   cudaLaunchConfig_t cfg = {};
@@ -1012,7 +1069,7 @@ static cudaError_t launch_range(const SeamArgs& a, const CUtensorMap* m, bool tc
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3((unsigned)(ncl * kcl), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(mx == 2 ? threads_of<2>() : threads_of<0>(), 1, 1);
   cfg.dynamicSmemBytes = smem_bytes(kcl);
   cfg.stream = stream;
   cfg.attrs = attr;

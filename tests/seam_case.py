@@ -23,14 +23,17 @@ GATE_TOL = 1e-3
 
 
 def make_case(T: int, H: int, seed: int, post: bool = True, mxfp8: bool = False, craft: bool = False,
-              unique_tokens: int | None = None, grid: bool = False) -> dict:
+              unique_tokens: int | None = None, grid: bool = False, ident: bool = False) -> dict:
+    """One seeded workload; ``ident`` makes it the identity (first-block) form:
+    no Y, no post and no comb, R' = R."""
+    post = post and not ident
     d = I.seam_draws(T, H, seed, post=post, unique_tokens=unique_tokens)
     if craft:
         I.craft_mxfp8(d, seed)
     pre, post_g, comb = O.carried_gates(d["pre_logits"], d["post_logits"], d["comb_logits"])
     d["pre_prev"] = torch.from_numpy(pre)
     d["post_prev"] = torch.from_numpy(post_g) if post else None
-    d["comb_prev"] = torch.from_numpy(comb)
+    d["comb_prev"] = None if ident else torch.from_numpy(comb)
     d["out_mode"] = B.MHC_OUT_FP8_GRID if grid else (B.MHC_OUT_MXFP8 if mxfp8 else B.MHC_OUT_BF16)
     return d
 
@@ -52,6 +55,8 @@ def run_gpu(d: dict, cfg=None, g: dict | None = None, out: dict | None = None, s
         g = to_dev(d)
     if out is None:
         out = B.alloc_outputs(T, H, d["out_mode"], "cuda", cfg)
+        if d["comb_prev"] is None:  # the identity form writes no residual
+            out["residual_out"] = None
     if inplace:
         out["residual_out"] = g["R"]
     B.mhc_seam(g["R"], g["Y"], g["post_prev"], g["comb_prev"], g["pre_prev"], g["fn"],
@@ -97,6 +102,8 @@ def compare(d: dict, h: dict, idx: np.ndarray | None = None, check_quant: bool =
     take = (lambda x: x) if idx is None else (lambda x: x[idx])
     rep = {}
     for k in ("residual_out", "norm"):
+        if k not in h:  # the identity form writes no residual
+            continue
         u = ulp_diff(take(h[k]), o[k])
         rep[k + "_exact"] = float(np.mean(u == 0))
         rep[k + "_within1"] = float(np.mean(u <= 1))

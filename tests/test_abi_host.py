@@ -66,6 +66,17 @@ def test_incomplete_post_is_rejected(L):
     assert _seam(L, Y=None) == -4
     assert _seam(L, post_prev=None) == -4
     assert "post_prev" in L.mhc_last_error_string().decode()
+    assert _seam(L, comb_prev=None) == -4        # Y and post without comb: not the identity form
+    assert "identity form" in L.mhc_last_error_string().decode()
+
+
+def test_identity_form_ignores_residual_out(L):
+    # comb, Y and post all NULL: the identity form; residual_out may be NULL or
+    # anything (it is not written), so the call gets as far as the workspace check
+    ident = dict(comb_prev=None, Y=None, post_prev=None, ws_bytes=1)
+    assert _seam(L, residual_out=None, **ident) == -5
+    assert _seam(L, residual_out=FAKE + 16, **ident) == -5   # would alias R in the other forms
+    assert _seam(L, comb_prev=None, Y=None, post_prev=None, pre_prev=None) == -1
 
 
 def test_null_and_alignment(L):

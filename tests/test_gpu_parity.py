@@ -378,30 +378,46 @@ def test_stream_projection_variants(proj, T, H, mx, post):
 
 
 # ------------------------------------------------------ chained seams (f3) --
-@pytest.mark.parametrize("T,path,post", [(64, 3, True), (1100, 2, True), (40, 1, True), (300, 2, False)])
-def test_three_seams_chained(T, path, post):
+@pytest.mark.parametrize("T,path,post,first", [(64, 3, True, False), (1100, 2, True, False), (40, 1, True, False),
+                                               (300, 2, False, False), (64, 3, True, True), (1100, 2, True, True),
+                                               (40, 1, True, True)])
+def test_three_seams_chained(T, path, post, first):
     """Three seams in a row, each fed the previous seam's residual and gates
     (a fresh sub-layer output Y per seam).  The oracle chain runs on its own
     outputs and the GPU chain on its own; they must agree at every seam (the
     bar is 1 ulp on >= 99.9% of the bf16 elements: a 1-ulp difference in one
-    seam's residual is an input difference to the next)."""
+    seam's residual is an input difference to the next).  With ``first`` the
+    chain opens with the identity (first-block) seam: no Y, no post, no comb,
+    the residual passes through unwritten."""
     H = 5120
     d = make_case(T, H, 8200 + T, post=post)
     g = to_dev(d)
     cfg = B.MhcConfig(path=path)
     o_state = {"R": d["R"], "pre_prev": d["pre_prev"], "post_prev": d["post_prev"], "comb_prev": d["comb_prev"]}
     g_state = {"R": g["R"], "pre_prev": g["pre_prev"], "post_prev": g["post_prev"], "comb_prev": g["comb_prev"]}
+    if first:
+        o_state.update(post_prev=None, comb_prev=None)
+        g_state.update(post_prev=None, comb_prev=None)
     for step in range(3):
-        Y = I.seam_draws(T, H, 8300 + 10 * T + step, post=post)["Y"] if post else None
+        ident = first and step == 0
+        Y = I.seam_draws(T, H, 8300 + 10 * T + step, post=post)["Y"] if post and not ident else None
         o = O.seam(o_state["R"], Y, o_state["post_prev"], o_state["comb_prev"], o_state["pre_prev"], d["fn"],
                    d["bias"], d["alpha"], d["gamma"], d["eps"])
         out = B.alloc_outputs(T, H, B.MHC_OUT_BF16, "cuda", cfg)
+        if ident:  # a sentinel residual_out: the identity form must leave it alone
+            out["residual_out"].fill_(7.0)
         B.mhc_seam(g_state["R"], None if Y is None else Y.to("cuda"), g_state["post_prev"], g_state["comb_prev"],
                    g_state["pre_prev"], g["fn"], g["fn_packed"], g["bias"], g["alpha"], g["gamma"], d["eps"],
                    B.MHC_OUT_BF16, out["residual_out"], out["norm"], None, None, out["pre_out"], out["post_out"],
                    out["comb_out"], out["workspace"], cfg=cfg)
         h = to_host(out)
+        if ident:
+            assert bool((out["residual_out"] == 7.0).all())
+            h.pop("residual_out")
+            assert np.array_equal(o["residual_out"], I.bf16_bits(d["R"]))
         for k in ("residual_out", "norm"):
+            if k not in h:
+                continue
             # from the second seam on the inputs differ by the earlier seams'
             # roundings (and the difference grows along the chain), so a
             # near-cancelling sum may land on either side of zero: an element
@@ -414,11 +430,12 @@ def test_three_seams_chained(T, path, post):
                 assert np.mean(u <= 1) >= 0.9999, (k, float(np.mean(u <= 1)))
         for gk, ok in (("pre_out", "pre"), ("post_out", "post"), ("comb_out", "comb")):
             assert np.abs(h[gk].astype(np.float64) - o[ok].reshape(h[gk].shape)).max() <= GATE_TOL, (step, ok)
-        # the next seam's inputs: each chain feeds itself
+        # the next seam's inputs: each chain feeds itself (after the identity
+        # seam the residual is its input, unchanged)
         o_state = {"R": o["residual_out"], "pre_prev": o["pre"].astype(np.float32),
                    "post_prev": o["post"].astype(np.float32) if post else None,
                    "comb_prev": o["comb"].astype(np.float32)}
-        g_state = {"R": out["residual_out"], "pre_prev": out["pre_out"],
+        g_state = {"R": g_state["R"] if ident else out["residual_out"], "pre_prev": out["pre_out"],
                    "post_prev": out["post_out"] if post else None, "comb_prev": out["comb_out"]}
 
 
@@ -449,3 +466,44 @@ def test_fp8_grid_no_post_and_split_path_refused():
     with pytest.raises(B.MhcError) as e:
         run_gpu(d, cfg=B.MhcConfig(path=1))
     assert e.value.code == -10
+
+
+# ------------------------------------------- identity (first-block) form (f3) --
+@pytest.mark.parametrize("T,H,path,mode", [(64, 5120, 3, B.MHC_OUT_BF16), (5, 5120, 3, B.MHC_OUT_FP8_GRID),
+                                           (1100, 5120, 2, B.MHC_OUT_MXFP8), (300, 5120, 2, B.MHC_OUT_FP8_GRID),
+                                           (2050, 5120, 2, B.MHC_OUT_BF16), (97, 7168, 2, B.MHC_OUT_BF16),
+                                           (40, 5120, 1, B.MHC_OUT_BF16), (33, 160, 1, B.MHC_OUT_MXFP8)])
+def test_identity_form(T, H, path, mode):
+    d = make_case(T, H, 8600 + T + H, ident=True, mxfp8=mode == B.MHC_OUT_MXFP8, grid=mode == B.MHC_OUT_FP8_GRID)
+    cfg = B.MhcConfig(path=path)
+    out = B.alloc_outputs(T, H, d["out_mode"], "cuda", cfg)
+    out["residual_out"].fill_(-3.0)  # must stay untouched
+    sentinel = out["residual_out"]
+    out["residual_out"] = None
+    h = to_host(run_gpu(d, cfg=cfg, out=out))
+    assert bool((sentinel == -3.0).all())
+    compare(d, h, sample_tokens(T, 24, 8600 + T) if T > 512 else None)
+
+
+def test_identity_form_matches_identity_comb_and_rejects_y():
+    # away from signed zeros (none in these draws) the identity form equals the
+    # no_post seam with comb = I on the same inputs
+    T, H = 300, 5120
+    d = make_case(T, H, 8700, ident=True)
+    g = to_dev(d)
+    a = to_host(run_gpu(d, cfg=B.MhcConfig(path=2), g=g))
+    eye = torch.eye(4, dtype=torch.float32).expand(T, 4, 4).contiguous()
+    d2 = dict(d, comb_prev=eye)
+    g2 = dict(g, comb_prev=eye.cuda())
+    b = to_host(run_gpu(d2, cfg=B.MhcConfig(path=2), g=g2))
+    assert np.array_equal(b["residual_out"], I.bf16_bits(d["R"]))
+    assert np.array_equal(a["norm"], b["norm"])
+    for k in ("pre_out", "post_out", "comb_out"):
+        assert np.array_equal(a[k], b[k]), k
+    out = B.alloc_outputs(T, H, B.MHC_OUT_BF16, "cuda")
+    Y = torch.zeros(T, H, dtype=torch.bfloat16, device="cuda")
+    post = torch.ones(T, 4, device="cuda")
+    with pytest.raises(RuntimeError, match="identity form"):
+        B.mhc_seam(g["R"], Y, post, None, g["pre_prev"], g["fn"], g["fn_packed"], g["bias"], g["alpha"],
+                   g["gamma"], d["eps"], B.MHC_OUT_BF16, out["residual_out"], out["norm"], None, None,
+                   out["pre_out"], out["post_out"], out["comb_out"], out["workspace"])
