@@ -65,6 +65,8 @@ def bind(cdll):
     L.mhc_oracle_sigmoid.argtypes = [C.c_double]
     L.mhc_oracle_seam.restype = C.c_int
     L.mhc_oracle_seam.argtypes = [C.c_int64, C.c_int] + [P] * 9 + [C.c_double, C.c_int, C.c_int] + [P] * 7
+    L.mhc_oracle_seam_unshifted.restype = C.c_int
+    L.mhc_oracle_seam_unshifted.argtypes = [C.c_int64, C.c_int] + [P] * 7 + [C.c_double, C.c_int] + [P] * 5
     return L
 
 
@@ -193,4 +195,31 @@ def seam(R, Y, post_prev, comb_prev, pre_prev, fn, bias, alpha, gamma, eps: floa
         raise ValueError("oracle rejected the inputs (NULL operand, half-present post inputs, or Y without comb)")
     if want_x:
         out["x"] = x
+    return out
+
+
+def seam_unshifted(R, Y, post_prev, comb_prev, fn, bias, alpha, eps: float, sinkhorn_iters: int = 20) -> dict:
+    """The unshifted ordering: post-mix with the carried comb and post, gates
+    from R', and the layer input x = sum_i pre[i] R'[i] with the fresh pre,
+    bf16 with no norm.  Returns ``residual_out`` [T,4,H] and ``x`` [T,H] as
+    uint16 bits and ``pre``, ``post`` [T,4], ``comb`` [T,4,4] in float64."""
+    Rb = _u16(R)
+    T, n, H = Rb.shape
+    assert n == 4
+    Yb = None if Y is None else _u16(Y)
+    post_a, comb_a = _f32(post_prev), _f32(comb_prev)
+    fn_a, bias_a, alpha_a = _f32(fn), _f32(bias), _f32(alpha)
+    out = {
+        "residual_out": np.zeros((T, 4, H), np.uint16),
+        "x": np.zeros((T, H), np.uint16),
+        "pre": np.zeros((T, 4)),
+        "post": np.zeros((T, 4)),
+        "comb": np.zeros((T, 4, 4)),
+    }
+    rc = lib().mhc_oracle_seam_unshifted(T, H, _ptr(Rb), _ptr(Yb), _ptr(post_a), _ptr(comb_a), _ptr(fn_a),
+                                         _ptr(bias_a), _ptr(alpha_a), float(eps), int(sinkhorn_iters),
+                                         _ptr(out["residual_out"]), _ptr(out["x"]), _ptr(out["pre"]),
+                                         _ptr(out["post"]), _ptr(out["comb"]))
+    if rc != 0:
+        raise ValueError("oracle rejected the inputs (NULL operand, half-present post inputs, or Y without comb)")
     return out

@@ -30,7 +30,10 @@
  * unrounded one) feeds the sums, the projection and x; x is not rounded before
  * the norm; ue8m0 exponent = smallest e with amax <= 448 * 2^e, amax floored
  * at amax_floor (1e-10 by default), clamped to [-127, 127]; e4m3fn codes by
- * round-to-nearest-even, saturating at +-448, sign of zero kept.
+ * round-to-nearest-even, saturating at +-448, sign of zero kept; the
+ * fp8_grid value is bf16(e4m3 value * 2^e); the identity (first-block) form,
+ * with no comb, Y or post, keeps R' = R; the unshifted ordering forms x with
+ * the fresh pre and has no norm.
  *
  * Parity pins: every function here is checked by the CPU test-suite against
  * closed forms, invariants, an exhaustive quantiser sweep and a
@@ -313,4 +316,50 @@ int mhc_oracle_seam(int64_t T, int H,
     free(rp);
     free(x);
     return 0;
+}
+
+/* ------------------------------------------------------ unshifted seam ---- */
+
+/* The unshifted ordering ("[FlyDSL] Single-launch Mega-mHC on gfx950", the
+ * table of seam implementations: the HIP mhc_fused_post_pre kernel uses the
+ * unshifted ordering and has no RMSNorm).  Read as: the same post-mix with the
+ * carried comb and post, the same gates from R', and then the layer input
+ * x[h] = sum_i pre[i] R'[i][h] with the FRESH pre just computed (not the
+ * carried one), stored as bf16 with no norm.  The steps up to the gates are
+ * those of mhc_oracle_seam (called here with a zero carried pre and a unit
+ * gamma, whose norm is discarded).
+ *
+ * Layouts as in mhc_oracle_seam; x_out [T,H] bf16 bits.  comb_prev NULL (with
+ * Y and post_prev NULL) is the identity form, R' = R.  Returns 0, or -1 as
+ * mhc_oracle_seam does or when memory runs out. */
+int mhc_oracle_seam_unshifted(int64_t T, int H,
+                              const uint16_t* R, const uint16_t* Y,
+                              const float* post_prev, const float* comb_prev,
+                              const float* fn, const float* bias, const float* alpha,
+                              double eps, int sinkhorn_iters,
+                              uint16_t* residual_out, uint16_t* x_out,
+                              double* pre_out, double* post_out, double* comb_out) {
+    if (!x_out || T < 0 || H <= 0) return -1;
+    float* pre0 = (float*)calloc((size_t)(T > 0 ? T : 1) * 4, sizeof(float));
+    uint16_t* gam1 = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)H);
+    uint16_t* norm = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(T > 0 ? T : 1) * (size_t)H);
+    if (!pre0 || !gam1 || !norm) { free(pre0); free(gam1); free(norm); return -1; }
+    for (int h = 0; h < H; ++h) gam1[h] = 0x3F80;  /* 1.0 */
+    int rc = mhc_oracle_seam(T, H, R, Y, post_prev, comb_prev, pre0, fn, bias, alpha, gam1, eps,
+                             sinkhorn_iters, 0, residual_out, norm, pre_out, post_out, comb_out, NULL, NULL);
+    if (rc == 0) {
+        const int K = N_HC * H;
+        for (int64_t t = 0; t < T; ++t) {
+            for (int h = 0; h < H; ++h) {
+                double v = 0.0;
+                for (int i = 0; i < N_HC; ++i)
+                    v += pre_out[t * 4 + i] * mhc_oracle_bf16_to_double(residual_out[t * K + i * H + h]);
+                x_out[t * H + h] = mhc_oracle_bf16_rne(v);
+            }
+        }
+    }
+    free(pre0);
+    free(gam1);
+    free(norm);
+    return rc;
 }

@@ -33,9 +33,14 @@ MUTATIONS = {
                               "mhc_oracle_bf16_rne(ldexp(mhc_oracle_e4m3_decode(code), e + 1))"),
     "e4m3_decode_bias_8": ("ldexp(1.0 + f / 8.0, E - 7)", "ldexp(1.0 + f / 8.0, E - 8)"),
     "identity_form_stream_shifted": ("const uint16_t b = Rt[i * H + h];", "const uint16_t b = Rt[((i + 1) % N_HC) * H + h];"),
+    "unshifted_pre_index_shifted": ("v += pre_out[t * 4 + i] * mhc_oracle_bf16_to_double(residual_out[t * K + i * H + h]);",
+                                    "v += pre_out[t * 4 + (i + 1) % N_HC] * mhc_oracle_bf16_to_double(residual_out[t * K + i * H + h]);"),
+    "unshifted_x_scaled": ("x_out[t * H + h] = mhc_oracle_bf16_rne(v);", "x_out[t * H + h] = mhc_oracle_bf16_rne(v * 1.0009765625);"),
 }
 
 PINS = [
+    P.test_unshifted_zero_fn_gives_half_sum_of_streams,
+    lambda o: P.test_brute_force_T1_H8_unshifted(o, 37, True),
     P.test_identity_form_keeps_signed_zeros_and_subnormals,
     P.test_e4m3_decode_matches_format_definition,
     P.test_grid_exact_on_the_e4m3_lattice,

@@ -410,10 +410,12 @@ def test_rounded_vs_unrounded_rprime_reading_is_small(oracle):
 
 
 # ------------------------------------------------- high-precision brute force
-def _brute_force_seam(d, t=0):
+def _brute_force_seam(d, t=0, unshifted=False):
     """The seam at one token in exact rationals (sums, products, roundings) and
     60-digit decimals (sqrt, exp, Sinkhorn divisions), straight from the
-    definition; independent of the oracle's code."""
+    definition; independent of the oracle's code.  With ``unshifted`` it also
+    returns the unshifted layer input bf16(sum_i pre[i] R'[i]) with the fresh
+    pre, no norm."""
     getcontext().prec = 60
     H = d["H"]
     Rv = d["R"].to(torch.float64).numpy()[t]
@@ -464,7 +466,15 @@ def _brute_force_seam(d, t=0):
     for h in range(H):
         y = D(x[h]) * rstdx * D(Fraction(gam[h]))
         norm[h] = bf16_rne_exact(Fraction(y))
-    return res, norm, np.array([float(v) for v in g_pre]), np.array([float(v) for v in g_post]), np.array([[float(v) for v in r] for r in M])
+    out = (res, norm, np.array([float(v) for v in g_pre]), np.array([float(v) for v in g_post]),
+           np.array([[float(v) for v in r] for r in M]))
+    if unshifted:
+        xu = np.zeros(H, np.uint16)
+        for h in range(H):
+            v = sum(g_pre[i] * D(rp[i][h]) for i in range(4))
+            xu[h] = bf16_rne_exact(Fraction(v))
+        out = out + (xu,)
+    return out
 
 
 @pytest.mark.parametrize("seed", [31, 32, 33])
@@ -514,6 +524,51 @@ def test_identity_form_keeps_signed_zeros_and_subnormals(oracle):
     assert not np.array_equal(eye["residual_out"], bits)  # the -0 entries differ
     # away from the signed zeros the two forms agree
     assert np.array_equal(ident["norm"][1], eye["norm"][1])
+
+
+# ------------------------------------------------------ unshifted seam ----
+def run_unshifted(oracle, d):
+    return oracle.seam_unshifted(d["R"], d["Y"], d["post_prev"], d["comb_prev"], d["fn"], d["bias"], d["alpha"],
+                                 d["eps"])
+
+
+@pytest.mark.parametrize("seed,post", [(37, True), (38, False)])
+def test_brute_force_T1_H8_unshifted(oracle, seed, post):
+    d = seam_inputs(1, 8, seed, post=post, oracle=oracle)
+    d["comb_prev"] = np.array([[[0.9, 0.05, 0.3, -0.2], [0.1, 0.7, 0.0, 0.4], [-0.3, 0.2, 1.1, 0.05], [0.25, -0.1, 0.15, 0.6]]], np.float32)
+    d["bias"] = torch.linspace(-0.7, 0.3, 24)
+    d["alpha"] = torch.tensor([1.2, 0.9, 0.7])
+    o = run_unshifted(oracle, d)
+    res, _, g_pre, g_post, comb, xu = _brute_force_seam(d, unshifted=True)
+    assert np.array_equal(o["residual_out"][0], res)
+    assert np.array_equal(o["x"][0], xu)
+    assert np.allclose(o["pre"][0], g_pre, atol=1e-13, rtol=0)
+    assert np.allclose(o["post"][0], g_post, atol=1e-13, rtol=0)
+    assert np.allclose(o["comb"][0], comb, atol=1e-13, rtol=0)
+
+
+def test_unshifted_zero_fn_gives_half_sum_of_streams(oracle):
+    # zero fn and bias: every logit is 0, so the fresh pre is sigma(0) = 1/2 and
+    # x = bf16(sum_i R'[i] / 2) exactly (the carried pre of the draws is not 1/2)
+    d = seam_inputs(3, 64, 42, oracle=oracle)
+    d["fn"] = torch.zeros_like(d["fn"])
+    d["bias"] = torch.zeros(24)
+    o = run_unshifted(oracle, d)
+    assert np.all(o["pre"] == 0.5) and np.all(o["post"] == 1.0) and np.allclose(o["comb"], 0.25, atol=1e-15)
+    rp = o["residual_out"]
+    for t in range(3):
+        for h in range(64):
+            v = Fraction(1, 2) * sum(Fraction(bf16_val(rp[t, i, h])) for i in range(4))
+            assert o["x"][t, h] == bf16_rne_exact(v), (t, h)
+
+
+def test_unshifted_shares_the_delayed_seams_residual_and_gates(oracle):
+    d = seam_inputs(4, 128, 43, oracle=oracle)
+    a = run_unshifted(oracle, d)
+    b = run(oracle, d)
+    assert np.array_equal(a["residual_out"], b["residual_out"])
+    for k in ("pre", "post", "comb"):
+        assert np.array_equal(a[k], b[k]), k
 
 
 def test_oracle_rejects_y_without_comb(oracle):
