@@ -47,8 +47,13 @@ WORKLOADS = {
     "seam_T4160_H5120_post_bf16": dict(T=4160, H=5120, post=True, out="bf16", seed=1003),
     "seam_T1024_H5120_post_mxfp8": dict(T=1024, H=5120, post=True, out="mxfp8", seed=1002),
     "seam_T16384_H5120_post_fp8grid": dict(T=16384, H=5120, post=True, out="fp8_grid", seed=1004),
+    "seam_T4160_H5120_post_fp8grid": dict(T=4160, H=5120, post=True, out="fp8_grid", seed=1003),
     # the identity (first-block) form: no Y, no post, no comb; R' = R is not written
     "seam_T16384_H5120_first_bf16": dict(T=16384, H=5120, post=False, out="bf16", seed=1004, ident=True),
+    "seam_T4160_H5120_first_bf16": dict(T=4160, H=5120, post=False, out="bf16", seed=1003, ident=True),
+    # the unshifted ordering: x with the fresh pre, no norm (split path)
+    **{f"seam_T{t}_H5120_post_unshifted": dict(T=t, H=5120, post=True, out="bf16", seed=1004, unshifted=True)
+       for t in (32, 2048, 16384)},
     "seam_T64_H5120_post_bf16": dict(T=64, H=5120, post=True, out="bf16", seed=1001),
     "seam_T64_H5120_nopost_bf16": dict(T=64, H=5120, post=False, out="bf16", seed=1001),
     "seam_T4_H5120_post_bf16": dict(T=4, H=5120, post=True, out="bf16", seed=1000),
@@ -169,15 +174,25 @@ def run_ours(args, w: dict, rank: int, world: int, local_rank: int) -> dict | No
 
     cfg = B.MhcConfig(projection={"auto": 0, "mma": 1, "tcgen05": 2}[args.projection],
                       path={"auto": 0, "split": 1, "stream": 2, "stream16": 3}[args.path])
-    out = B.alloc_outputs(T, H, mode, device, cfg)
+    unsh = bool(w.get("unshifted"))
+    out = B.alloc_outputs(T, H, mode, device, cfg, unshifted=unsh)
     if w.get("ident"):  # the identity form writes no residual
         out["residual_out"] = None
 
+    def seam_call(gi: dict, o: dict, ws, s):
+        """One call through the C ABI on inputs gi and outputs o."""
+        if unsh:
+            B.mhc_seam_unshifted(gi["R"], gi["Y"], gi["post_prev"], gi["comb_prev"], g["fn"], g["fn_packed"], g["bias"],
+                                 g["alpha"], wl["eps"], o["residual_out"], o["norm"], o["pre_out"], o["post_out"],
+                                 o["comb_out"], ws, cfg=cfg, stream=s)
+        else:
+            B.mhc_seam(gi["R"], gi["Y"], gi["post_prev"], gi["comb_prev"], gi["pre_prev"], g["fn"], g["fn_packed"],
+                       g["bias"], g["alpha"], g["gamma"], wl["eps"], mode, o["residual_out"], o["norm"],
+                       o["fp8_codes"], o["e8m0_scales"], o["pre_out"], o["post_out"], o["comb_out"], ws, cfg=cfg,
+                       stream=s)
+
     def step():
-        B.mhc_seam(g["R"], g["Y"], g["post_prev"], g["comb_prev"], g["pre_prev"], g["fn"], g["fn_packed"], g["bias"],
-                   g["alpha"], g["gamma"], wl["eps"], mode, out["residual_out"], out["norm"], out["fp8_codes"],
-                   out["e8m0_scales"], out["pre_out"], out["post_out"], out["comb_out"], out["workspace"],
-                   cfg=cfg, stream=stream)
+        seam_call(g, out, out["workspace"], stream)
 
     for _ in range(args.warmup):
         step()
@@ -193,10 +208,7 @@ def run_ours(args, w: dict, rank: int, world: int, local_rank: int) -> dict | No
         with torch.cuda.stream(gstream):
             with torch.cuda.graph(graph, stream=gstream):
                 for _ in range(per_graph):
-                    B.mhc_seam(g["R"], g["Y"], g["post_prev"], g["comb_prev"], g["pre_prev"], g["fn"], g["fn_packed"],
-                               g["bias"], g["alpha"], g["gamma"], wl["eps"], mode, out["residual_out"], out["norm"],
-                               out["fp8_codes"], out["e8m0_scales"], out["pre_out"], out["post_out"], out["comb_out"],
-                               out["workspace"], cfg=cfg, stream=gstream)
+                    seam_call(g, out, out["workspace"], gstream)
         for _ in range(args.warmup):
             graph.replay()
         torch.cuda.synchronize(device)
@@ -237,7 +249,8 @@ def run_ours(args, w: dict, rank: int, world: int, local_rank: int) -> dict | No
         n_split = 8 if T >= 2048 else (4 if T >= 512 else 1)
         bounds = [(T * i // n_split, T * (i + 1) // n_split) for i in range(n_split)]
         streams = [torch.cuda.Stream(device) for _ in range(min(2, n_split))]
-        spaces = [B.alloc_outputs(max(t1 - t0 for t0, t1 in bounds), H, mode, device, cfg)["workspace"] for _ in streams]
+        spaces = [B.alloc_outputs(max(t1 - t0 for t0, t1 in bounds), H, mode, device, cfg, unshifted=unsh)["workspace"]
+                  for _ in streams]
 
         def e2e_step():
             start = torch.cuda.Event()
@@ -252,13 +265,9 @@ def run_ours(args, w: dict, rank: int, world: int, local_rank: int) -> dict | No
                         if v is not None:
                             g[k][t0:t1].copy_(v[t0:t1], non_blocking=True)
                     sl = {k: (None if v is None else v[t0:t1]) for k, v in out.items() if k != "workspace"}
-                    B.mhc_seam(g["R"][t0:t1], None if g["Y"] is None else g["Y"][t0:t1],
-                               None if g["post_prev"] is None else g["post_prev"][t0:t1],
-                               None if g["comb_prev"] is None else g["comb_prev"][t0:t1],
-                               g["pre_prev"][t0:t1], g["fn"], g["fn_packed"], g["bias"], g["alpha"], g["gamma"],
-                               wl["eps"], mode, sl["residual_out"], sl["norm"], sl["fp8_codes"], sl["e8m0_scales"],
-                               sl["pre_out"], sl["post_out"], sl["comb_out"], spaces[i % len(streams)], cfg=cfg,
-                               stream=s)
+                    gi = {k: (None if g[k] is None else g[k][t0:t1]) for k in ("R", "Y", "post_prev", "comb_prev",
+                                                                             "pre_prev")}
+                    seam_call(gi, sl, spaces[i % len(streams)], s)
                     for k in outs:
                         pout[k][t0:t1].copy_(out[k][t0:t1], non_blocking=True)
             for s in streams:
@@ -302,6 +311,11 @@ def cpu_baseline(w: dict, wl: dict | None, budget_s: float = 15.0, steps: int = 
     times = []
     for _ in range(steps):
         t0 = time.perf_counter()
+        if w.get("unshifted"):
+            O.seam_unshifted(d["R"][:n], d["Y"][:n] if w["post"] else None, post[:n] if w["post"] else None,
+                             None if comb is None else comb[:n], d["fn"], d["bias"], d["alpha"], d["eps"])
+            times.append(time.perf_counter() - t0)
+            continue
         o = O.seam(d["R"][:n], d["Y"][:n] if w["post"] else None, post[:n] if w["post"] else None,
                    None if comb is None else comb[:n],
                    pre[:n], d["fn"], d["bias"], d["alpha"], d["gamma"], d["eps"])
@@ -363,6 +377,7 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     config = {"workload": args.workload, "T": w["T"], "H": w["H"], "n_hc": 4,
               "form": "identity" if w.get("ident") else ("post" if w["post"] else "no_post"), "out": w["out"],
+              "ordering": "unshifted" if w.get("unshifted") else "delayed",
               "tokens_per_rank": w["T"], "parallelism": f"token-shard x{args.gpus} (independent)",
               "projection": args.projection, "path": args.path,
               "timing": (f"cuda-graph replay ({GRAPH_CALLS} calls per graph)" if args.graph

@@ -106,6 +106,10 @@ typedef struct {
  * call (T' <= T, same H and cfg) may follow any other. */
 size_t mhc_workspace_bytes(int64_t T, int H, const mhc_config* cfg);
 
+/* The same for mhc_seam_unshifted() (the split path needs more shared memory
+ * there, so a cfg may be refused by one and not the other). */
+size_t mhc_workspace_bytes_unshifted(int64_t T, int H, const mhc_config* cfg);
+
 /* Zero a workspace on `stream` (async).  Returns MHC_ERR_WORKSPACE when
  * `ws` is NULL or `bytes` is smaller than the status word. */
 int mhc_workspace_init(void* ws, size_t bytes, void* stream);
@@ -163,6 +167,31 @@ int mhc_seam(const void* R, const void* Y, const float* post_prev, const float* 
              mhc_out_mode out_mode, void* residual_out, void* norm, uint8_t* fp8_codes,
              uint8_t* e8m0_scales, float* pre_out, float* post_out, float* comb_out,
              void* workspace, size_t ws_bytes, const mhc_config* cfg, void* stream);
+
+/* The unshifted ordering of the seam ("[FlyDSL] Single-launch Mega-mHC on
+ * gfx950", the table of seam implementations: the HIP mhc_fused_post_pre
+ * kernel uses the unshifted ordering and has no RMSNorm).  The post-mix and the
+ * gates are those of mhc_seam(); the layer input then uses the FRESH pre just
+ * computed instead of a carried one, and is not normalised:
+ *   x[t,h] = bf16( sum_i pre[t,i] R'[t,i,h] ),  pre = sigmoid(l[0:4]) of this call
+ * Arguments as in mhc_seam(), without pre_prev, gamma, out_mode and the
+ * quantised outputs:
+ *   x_out      [T,H] bf16, 16-byte aligned (the layer input)
+ *   pre_out    the fresh pre used for x; post_out and comb_out are the gates
+ *              of the next seam's post-mix
+ *   workspace  mhc_workspace_bytes_unshifted(T, H, cfg) bytes
+ * comb_prev NULL (with Y and post_prev NULL) is the identity form.  The path
+ * policy is mhc_seam()'s.  On the streaming paths (2, 3) the call is two
+ * launches: the seam kernel writes R' and the gates, then a second kernel reads
+ * R' back and forms x (8 H more bytes per token than the ordering needs).  On
+ * the split path each CTA keeps its R' in shared memory and x is formed in the
+ * same launch; a cfg->block_m * cfg->cols_per_cta whose R' tile (8 bytes per
+ * element) does not fit is refused (MHC_ERR_CONFIG).  Errors as in
+ * mhc_seam(). */
+int mhc_seam_unshifted(const void* R, const void* Y, const float* post_prev, const float* comb_prev,
+                       const float* fn, const void* fn_packed, const float* bias, const float* alpha, float eps,
+                       int64_t T, int H, void* residual_out, void* x_out, float* pre_out, float* post_out,
+                       float* comb_out, void* workspace, size_t ws_bytes, const mhc_config* cfg, void* stream);
 
 /* Standalone per-32 ue8m0 quantiser of bf16 rows x [rows,H] (the same rule as
  * the seam's mxfp8 output; used to test the quantiser on crafted groups).

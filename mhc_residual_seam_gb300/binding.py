@@ -50,6 +50,8 @@ def lib():
         P, I64, I = C.c_void_p, C.c_int64, C.c_int
         L.mhc_workspace_bytes.restype = C.c_size_t
         L.mhc_workspace_bytes.argtypes = [I64, I, P]
+        L.mhc_workspace_bytes_unshifted.restype = C.c_size_t
+        L.mhc_workspace_bytes_unshifted.argtypes = [I64, I, P]
         L.mhc_workspace_init.restype = I
         L.mhc_workspace_init.argtypes = [P, C.c_size_t, P]
         L.mhc_check_status.restype = I
@@ -60,6 +62,8 @@ def lib():
         L.mhc_pack_fn.argtypes = [P, P, I, P]
         L.mhc_seam.restype = I
         L.mhc_seam.argtypes = [P] * 10 + [C.c_float, I64, I, I] + [P] * 7 + [P, C.c_size_t, P, P]
+        L.mhc_seam_unshifted.restype = I
+        L.mhc_seam_unshifted.argtypes = [P] * 8 + [C.c_float, I64, I] + [P] * 6 + [C.c_size_t, P, P]
         L.mhc_seam_noalloc.restype = I
         L.mhc_seam_noalloc.argtypes = [P] * 9 + [C.c_float, I64, I, I] + [P] * 7 + [P, P]
         L.mhc_quant_ue8m0.restype = I
@@ -148,6 +152,27 @@ def mhc_seam(R, Y, post_prev, comb_prev, pre_prev, fn, fn_packed, bias, alpha, g
                           _stream(stream)))
 
 
+def mhc_seam_unshifted(R, Y, post_prev, comb_prev, fn, fn_packed, bias, alpha, eps: float, residual_out, x_out,
+                       pre_out, post_out, comb_out, workspace, cfg=None, stream=None, T: int | None = None,
+                       H: int | None = None) -> None:
+    """One seam call in the unshifted ordering (x with the fresh pre, no norm);
+    T and H default to R's shape [T, 4, H]."""
+    if T is None:
+        T = R.shape[0]
+    if H is None:
+        H = R.shape[-1]
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().mhc_seam_unshifted(_ptr(R), _ptr(Y), _ptr(post_prev), _ptr(comb_prev), _ptr(fn), _ptr(fn_packed),
+                                    _ptr(bias),
+                                    _ptr(alpha), float(eps), int(T), int(H), _ptr(residual_out), _ptr(x_out),
+                                    _ptr(pre_out), _ptr(post_out), _ptr(comb_out), _ptr(workspace), ws_bytes,
+                                    _cfg(cfg), _stream(stream)))
+
+
+def mhc_workspace_bytes_unshifted(T: int, H: int, cfg=None) -> int:
+    return int(lib().mhc_workspace_bytes_unshifted(int(T), int(H), _cfg(cfg)))
+
+
 def mhc_seam_noalloc(R, Y, post_prev, comb_prev, pre_prev, fn, bias, alpha, gamma, eps: float, out_mode: int,
                      residual_out, norm, fp8_codes, e8m0_scales, pre_out, post_out, comb_out, cfg=None,
                      stream=None, T: int | None = None, H: int | None = None) -> None:
@@ -183,8 +208,9 @@ def mhc_last_error_string() -> str:
 
 
 # ----------------------------------------------------------- allocation ----
-def alloc_outputs(T: int, H: int, out_mode: int, device, cfg=None) -> dict:
-    """Output tensors and an initialised workspace for one seam call."""
+def alloc_outputs(T: int, H: int, out_mode: int, device, cfg=None, unshifted: bool = False) -> dict:
+    """Output tensors and an initialised workspace for one seam call (with
+    ``unshifted``, for mhc_seam_unshifted: ``norm`` then receives x)."""
     import torch
     o = {
         "residual_out": torch.empty((T, 4, H), dtype=torch.bfloat16, device=device),
@@ -198,7 +224,7 @@ def alloc_outputs(T: int, H: int, out_mode: int, device, cfg=None) -> dict:
         "post_out": torch.empty((T, 4), dtype=torch.float32, device=device),
         "comb_out": torch.empty((T, 4, 4), dtype=torch.float32, device=device),
     }
-    nbytes = mhc_workspace_bytes(T, H, cfg)
+    nbytes = mhc_workspace_bytes_unshifted(T, H, cfg) if unshifted else mhc_workspace_bytes(T, H, cfg)
     o["workspace"] = torch.empty((nbytes + 15) // 16 * 16, dtype=torch.uint8, device=device)
     mhc_workspace_init(o["workspace"])
     return o

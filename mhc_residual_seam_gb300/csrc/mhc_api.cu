@@ -11,9 +11,9 @@ namespace mhc {
 // mhc_split.cu
 using SplitKernel = void (*)(SeamArgs, int, int, int64_t, char*, size_t);
 size_t split_slot_bytes(int Gh, int BT);
-size_t split_smem_bytes(int BT, int Wd);
+size_t split_smem_bytes(int BT, int Wd, bool unshifted);
 cudaError_t split_init(size_t max_smem);
-cudaError_t split_capacity(bool post, bool mxfp8, int BT, int Wd, int num_sms, int* ctas);
+cudaError_t split_capacity(bool post, int mode, int BT, int Wd, int num_sms, int* ctas);
 cudaError_t split_launch(const SeamArgs& a, int BT, int Wd, int64_t groups_per_launch, char* slots,
                          cudaStream_t stream, int* launches);
 // mhc_stream.cu
@@ -27,6 +27,8 @@ cudaError_t pack_fn_launch(const float* fn, void* out, int H, cudaStream_t s);
 cudaError_t quant_launch(const void* x, int64_t rows, int H, float floor_, uint8_t* codes, uint8_t* scales,
                          cudaStream_t s);
 cudaError_t copy_launch(const void* src, void* dst, size_t bytes, int num_sms, cudaStream_t s);
+cudaError_t unshifted_x_launch(const void* rp, const float* pre, int64_t T, int H, void* x, int num_sms,
+                               cudaStream_t s);
 }  // namespace mhc
 
 namespace {
@@ -99,10 +101,13 @@ int next_pow2(int64_t v) {
   return p;
 }
 
-// Launch policy: a pure function of (T, H, cfg, whether fn_packed is given).
-// Workspace sizing asks with have_packed = false, so a workspace sized for the
-// automatic policy also fits the split path it falls back to without fn_packed.
-int make_plan(int64_t T, int H, const mhc_config* cfg, bool have_packed, Plan* p) {
+// Launch policy: a pure function of (T, H, cfg, whether fn_packed is given,
+// the ordering).  Workspace sizing asks with have_packed = false, so a
+// workspace sized for the automatic policy also fits the split path it falls
+// back to without fn_packed.  The unshifted ordering takes the same paths (on
+// the streaming path as two launches) but needs twice the split path's shared
+// memory per CTA.
+int make_plan(int64_t T, int H, const mhc_config* cfg, bool have_packed, Plan* p, bool unshifted = false) {
   mhc_config c = {};
   if (cfg) c = *cfg;
   if (c.path < 0 || c.path > 3) return fail(MHC_ERR_CONFIG, "cfg.path must be 0, 1, 2 or 3");
@@ -151,7 +156,7 @@ int make_plan(int64_t T, int H, const mhc_config* cfg, bool have_packed, Plan* p
   if (c.cols_per_cta) p->Wd = c.cols_per_cta;
   const int Hr = (H + 31) / 32 * 32;
   if (p->Wd > Hr) p->Wd = Hr;
-  if (mhc::split_smem_bytes(p->BT, p->Wd) > kSplitMaxSmem)
+  if (mhc::split_smem_bytes(p->BT, p->Wd, unshifted) > kSplitMaxSmem)
     return fail(MHC_ERR_CONFIG, "block_m * cols_per_cta too large: x of one CTA does not fit in shared memory");
   return MHC_OK;
 }
@@ -179,6 +184,12 @@ extern "C" {
 size_t mhc_workspace_bytes(int64_t T, int H, const mhc_config* cfg) {
   Plan p;
   if (T < 0 || H <= 0 || make_plan(T, H, cfg, false, &p) != MHC_OK) return kHeaderBytes;
+  return plan_workspace(T, H, p);
+}
+
+size_t mhc_workspace_bytes_unshifted(int64_t T, int H, const mhc_config* cfg) {
+  Plan p;
+  if (T < 0 || H <= 0 || make_plan(T, H, cfg, false, &p, true) != MHC_OK) return kHeaderBytes;
   return plan_workspace(T, H, p);
 }
 
@@ -211,11 +222,14 @@ int mhc_pack_fn(const float* fn, void* fn_packed, int H, void* stream) {
   return e == cudaSuccess ? MHC_OK : cuda_fail(e, "pack_fn launch");
 }
 
-int mhc_seam(const void* R, const void* Y, const float* post_prev, const float* comb_prev, const float* pre_prev,
-             const float* fn, const void* fn_packed, const float* bias, const float* alpha, const void* gamma,
-             float eps, int64_t T, int H, mhc_out_mode out_mode, void* residual_out, void* norm, uint8_t* fp8_codes,
-             uint8_t* e8m0_scales, float* pre_out, float* post_out, float* comb_out, void* workspace,
-             size_t ws_bytes, const mhc_config* cfg, void* stream) {
+// Both orderings: `unsh` selects the unshifted one (then pre_prev and gamma
+// are NULL, out_mode is bf16, and `norm` receives x).
+static int seam_impl(bool unsh, const void* R, const void* Y, const float* post_prev, const float* comb_prev,
+                     const float* pre_prev, const float* fn, const void* fn_packed, const float* bias,
+                     const float* alpha, const void* gamma, float eps, int64_t T, int H, mhc_out_mode out_mode,
+                     void* residual_out, void* norm, uint8_t* fp8_codes, uint8_t* e8m0_scales, float* pre_out,
+                     float* post_out, float* comb_out, void* workspace, size_t ws_bytes, const mhc_config* cfg,
+                     void* stream) {
   g_launches = 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (out_mode != MHC_OUT_BF16 && out_mode != MHC_OUT_MXFP8 && out_mode != MHC_OUT_FP8_GRID)
@@ -225,7 +239,7 @@ int mhc_seam(const void* R, const void* Y, const float* post_prev, const float* 
   if ((mx || gridm) && H % 32 != 0) return fail(MHC_ERR_SHAPE, "mxfp8 and fp8_grid outputs need H % 32 == 0");
   if (!(eps >= 0.f) || eps > 1e30f) return fail(MHC_ERR_CONFIG, "eps must be finite and >= 0");
   Plan plan;
-  int rc = make_plan(T, H, cfg, fn_packed != nullptr, &plan);
+  int rc = make_plan(T, H, cfg, fn_packed != nullptr, &plan, unsh);
   if (rc != MHC_OK) return rc;
   if (T == 0) return MHC_OK;
   if ((Y == nullptr) != (post_prev == nullptr))
@@ -235,8 +249,8 @@ int mhc_seam(const void* R, const void* Y, const float* post_prev, const float* 
   const bool ident = comb_prev == nullptr;
   if (ident && Y) return fail(MHC_ERR_INCOMPLETE_POST, "the identity form (comb_prev NULL) takes no Y and no post_prev");
   if (ident) residual_out = nullptr;
-  if (!R || !pre_prev || !fn || !bias || !alpha || !gamma || (!ident && !residual_out) || !norm || !pre_out ||
-      !post_out || !comb_out)
+  if (!R || (!unsh && (!pre_prev || !gamma)) || !fn || !bias || !alpha || (!ident && !residual_out) || !norm ||
+      !pre_out || !post_out || !comb_out)
     return fail(MHC_ERR_NULL, "a required pointer is NULL");
   if (mx && (!fp8_codes || !e8m0_scales)) return fail(MHC_ERR_NULL, "mxfp8 output needs fp8_codes and e8m0_scales");
   if (gridm && !fp8_codes) return fail(MHC_ERR_NULL, "fp8_grid output needs fp8_codes (the bf16 grid)");
@@ -255,9 +269,9 @@ int mhc_seam(const void* R, const void* Y, const float* post_prev, const float* 
   // Overlap checks: outputs against inputs (R' may be R exactly) and each other.
   const size_t TH = (size_t)T * H;
   Range in[] = {rng(R, TH * 8), rng(Y, Y ? TH * 2 : 0), rng(post_prev, post_prev ? (size_t)T * 16 : 0),
-                rng(comb_prev, comb_prev ? (size_t)T * 64 : 0), rng(pre_prev, (size_t)T * 16), rng(fn, (size_t)H * 4 * 24 * 4),
+                rng(comb_prev, comb_prev ? (size_t)T * 64 : 0), rng(pre_prev, pre_prev ? (size_t)T * 16 : 0), rng(fn, (size_t)H * 4 * 24 * 4),
                 rng(fn_packed, fn_packed ? mhc_packed_fn_bytes(H) : 0), rng(bias, 96), rng(alpha, 12),
-                rng(gamma, (size_t)H * 2)};
+                rng(gamma, gamma ? (size_t)H * 2 : 0)};
   Range out[] = {rng(residual_out, residual_out ? TH * 8 : 0), rng(norm, TH * 2), rng(fp8_codes, mx ? TH : (gridm ? TH * 2 : 0)),
                  rng(e8m0_scales, mx ? TH / 32 : 0), rng(pre_out, (size_t)T * 16), rng(post_out, (size_t)T * 16),
                  rng(comb_out, (size_t)T * 64), rng(workspace, need)};
@@ -301,20 +315,38 @@ int mhc_seam(const void* R, const void* Y, const float* post_prev, const float* 
   a.sinkhorn_iters = (cfg && cfg->sinkhorn_iters) ? cfg->sinkhorn_iters : 20;
   a.amax_floor = (cfg && cfg->amax_floor > 0.f) ? cfg->amax_floor : 1e-10f;
   a.spin_limit = (cfg && cfg->spin_limit) ? cfg->spin_limit : kDefaultSpin;
+  a.unshifted = unsh ? 1 : 0;
 
   int launches = 0;
   if (plan.path == 2 || plan.path == 3) {
     if (!fn_packed) return fail(MHC_ERR_NULL, "the streaming path needs fn_packed (mhc_pack_fn) or cfg.path = 1");
     if (T >= ((int64_t)1 << 31)) return fail(MHC_ERR_SHAPE, "the streaming path takes T < 2^31");
-    cudaError_t e = mhc::stream_launch(a, plan.tc_proj, plan.path == 3 ? 16 : 4, s,
+    mhc::SeamArgs a1 = a;
+    if (unsh) {
+      // First pass of the unshifted ordering: R', the gates and the fresh pre.
+      // Its x and norm are not stored (norm NULL); the carried pre and gamma
+      // that feed them are pointed at R, which is valid memory of at least
+      // T * 16 and H * 2 bytes, so the discarded arithmetic reads no stray
+      // address.
+      a1.norm = nullptr;
+      a1.gamma = a.R;
+      a1.pre_prev = reinterpret_cast<const float*>(a.R);
+      a1.unshifted = 0;
+    }
+    cudaError_t e = mhc::stream_launch(a1, plan.tc_proj, plan.path == 3 ? 16 : 4, s,
                                        (unsigned long long)a.spin_limit * 100ull, &launches);
     if (e == cudaErrorInvalidValue) return fail(MHC_ERR_CUDA, "tensor map encoding failed (streaming path)");
     if (e != cudaSuccess) return cuda_fail(e, "seam launch (streaming path)");
+    if (unsh) {  // second pass: x = sum_i pre[i] R'[i] with the fresh pre
+      e = mhc::unshifted_x_launch(ident ? R : residual_out, pre_out, T, H, norm, dev->num_sms, s);
+      if (e != cudaSuccess) return cuda_fail(e, "x launch (unshifted ordering)");
+      ++launches;
+    }
     g_launches = launches;
     return MHC_OK;
   }
   int cap = 0;
-  cudaError_t e = mhc::split_capacity(Y != nullptr, mx, plan.BT, plan.Wd, dev->num_sms, &cap);
+  cudaError_t e = mhc::split_capacity(Y != nullptr, unsh ? 2 : (mx ? 1 : 0), plan.BT, plan.Wd, dev->num_sms, &cap);
   if (e != cudaSuccess) return cuda_fail(e, "occupancy query (split path)");
   const int Gh = (H + plan.Wd - 1) / plan.Wd;
   int64_t per_launch = cap / Gh;
@@ -323,6 +355,25 @@ int mhc_seam(const void* R, const void* Y, const float* post_prev, const float* 
   if (e != cudaSuccess) return cuda_fail(e, "seam launch (split path)");
   g_launches = launches;
   return MHC_OK;
+}
+
+int mhc_seam(const void* R, const void* Y, const float* post_prev, const float* comb_prev, const float* pre_prev,
+             const float* fn, const void* fn_packed, const float* bias, const float* alpha, const void* gamma,
+             float eps, int64_t T, int H, mhc_out_mode out_mode, void* residual_out, void* norm, uint8_t* fp8_codes,
+             uint8_t* e8m0_scales, float* pre_out, float* post_out, float* comb_out, void* workspace,
+             size_t ws_bytes, const mhc_config* cfg, void* stream) {
+  return seam_impl(false, R, Y, post_prev, comb_prev, pre_prev, fn, fn_packed, bias, alpha, gamma, eps, T, H,
+                   out_mode, residual_out, norm, fp8_codes, e8m0_scales, pre_out, post_out, comb_out, workspace,
+                   ws_bytes, cfg, stream);
+}
+
+int mhc_seam_unshifted(const void* R, const void* Y, const float* post_prev, const float* comb_prev,
+                       const float* fn, const void* fn_packed, const float* bias, const float* alpha, float eps,
+                       int64_t T, int H, void* residual_out, void* x_out, float* pre_out, float* post_out,
+                       float* comb_out, void* workspace, size_t ws_bytes, const mhc_config* cfg, void* stream) {
+  return seam_impl(true, R, Y, post_prev, comb_prev, nullptr, fn, fn_packed, bias, alpha, nullptr, eps, T, H,
+                   MHC_OUT_BF16, residual_out, x_out, nullptr, nullptr, pre_out, post_out, comb_out, workspace,
+                   ws_bytes, cfg, stream);
 }
 
 int mhc_quant_ue8m0(const void* x, int64_t rows, int H, float amax_floor, uint8_t* codes, uint8_t* scales,

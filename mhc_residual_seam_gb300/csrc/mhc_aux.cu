@@ -1,5 +1,6 @@
 // Auxiliary kernels of libmhcseam: the fn hi/lo pack, the standalone ue8m0
-// quantiser, and the streaming copy used as the bandwidth ceiling.
+// quantiser, the streaming copy used as the bandwidth ceiling, and the second
+// pass of the unshifted ordering.
 
 #include "mhc_common.cuh"
 
@@ -57,6 +58,48 @@ __global__ void __launch_bounds__(512) copy_kernel(const uint4* __restrict__ src
     __stcs(dst + i + 3 * stride, d);
   }
   for (; i < n16; i += stride) __stcs(dst + i, __ldcs(src + i));
+}
+
+// The unshifted ordering's second pass on the streaming path: x[t,h] =
+// bf16(sum_i pre[t,i] R'[t,i,h]) with the fresh pre the seam kernel just wrote
+// (it needs every column's projection, so it follows that kernel on the same
+// stream; the recent part of R' is still in L2).  Work item = (token, 8
+// columns): four 16-byte R' loads and one 16-byte store, grid-stride.
+__global__ void __launch_bounds__(256) unshifted_x_kernel(const __nv_bfloat16* __restrict__ rp,
+                                                          const float* __restrict__ pre, int64_t T, int H,
+                                                          __nv_bfloat16* __restrict__ x) {
+  const int segs = H / 8;
+  const int64_t n = T * segs;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const int64_t t = i / segs;
+    const int h = (int)(i - t * segs) * 8;
+    const float4 p = __ldg(reinterpret_cast<const float4*>(pre + t * 4));
+    const __nv_bfloat16* r = rp + t * kStreams * H + h;
+    float r0[8], r1[8], r2[8], r3[8], xv[8];
+    unpack8(__ldcs(reinterpret_cast<const uint4*>(r)), r0);
+    unpack8(__ldcs(reinterpret_cast<const uint4*>(r + H)), r1);
+    unpack8(__ldcs(reinterpret_cast<const uint4*>(r + 2 * H)), r2);
+    unpack8(__ldcs(reinterpret_cast<const uint4*>(r + 3 * H)), r3);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) xv[e] = fmaf(p.w, r3[e], fmaf(p.z, r2[e], fmaf(p.y, r1[e], p.x * r0[e])));
+    uint4 ov;
+    ov.x = pack_bf16x2(xv[0], xv[1]); ov.y = pack_bf16x2(xv[2], xv[3]);
+    ov.z = pack_bf16x2(xv[4], xv[5]); ov.w = pack_bf16x2(xv[6], xv[7]);
+    __stcs(reinterpret_cast<uint4*>(x + t * H + h), ov);
+  }
+}
+
+cudaError_t unshifted_x_launch(const void* rp, const float* pre, int64_t T, int H, void* x, int num_sms,
+                               cudaStream_t s) {
+  const int64_t n = T * (H / 8);
+  int64_t blocks = (int64_t)num_sms * 8;
+  const int64_t need = (n + 255) / 256;
+  if (blocks > need) blocks = need;
+  if (blocks < 1) blocks = 1;
+  unshifted_x_kernel<<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<const __nv_bfloat16*>(rp), pre, T, H,
+                                                      reinterpret_cast<__nv_bfloat16*>(x));
+  return cudaGetLastError();
 }
 
 cudaError_t pack_fn_launch(const float* fn, void* out, int H, cudaStream_t s) {

@@ -46,6 +46,7 @@ struct SeamArgs {
   int sinkhorn_iters;
   float amax_floor;
   long long spin_limit;
+  int unshifted;                   // 1: the unshifted ordering (x with the fresh pre, no norm; into `norm`)
 };
 
 // ------------------------------------------------------------------ bf16 --

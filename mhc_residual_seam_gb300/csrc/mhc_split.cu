@@ -16,6 +16,11 @@
 // Work item = (token, 8 consecutive columns): four 16-byte R loads and one Y
 // load, the 4x4 post-mix in fp32, one bf16 rounding, and the rounded R' feeds
 // the sums, the projection and x (x stays in shared memory until rstd_x).
+//
+// The unshifted ordering (MODE 2) keeps the CTA's R' in shared memory instead
+// of x: the finishing CTA publishes the fresh pre of each token (in place of
+// rstd_x), and every CTA then forms its columns of x = sum_i pre[i] R'[i],
+// stored as bf16 with no norm.
 
 #include <string>
 
@@ -28,7 +33,8 @@ constexpr int kSplitWarps = kSplitThreads / 32;
 
 // Workspace of one token group (one slot per gridDim.y): arrival counter and
 // generation word, rstd_x of the group's tokens, and the per-CTA partials
-// [Gh][BT][32] (26 used).
+// [Gh][BT][32] (26 used; in the unshifted ordering words 26-29 of CTA 0's rows
+// carry the fresh pre from the finishing CTA to the others).
 constexpr size_t kSlotCtrl = 64;
 constexpr size_t kSlotRstd = 128;  // 32 floats
 
@@ -37,19 +43,27 @@ size_t split_slot_bytes(int Gh, int BT) {
   return (b + 255) & ~(size_t)255;
 }
 
-size_t split_smem_bytes(int BT, int Wd) {
-  return sizeof(float) * ((size_t)BT * Wd + (size_t)kSplitWarps * BT * kParts + (size_t)BT * kParts);
+constexpr int kPartPre = 26;  // unshifted: the fresh pre in words 26-29 of CTA 0's partial rows
+
+// Dynamic shared memory: x [BT][Wd] fp32 (unshifted: R' [BT][Wd/8][4] of
+// 16-byte bf16 runs, twice the bytes), per-warp partials, the finisher's sums.
+size_t split_smem_bytes(int BT, int Wd, bool unshifted) {
+  return sizeof(float) * ((size_t)BT * Wd * (unshifted ? 2 : 1) + (size_t)kSplitWarps * BT * kParts +
+                          (size_t)BT * kParts);
 }
 
-template <bool POST, bool MXFP8, int BT>
+// MODE: 0 bf16 norm, 1 bf16 norm + mxfp8, 2 the unshifted ordering
+template <bool POST, int MODE, int BT>
 __global__ void __launch_bounds__(kSplitThreads) split_seam_kernel(SeamArgs a, int Wd, int Gh,
                                                                    int64_t tok_base, char* slots,
                                                                    size_t slot_bytes) {
+  constexpr bool MXFP8 = MODE == 1, UNSH = MODE == 2;
   extern __shared__ float smem[];
-  float* xs = smem;                               // [BT][Wd]
-  float* wp = xs + (size_t)BT * Wd;               // [warps][BT][kParts]
+  float* xs = smem;                               // [BT][Wd] (unshifted: R' of the four streams)
+  float* wp = xs + (size_t)BT * Wd * (UNSH ? 2 : 1);    // [warps][BT][kParts]
   float* tot = wp + (size_t)kSplitWarps * BT * kParts;  // [BT][kParts]
   __shared__ float s_rstd[BT];
+  __shared__ float4 s_pre[UNSH ? BT : 1];
   __shared__ int s_last;
   __shared__ unsigned s_gen;
 
@@ -79,7 +93,8 @@ __global__ void __launch_bounds__(kSplitThreads) split_seam_kernel(SeamArgs a, i
       float4 c = ident ? make_float4(0.f, 0.f, 0.f, 0.f) : __ldg(reinterpret_cast<const float4*>(a.comb_prev + t * 16) + q);
       comb[4 * q] = c.x; comb[4 * q + 1] = c.y; comb[4 * q + 2] = c.z; comb[4 * q + 3] = c.w;
     }
-    float4 p = __ldg(reinterpret_cast<const float4*>(a.pre_prev + t * 4));
+    float4 p = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (!UNSH) p = __ldg(reinterpret_cast<const float4*>(a.pre_prev + t * 4));
     preg[0] = p.x; preg[1] = p.y; preg[2] = p.z; preg[3] = p.w;
     if (POST) {
       float4 q = __ldg(reinterpret_cast<const float4*>(a.post_prev + t * 4));
@@ -123,6 +138,7 @@ __global__ void __launch_bounds__(kSplitThreads) split_seam_kernel(SeamArgs a, i
           ov.z = pack_bf16x2(v[4], v[5]); ov.w = pack_bf16x2(v[6], v[7]);
           st_stream(a.res_out + (t * kStreams + i) * H + h, ov);
         }
+        if (UNSH) reinterpret_cast<uint4*>(xs)[((size_t)tl * (Wd >> 3) + seg) * kStreams + i] = ov;
         float rp[8];
         unpack8(ov, rp);
         const float4* f = reinterpret_cast<const float4*>(a.fn + ((size_t)i * H + h) * kLogits);
@@ -140,11 +156,13 @@ __global__ void __launch_bounds__(kSplitThreads) split_seam_kernel(SeamArgs a, i
           }
         }
       }
-      float* xrow = xs + (size_t)tl * Wd + seg * 8;
+      if (!UNSH) {
+        float* xrow = xs + (size_t)tl * Wd + seg * 8;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        xrow[e] = x[e];
-        acc[25] = fmaf(x[e], x[e], acc[25]);
+        for (int e = 0; e < 8; ++e) {
+          xrow[e] = x[e];
+          acc[25] = fmaf(x[e], x[e], acc[25]);
+        }
       }
     }
   }
@@ -198,6 +216,14 @@ __global__ void __launch_bounds__(kSplitThreads) split_seam_kernel(SeamArgs a, i
         finish_gates(p[24], p, a.alpha, a.bias, kStreams * H, a.eps, a.sinkhorn_iters, pre, post, cb);
         store_gates(a, tt, pre, post, cb);
         r = 1.0f / sqrtf(p[25] / (float)H + a.eps);
+        if (UNSH) {
+          const float4 pv = make_float4(pre[0], pre[1], pre[2], pre[3]);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) __stcg(part + (size_t)tid * kPartStride + kPartPre + q, (&pv.x)[q]);
+          s_pre[tid] = pv;
+        }
+      } else if (UNSH) {
+        s_pre[tid] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
       __stcg(rstd_ws + tid, r);
       s_rstd[tid] = r;
@@ -217,9 +243,41 @@ __global__ void __launch_bounds__(kSplitThreads) split_seam_kernel(SeamArgs a, i
       }
     }
     __syncthreads();
-    if (tid < BT) s_rstd[tid] = __ldcg(rstd_ws + tid);
+    if (tid < BT) {
+      s_rstd[tid] = __ldcg(rstd_ws + tid);
+      if (UNSH) {
+        float4 pv;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) (&pv.x)[q] = __ldcg(part + (size_t)tid * kPartStride + kPartPre + q);
+        s_pre[tid] = pv;
+      }
+    }
   }
   __syncthreads();
+
+  // ---- unshifted: x = sum_i pre[i] R'[i] with the fresh pre, bf16, no norm ----
+  if (UNSH) {
+    if (tvalid) {
+      const float4 pv = s_pre[tl];
+      for (int item = tid; item < BT * nseg; item += kSplitThreads) {
+        const int seg = item / BT;
+        const int h = h0 + seg * 8;
+        const uint4* rr = reinterpret_cast<const uint4*>(xs) + ((size_t)tl * (Wd >> 3) + seg) * kStreams;
+        float r0[8], r1[8], r2[8], r3[8], xv[8];
+        unpack8(rr[0], r0);
+        unpack8(rr[1], r1);
+        unpack8(rr[2], r2);
+        unpack8(rr[3], r3);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) xv[e] = fmaf(pv.w, r3[e], fmaf(pv.z, r2[e], fmaf(pv.y, r1[e], pv.x * r0[e])));
+        uint4 ov;
+        ov.x = pack_bf16x2(xv[0], xv[1]); ov.y = pack_bf16x2(xv[2], xv[3]);
+        ov.z = pack_bf16x2(xv[4], xv[5]); ov.w = pack_bf16x2(xv[6], xv[7]);
+        st_stream(a.norm + t * H + h, ov);
+      }
+    }
+    return;
+  }
 
   // ---- norm (and the ue8m0 quantiser) of this CTA's columns ----
   if (!MXFP8) {
@@ -273,22 +331,23 @@ __global__ void __launch_bounds__(kSplitThreads) split_seam_kernel(SeamArgs a, i
 // ------------------------------------------------------------- launcher --
 using SplitKernel = void (*)(SeamArgs, int, int, int64_t, char*, size_t);
 
-template <bool POST, bool MXFP8>
+template <bool POST, int MODE>
 static SplitKernel pick_bt(int BT) {
   switch (BT) {
-    case 1: return split_seam_kernel<POST, MXFP8, 1>;
-    case 2: return split_seam_kernel<POST, MXFP8, 2>;
-    case 4: return split_seam_kernel<POST, MXFP8, 4>;
-    case 8: return split_seam_kernel<POST, MXFP8, 8>;
-    case 16: return split_seam_kernel<POST, MXFP8, 16>;
-    case 32: return split_seam_kernel<POST, MXFP8, 32>;
+    case 1: return split_seam_kernel<POST, MODE, 1>;
+    case 2: return split_seam_kernel<POST, MODE, 2>;
+    case 4: return split_seam_kernel<POST, MODE, 4>;
+    case 8: return split_seam_kernel<POST, MODE, 8>;
+    case 16: return split_seam_kernel<POST, MODE, 16>;
+    case 32: return split_seam_kernel<POST, MODE, 32>;
     default: return nullptr;
   }
 }
 
-SplitKernel split_kernel(bool post, bool mxfp8, int BT) {
-  if (post) return mxfp8 ? pick_bt<true, true>(BT) : pick_bt<true, false>(BT);
-  return mxfp8 ? pick_bt<false, true>(BT) : pick_bt<false, false>(BT);
+// mode: 0 bf16 norm, 1 + mxfp8, 2 the unshifted ordering
+SplitKernel split_kernel(bool post, int mode, int BT) {
+  if (post) return mode == 2 ? pick_bt<true, 2>(BT) : mode == 1 ? pick_bt<true, 1>(BT) : pick_bt<true, 0>(BT);
+  return mode == 2 ? pick_bt<false, 2>(BT) : mode == 1 ? pick_bt<false, 1>(BT) : pick_bt<false, 0>(BT);
 }
 
 size_t split_workspace_bytes(int Gh, int BT, int64_t groups_per_launch) {
@@ -299,7 +358,7 @@ size_t split_workspace_bytes(int Gh, int BT, int64_t groups_per_launch) {
 cudaError_t split_init(size_t max_smem) {
   const int bts[] = {1, 2, 4, 8, 16, 32};
   for (int p = 0; p < 2; ++p)
-    for (int m = 0; m < 2; ++m)
+    for (int m = 0; m < 3; ++m)
       for (int b : bts) {
         cudaError_t e = cudaFuncSetAttribute(split_kernel(p, m, b), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)max_smem);
@@ -309,10 +368,10 @@ cudaError_t split_init(size_t max_smem) {
 }
 
 // Largest number of CTAs of this instantiation that can be resident at once.
-cudaError_t split_capacity(bool post, bool mxfp8, int BT, int Wd, int num_sms, int* ctas) {
+cudaError_t split_capacity(bool post, int mode, int BT, int Wd, int num_sms, int* ctas) {
   int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, split_kernel(post, mxfp8, BT), kSplitThreads,
-                                                                split_smem_bytes(BT, Wd));
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, split_kernel(post, mode, BT), kSplitThreads,
+                                                                split_smem_bytes(BT, Wd, mode == 2));
   *ctas = per_sm * num_sms;
   return e;
 }
@@ -324,13 +383,14 @@ cudaError_t split_launch(const SeamArgs& a, int BT, int Wd, int64_t groups_per_l
   const int Gh = (a.H + Wd - 1) / Wd;
   const size_t slot_bytes = split_slot_bytes(Gh, BT);
   const int64_t groups = (a.T + BT - 1) / BT;
-  SplitKernel k = split_kernel(a.Y != nullptr, a.codes != nullptr, BT);
+  const int mode = a.unshifted ? 2 : (a.codes != nullptr ? 1 : 0);
+  SplitKernel k = split_kernel(a.Y != nullptr, mode, BT);
   for (int64_t g0 = 0; g0 < groups; g0 += groups_per_launch) {
     const int64_t n = groups - g0 < groups_per_launch ? groups - g0 : groups_per_launch;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)Gh, (unsigned)n, 1);
     cfg.blockDim = dim3(kSplitThreads, 1, 1);
-    cfg.dynamicSmemBytes = split_smem_bytes(BT, Wd);
+    cfg.dynamicSmemBytes = split_smem_bytes(BT, Wd, mode == 2);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;

@@ -68,6 +68,13 @@ constexpr uint32_t kRTile = kBM * 128;                 // 4 KB
 constexpr uint32_t kFnTile = kFnRows * 128;            // 6 KB
 constexpr uint32_t kFnStage = 4 * kFnTile;             // 24 KB: [192 x 64] bf16
 constexpr uint32_t kInStage = 5 * kRTile;              // 20 KB: R tiles 0-3, Y tile 4
+// The input ring holds 4 stages of R + Y, or, in the forms without Y, 5
+// stages of R in the same bytes (more loads in flight per SM).
+constexpr int kNIMax = 5;
+template <int FORM>
+__host__ __device__ constexpr int in_stages() { return FORM == 1 ? 4 : 5; }
+template <int FORM>
+__host__ __device__ constexpr uint32_t in_stage_bytes() { return FORM == 1 ? kInStage : 4 * kRTile; }
 constexpr uint32_t kOffNormT = 4 * kRTile;             // output stage: R' tiles 0-3, then the norm tile,
 constexpr uint32_t kOffCodesT = 5 * kRTile;            //   then the codes tile [32 x 64] u8
 constexpr uint32_t kOutStage = 5 * kRTile + kBM * 64;  // 22 KB (a multiple of 1 KB: swizzled tiles)
@@ -101,16 +108,16 @@ struct alignas(128) GateTile {
 template <int KCL>
 struct Geo {
   static constexpr int kCl = KCL;
-  static constexpr int kNI = 4;                         // input stages
+  static constexpr uint32_t kInRing = 4 * kInStage;     // input ring: 80 KB
   static constexpr int kSlots = kBM / KCL;              // tokens owned per CTA and block
   static constexpr int kGamChunks = KCL == 4 ? kMaxChunksTC : (kMaxChunks * 4) / KCL;  // gamma staged in smem
   static constexpr uint32_t kXsBytes = KCL * kBM * 4;   // s_x partials landing in each CTA per block
   static constexpr uint32_t kRecvBytes = KCL * kSlots * kOwnerParts * 4;  // owner partials per CTA per block
   static constexpr uint32_t kOffIn = kOffOut + kNO * kOutStage;
-  static constexpr uint32_t kOffTail = kOffIn + kNI * kInStage;
+  static constexpr uint32_t kOffTail = kOffIn + kInRing;
   struct Tail {
     GateTile gates;                        // one block's carried gates (the producer loads the next once compute has read them)
-    uint64_t in_full[kNI], in_empty[kNI], fn_full[kNF], fn_empty[kNF], out_full[kNO], out_empty[kNO];
+    uint64_t in_full[kNIMax], in_empty[kNIMax], fn_full[kNF], fn_empty[kNF], out_full[kNO], out_empty[kNO];
     uint64_t d_full, xs_full[2], recv_full[2], recv_free[2], gates_full, gates_empty;
     uint64_t red_full[2], dbuf_full, dbuf_free, d_free;
     uint32_t tmem_base;
@@ -190,7 +197,10 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
   using G = Geo<KCL>;
   constexpr int kThreads = threads_of<OUT>();
   constexpr bool POST = FORM == 1, IDENT = FORM == 2;
-  constexpr int kCl = G::kCl, kNI = G::kNI, kSlots = G::kSlots;
+  constexpr int kNI = in_stages<FORM>();
+  constexpr uint32_t kInStageF = in_stage_bytes<FORM>();
+  static_assert(kNI <= kNIMax && kNI * kInStageF <= G::kInRing, "input ring");
+  constexpr int kCl = G::kCl, kSlots = G::kSlots;
   constexpr uint32_t kOffIn = G::kOffIn, kXsBytes = G::kXsBytes, kRecvBytes = G::kRecvBytes;
   typename G::Tail* tl = reinterpret_cast<typename G::Tail*>(sm + G::kOffTail);
   const Ctx X{&a, &tl->err, limit_ns};
@@ -285,7 +295,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
         for (int c = 0; c < nch; ++c, ++j) {
           const int s = j % kNI;
           wait_local(X, &tl->in_empty[s], ((j / kNI) & 1) ^ 1);
-          uint8_t* st = sm + kOffIn + s * kInStage;
+          uint8_t* st = sm + kOffIn + s * kInStageF;
           const int h = (c * kCl + (int)rank) * kChunk;
           mbar_arrive_expect_tx(&tl->in_full[s], bytes);
 #pragma unroll
@@ -352,6 +362,9 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
     }
   } else if (warp == 12) {
     // ---------------------------- stores: R' tiles, norm tile, e4m3 codes --
+    // (no norm pointer: the first pass of the unshifted ordering, which keeps
+    // R' and the gates only)
+    const bool store_norm = a.norm != nullptr;
     int j = 0;
     // lane = token: the ue8m0 codes of one norm tile (two 32-column groups)
     auto quant_tile = [&](const uint8_t* nt, uint8_t* ct, int64_t tp, int h) {
@@ -392,7 +405,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
           if (lane == 0) {
             for (int g = 0; g < ng; ++g) {
               const int h = ((c0 + g) * kCl + (int)rank) * kChunk;
-              tma_store_2d(&tmN, ost + g * kRTile, h, tp);
+              if (store_norm) tma_store_2d(&tmN, ost + g * kRTile, h, tp);
               if (OUT == 1) tma_store_2d(&tmC, ost + kOffNormT + g * 2048, h, tp);
             }
             tma_store_commit();
@@ -419,7 +432,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
             for (int i = 0; i < 4; ++i) tma_store_3d(&tmRo, ost + i * kRTile, h, i, t0);
           }
           if (prev) {
-            tma_store_2d(&tmN, ost + kOffNormT, h, tp);
+            if (store_norm) tma_store_2d(&tmN, ost + kOffNormT, h, tp);
             if (OUT == 1) tma_store_2d(&tmC, ost + kOffCodesT, h, tp);
           }
           tma_store_commit();
@@ -748,7 +761,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
         {
           const int s = ji % kNI;
           wait_local(X, &tl->in_full[s], (ji / kNI) & 1);
-          const uint8_t* st = sm + kOffIn + s * kInStage;
+          const uint8_t* st = sm + kOffIn + s * kInStageF;
           uint4 rin[4], yin = make_uint4(0, 0, 0, 0);
 #pragma unroll
           for (int i = 0; i < 4; ++i) rin[i] = *reinterpret_cast<const uint4*>(st + i * kRTile + off);
@@ -1012,7 +1025,8 @@ cudaError_t stream_launch(const SeamArgs& a, bool tcgen05_proj, int kcl, cudaStr
             encode(&mRo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.res_out ? (const void*)a.res_out : (const void*)a.R, d3, s3,
                    b3, CU_TENSOR_MAP_SWIZZLE_128B) &&
             encode(&mFn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.fn_packed, dF, s3, bF, CU_TENSOR_MAP_SWIZZLE_128B) &&
-            encode(&mN, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.norm, d2, s2, b2, CU_TENSOR_MAP_SWIZZLE_128B);
+            encode(&mN, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.norm ? (const void*)a.norm : (const void*)a.R, d2, s2, b2,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
   if (ok) ok = encode(&mY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.Y ? (const void*)a.Y : (const void*)a.R, d2, s2, b2,
                       CU_TENSOR_MAP_SWIZZLE_128B);
   if (ok) {  // the quantised output: e4m3 codes (u8), or the fp8_grid (bf16, laid out like the norm)

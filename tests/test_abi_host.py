@@ -79,6 +79,36 @@ def test_identity_form_ignores_residual_out(L):
     assert _seam(L, comb_prev=None, Y=None, post_prev=None, pre_prev=None) == -1
 
 
+def _unsh(L, **over):
+    args = dict(R=FAKE, Y=FAKE + 0x100000, post_prev=FAKE + 0x200000, comb_prev=FAKE + 0x300000, fn=FAKE + 0x500000,
+                fn_packed=None, bias=FAKE + 0x600000, alpha=FAKE + 0x700000, eps=1e-6, T=4, H=64, residual_out=FAKE + 0x900000,
+                x_out=FAKE + 0xA00000, pre_out=FAKE + 0xB00000, post_out=FAKE + 0xC00000, comb_out=FAKE + 0xD00000,
+                ws=FAKE + 0xE00000, ws_bytes=1 << 30, cfg=None)
+    args.update(over)
+    a = args
+    return L.mhc_seam_unshifted(a["R"], a["Y"], a["post_prev"], a["comb_prev"], a["fn"], a["fn_packed"], a["bias"],
+                                a["alpha"],
+                                a["eps"], a["T"], a["H"], a["residual_out"], a["x_out"], a["pre_out"], a["post_out"],
+                                a["comb_out"], a["ws"], a["ws_bytes"], a["cfg"], None)
+
+
+def test_unshifted_argument_rules(L):
+    assert _unsh(L, T=0, R=None, ws=None) == 0
+    assert _unsh(L, x_out=None) == -1
+    assert _unsh(L, Y=None) == -4
+    assert _unsh(L, comb_prev=None) == -4
+    assert _unsh(L, x_out=FAKE + 0x100000) == -9          # x over Y
+    # the split path keeps R' (8 bytes per element) in shared memory: a tile the
+    # delayed seam takes is refused here
+    big = B.MhcConfig(block_m=32, cols_per_cta=640)
+    assert _unsh(L, H=5120, cfg=C.byref(big)) == -10
+    assert _seam(L, H=5120, cfg=C.byref(big), ws_bytes=1) == -5
+    assert L.mhc_workspace_bytes_unshifted(4096, 5120, None) == L.mhc_workspace_bytes(4096, 5120, None) == 256
+    p1 = B.MhcConfig(path=1)
+    need = L.mhc_workspace_bytes_unshifted(4096, 5120, C.byref(p1))
+    assert need > 256 and _unsh(L, T=4096, H=5120, cfg=C.byref(p1), ws_bytes=need - 1) == -5
+
+
 def test_null_and_alignment(L):
     assert _seam(L, gamma=None) == -1
     assert _seam(L, out_mode=1) == -1           # mxfp8 without codes/scales

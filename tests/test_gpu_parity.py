@@ -507,3 +507,81 @@ def test_identity_form_matches_identity_comb_and_rejects_y():
         B.mhc_seam(g["R"], Y, post, None, g["pre_prev"], g["fn"], g["fn_packed"], g["bias"], g["alpha"],
                    g["gamma"], d["eps"], B.MHC_OUT_BF16, out["residual_out"], out["norm"], None, None,
                    out["pre_out"], out["post_out"], out["comb_out"], out["workspace"])
+
+
+# ------------------------------------------------------ unshifted ordering (f4) --
+def _run_unshifted(d, cfg=None):
+    T, H = d["T"], d["H"]
+    g = to_dev(d)
+    out = B.alloc_outputs(T, H, B.MHC_OUT_BF16, "cuda", cfg, unshifted=True)
+    if d["comb_prev"] is None:
+        out["residual_out"] = None
+    B.mhc_seam_unshifted(g["R"], g["Y"], g["post_prev"], g["comb_prev"], g["fn"], g["fn_packed"], g["bias"],
+                         g["alpha"], d["eps"], out["residual_out"], out["norm"], out["pre_out"], out["post_out"],
+                         out["comb_out"], out["workspace"], cfg=cfg)
+    h = to_host(out)
+    h["launches"] = B.mhc_last_launch_count()
+    return h
+
+
+def check_unshifted_x(xg: np.ndarray, pre_g: np.ndarray, o: dict, rp_g: np.ndarray | None = None) -> None:
+    """The unshifted x against the oracle.  x = sum_i pre[i] R'[i] takes the
+    FRESH pre, which the kernel computes in fp32 (within the 1e-3 gate bar,
+    in practice about 1e-6) and the oracle in double, and the kernel's R' may
+    differ from the oracle's by the 1 ulp the residual bar allows; where the
+    four terms nearly cancel, those differences are many ulps of x.  So every
+    element must be within 1 ulp of the oracle or within the difference the
+    inputs explain, sum_i |dpre_i| |R'_i| + sum_i |pre_i| |dR'_i| + 2^-20
+    sum_i |pre_i R'_i| (fp32 accumulation) + 1 ulp; and 99.9 % of them within
+    1 ulp.  rp_g: the kernel's R' bits (None where R' = R on both sides)."""
+    u = ulp_diff(xg, o["x"])
+    rp = I.from_bf16_bits(o["residual_out"]).double().numpy()             # [n, 4, H]
+    dpre = np.abs(pre_g.astype(np.float64) - o["pre"])                      # [n, 4]
+    bound = (np.einsum("ni,nih->nh", dpre, np.abs(rp)) +
+             2.0 ** -20 * np.einsum("ni,nih->nh", np.abs(o["pre"]), np.abs(rp)))
+    if rp_g is not None:
+        drp = np.abs(I.from_bf16_bits(rp_g).double().numpy() - rp)
+        bound += np.einsum("ni,nih->nh", np.abs(o["pre"]), drp)
+    xo = I.from_bf16_bits(o["x"]).double().numpy()
+    ulp_o = np.maximum(np.abs(xo), 2.0 ** -126) * 2.0 ** -7
+    ad = np.abs(I.from_bf16_bits(xg).double().numpy() - xo)
+    ok = (u <= 1) | (ad <= bound + ulp_o)
+    assert ok.all(), ("x", int((~ok).sum()), float(ad[~ok].max()))
+    assert np.mean(u <= 1) >= 0.999, ("x", float(np.mean(u <= 1)))
+
+
+@pytest.mark.parametrize("T,H,post,ident,path", [
+    (4, 5120, True, False, 0), (64, 5120, False, False, 0), (300, 5120, True, False, 1), (1100, 5120, True, False, 0),
+    (1100, 5120, True, False, 1), (33, 160, True, False, 0), (40, 5120, False, True, 0), (40, 5120, False, True, 1),
+    (2050, 4096, True, False, 2), (17, 7168, True, False, 0), (1500, 7168, False, False, 2), (300, 5120, True, True, 3),
+    (97, 1024, True, False, 3)])
+def test_unshifted(T, H, post, ident, path):
+    d = make_case(T, H, 8800 + T + H, post=post, ident=ident)
+    h = _run_unshifted(d, cfg=B.MhcConfig(path=path))
+    idx = sample_tokens(T, 24, 8800 + T) if T > 512 else None
+    sl = (lambda x: x) if idx is None else (lambda x: None if x is None else x[torch.from_numpy(idx)])
+    take = (lambda x: x) if idx is None else (lambda x: x[idx])
+    o = O.seam_unshifted(sl(d["R"]), sl(d["Y"]), sl(d["post_prev"]), sl(d["comb_prev"]), d["fn"], d["bias"],
+                         d["alpha"], d["eps"])
+    if not ident:
+        u = ulp_diff(take(h["residual_out"]), o["residual_out"])
+        assert np.mean(u <= 1) >= 0.9999, ("residual_out", float(np.mean(u <= 1)), int(u.max()))
+    check_unshifted_x(take(h["norm"]), take(h["pre_out"]), o, None if ident else take(h["residual_out"]))
+    for gk, ok in (("pre_out", "pre"), ("post_out", "post"), ("comb_out", "comb")):
+        err = np.abs(take(h[gk]).astype(np.float64) - o[ok].reshape(take(h[gk]).shape))
+        assert err.max() <= GATE_TOL, (ok, float(err.max()))
+
+
+def test_unshifted_paths_agree_and_launch_counts():
+    d = make_case(300, 5120, 8900)
+    o = O.seam_unshifted(d["R"], d["Y"], d["post_prev"], d["comb_prev"], d["fn"], d["bias"], d["alpha"], d["eps"])
+    a = _run_unshifted(d, cfg=B.MhcConfig(block_m=8, cols_per_cta=128))   # split path, another tiling
+    b = _run_unshifted(d, cfg=B.MhcConfig(path=2))                        # streaming: two launches
+    c = _run_unshifted(d, cfg=B.MhcConfig(path=3))
+    assert a["launches"] >= 1 and b["launches"] == 2 and c["launches"] == 2
+    for h in (a, b, c):
+        check_unshifted_x(h["norm"], h["pre_out"], o, h["residual_out"])
+        assert np.mean(ulp_diff(h["residual_out"], o["residual_out"]) <= 1) >= 0.9999
+    big = B.MhcConfig(block_m=32, cols_per_cta=640)   # the split path's R' tile does not fit
+    with pytest.raises(RuntimeError, match="shared memory"):
+        _run_unshifted(d, cfg=big)
