@@ -585,3 +585,71 @@ def test_unshifted_paths_agree_and_launch_counts():
     big = B.MhcConfig(block_m=32, cols_per_cta=640)   # the split path's R' tile does not fit
     with pytest.raises(RuntimeError, match="shared memory"):
         _run_unshifted(d, cfg=big)
+
+
+# ------------------------------------------------ robustness of the new forms --
+@pytest.mark.parametrize("path", [1, 2])
+def test_unshifted_in_place_and_empty(path):
+    d = make_case(300, 5120, 9300 + path)
+    o = O.seam_unshifted(d["R"], d["Y"], d["post_prev"], d["comb_prev"], d["fn"], d["bias"], d["alpha"], d["eps"])
+    g = to_dev(d)
+    cfg = B.MhcConfig(path=path)
+    out = B.alloc_outputs(300, 5120, B.MHC_OUT_BF16, "cuda", cfg, unshifted=True)
+    # residual_out == R: R' overwrites R in place, and the second pass reads it back
+    B.mhc_seam_unshifted(g["R"], g["Y"], g["post_prev"], g["comb_prev"], g["fn"], g["fn_packed"], g["bias"],
+                         g["alpha"], d["eps"], g["R"], out["norm"], out["pre_out"], out["post_out"], out["comb_out"],
+                         out["workspace"], cfg=cfg)
+    torch.cuda.synchronize()
+    rp = I.bf16_bits(g["R"].cpu())
+    assert np.mean(ulp_diff(rp, o["residual_out"]) <= 1) >= 0.9999
+    h = to_host(out)
+    check_unshifted_x(h["norm"], h["pre_out"], o, rp)
+    # T = 0: nothing launched
+    B.mhc_seam_unshifted(g["R"], g["Y"], g["post_prev"], g["comb_prev"], g["fn"], g["fn_packed"], g["bias"],
+                         g["alpha"], d["eps"], out["residual_out"], out["norm"], out["pre_out"], out["post_out"],
+                         out["comb_out"], out["workspace"], cfg=cfg, T=0)
+    assert B.mhc_last_launch_count() == 0
+
+
+def test_unshifted_graph_capture_matches_eager():
+    d = make_case(1100, 5120, 9310)
+    g = to_dev(d)
+    cfg = B.MhcConfig(path=2)
+    out = B.alloc_outputs(1100, 5120, B.MHC_OUT_BF16, "cuda", cfg, unshifted=True)
+
+    def call(s=None):
+        B.mhc_seam_unshifted(g["R"], g["Y"], g["post_prev"], g["comb_prev"], g["fn"], g["fn_packed"], g["bias"],
+                             g["alpha"], d["eps"], out["residual_out"], out["norm"], out["pre_out"], out["post_out"],
+                             out["comb_out"], out["workspace"], cfg=cfg, stream=s)
+
+    call()
+    eager = to_host(out)
+    for k in ("residual_out", "norm", "pre_out", "post_out", "comb_out"):
+        out[k].zero_()
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            call(s)                     # both launches captured
+    for _ in range(3):
+        graph.replay()
+    rep = to_host(out)
+    for k in ("residual_out", "norm", "pre_out", "post_out", "comb_out"):
+        assert np.array_equal(rep[k], eager[k]), k
+
+
+def test_fp8_grid_graph_replay_is_deterministic():
+    d = make_case(1024, 5120, 9320, grid=True)
+    g = to_dev(d)
+    out = run_gpu(d, g=g, cfg=B.MhcConfig(path=2))
+    eager = to_host(out)
+    out["fp8_codes"].zero_()
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            run_gpu(d, g=g, out=out, cfg=B.MhcConfig(path=2), stream=s)
+    for _ in range(2):
+        graph.replay()
+    rep = to_host(out)
+    assert np.array_equal(rep["fp8_codes"], eager["fp8_codes"]) and np.array_equal(rep["norm"], eager["norm"])

@@ -64,3 +64,20 @@ def test_noalloc_refuses_calls_beyond_its_scratch():
     with pytest.raises(B.MhcError) as e:
         _noalloc(d, g, out, cfg=B.MhcConfig(path=2))
     assert e.value.code == -10
+
+
+def test_noalloc_identity_form():
+    # no comb, Y or post: R' = R, the residual buffer is left alone
+    d = make_case(64, 5120, 9400, ident=True)
+    g = to_dev(d)
+    ref = to_host(run_gpu(d, g=g, cfg=B.MhcConfig(path=1)))
+    out = B.alloc_outputs(64, 5120, d["out_mode"], "cuda")
+    out["residual_out"].fill_(5.0)
+    _noalloc(d, g, out)
+    torch.cuda.synchronize()
+    assert bool((out["residual_out"] == 5.0).all())
+    h = to_host(out)
+    assert np.mean(ulp_diff(h["norm"], ref["norm"]) <= 1) >= 0.9999
+    for k in ("pre_out", "post_out", "comb_out"):
+        assert np.max(np.abs(h[k].astype(np.float64) - ref[k])) <= 1e-3, k
+
