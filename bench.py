@@ -27,6 +27,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -109,9 +110,9 @@ class ClockSampler:
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index: int):
+    def __init__(self, device_index: int, path: str | None = None):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
+        self.path = path or os.path.join(tempfile.gettempdir(), f"mhc_bench_clocks_rank{device_index}.csv")
         sel = []
         try:
             uuid = str(torch.cuda.get_device_properties(device_index).uuid)
@@ -122,7 +123,8 @@ class ClockSampler:
 
     def start(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            if os.path.dirname(self.path):
+                os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(self.cmd, stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
@@ -214,7 +216,7 @@ def run_ours(args, w: dict, rank: int, world: int, local_rank: int) -> dict | No
         torch.cuda.synchronize(device)
         run_step = graph.replay
 
-    sampler = ClockSampler(local_rank)
+    sampler = ClockSampler(local_rank, args.clocks_csv and args.clocks_csv.replace("{rank}", str(local_rank)))
     sampler.start()
     time.sleep(0.2)
     if world > 1:
@@ -359,6 +361,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT)
+    ap.add_argument("--clocks-csv", default=None,
+                    help="where the nvidia-smi samples of the timed region go ({rank} is replaced); default: a temp file")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--projection", choices=["auto", "mma", "tcgen05"], default="auto",

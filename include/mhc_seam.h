@@ -209,8 +209,8 @@ int mhc_copy(const void* src, void* dst, size_t bytes, void* stream);
 /* mhc_seam() on the split path (cfg->path 0 or 1; paths 2 and 3 are refused) for
  * callers that cannot allocate device memory: a plug-in inside a host program
  * that owns every device allocation, code running inside an allocator
- * callback, or a loop that must never block in the allocator.  The paper has
- * no counterpart; this entry point exists only for such callers.
+ * callback, or a loop that must never block in the allocator.  The method's
+ * pages describe no such entry point; it exists only for such callers.
  * Arguments are those of mhc_seam() without fn_packed, workspace and ws_bytes.
  * The scratch (partial sums, arrival counters, status word) lives in a fixed
  * 1 MiB static device array in the library, held by every GPU that loads it
