@@ -58,6 +58,9 @@ WORKLOADS = {
     "seam_T64_H5120_post_bf16": dict(T=64, H=5120, post=True, out="bf16", seed=1001),
     "seam_T64_H5120_nopost_bf16": dict(T=64, H=5120, post=False, out="bf16", seed=1001),
     "seam_T4_H5120_post_bf16": dict(T=4, H=5120, post=True, out="bf16", seed=1000),
+    # this GPU's own wave edge: 36 clusters of 4 take 36 blocks of 32 tokens a round
+    **{f"seam_T{t}_H5120_post_bf16": dict(T=t, H=5120, post=True, out="bf16", seed=1003)
+       for t in (1152, 1184, 2304, 2336)},
     # the T sweep of the pages' single-launch table (config 4 inputs)
     **{f"seam_T{t}_H5120_post_bf16": dict(T=t, H=5120, post=True, out="bf16", seed=1004)
        for t in (1, 32, 384, 2048, 8192)},

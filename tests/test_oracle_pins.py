@@ -389,6 +389,25 @@ def test_constant_row_norm_closed_form(oracle):
     assert np.array_equal(o["norm"], np.broadcast_to(g ^ 0x8000, (T, H)))
 
 
+def test_unit_gamma_zero_eps_norm_has_unit_rms(oracle):
+    # gamma = 1 and eps = 0: norm = x / rms(x), so each row's mean square is 1
+    # up to the bf16 rounding of every element (relative 2^-9 each)
+    T, H = 4, 512
+    d = seam_inputs(T, H, 21, oracle=oracle)
+    d["gamma"] = I.to_bf16(np.ones(H))
+    d["eps"] = 0.0
+    o = run(oracle, d, want_x=True)
+    nv = np.array([[bf16_val(b) for b in row] for row in o["norm"]])
+    ms = np.mean(nv * nv, axis=1)
+    assert np.all(np.abs(ms - 1.0) < 2 * 2.0 ** -8), ms
+    # and each element is the RNE of x / rms(x) computed exactly from x
+    x = o["x"]
+    for t in range(T):
+        rms = math.sqrt(float(np.mean(x[t] * x[t])))
+        for h in range(0, H, 37):
+            assert o["norm"][t, h] == bf16_rne_exact(Fraction(x[t, h] / rms)), (t, h)
+
+
 def test_gate_ranges_and_doubly_stochastic_on_config_inputs(oracle):
     d = seam_inputs(16, 256, 1000, oracle=oracle)
     o = run(oracle, d)
