@@ -551,10 +551,11 @@ def run_unshifted(oracle, d):
                                  d["eps"])
 
 
-@pytest.mark.parametrize("seed,post", [(37, True), (38, False)])
-def test_brute_force_T1_H8_unshifted(oracle, seed, post):
+@pytest.mark.parametrize("seed,post,ident", [(37, True, False), (38, False, False), (39, False, True)])
+def test_brute_force_T1_H8_unshifted(oracle, seed, post, ident):
     d = seam_inputs(1, 8, seed, post=post, oracle=oracle)
-    d["comb_prev"] = np.array([[[0.9, 0.05, 0.3, -0.2], [0.1, 0.7, 0.0, 0.4], [-0.3, 0.2, 1.1, 0.05], [0.25, -0.1, 0.15, 0.6]]], np.float32)
+    d["comb_prev"] = None if ident else np.array(
+        [[[0.9, 0.05, 0.3, -0.2], [0.1, 0.7, 0.0, 0.4], [-0.3, 0.2, 1.1, 0.05], [0.25, -0.1, 0.15, 0.6]]], np.float32)
     d["bias"] = torch.linspace(-0.7, 0.3, 24)
     d["alpha"] = torch.tensor([1.2, 0.9, 0.7])
     o = run_unshifted(oracle, d)
