@@ -6,7 +6,7 @@
 // for all four streams (the cluster reads each row in long runs) and the
 // cluster walks blocks of 32 tokens.  Per 64-column chunk:
 //  - an input producer warp TMA-loads the four R tiles and the Y tile into a
-//    ring of 4 input stages (128-byte swizzle), and each block's carried
+//    ring of 4 input stages (5 without Y; 128-byte swizzle), and each block's carried
 //    gates (comb, pre, post) into a buffer as it starts the block, so they
 //    wait in shared memory when compute gets there;
 //  - an fn producer warp TMA-loads the four hi/lo-packed fn tiles [48 x 64]
@@ -41,6 +41,10 @@
 // ("[FlyDSL] Single-launch Mega-mHC on gfx950", Kernel Architecture: split-K
 // with a distributed finish; here the cluster launch makes every CTA of a
 // split co-resident.)
+//
+// Forms: post, no_post, and identity (the first block's seam: R' = R, no
+// residual store).  A call with no norm pointer stores no norm: the first
+// pass of the unshifted ordering, which needs only R' and the gates.
 //
 // Every wait is bounded; after the first wait that runs out, the CTA records
 // the error (bit 1 of the status word) and every later wait returns at once,
