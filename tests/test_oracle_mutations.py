@@ -35,6 +35,17 @@ MUTATIONS = {
     "identity_form_stream_shifted": ("const uint16_t b = Rt[i * H + h];", "const uint16_t b = Rt[((i + 1) % N_HC) * H + h];"),
     "unshifted_pre_index_shifted": ("v += pre_out[t * 4 + i] * mhc_oracle_bf16_to_double(residual_out[t * K + i * H + h]);",
                                     "v += pre_out[t * 4 + (i + 1) % N_HC] * mhc_oracle_bf16_to_double(residual_out[t * K + i * H + h]);"),
+    "sigmoid_sign_flipped": ("return 1.0 / (1.0 + exp(-z));", "return 1.0 / (1.0 + exp(z));"),
+    "eps_outside_rstd_sqrt": ("double rstdR = 1.0 / sqrt(sR / (double)K + eps);",
+                              "double rstdR = 1.0 / (sqrt(sR / (double)K) + eps);"),
+    "norm_uses_gate_rstd": ("mhc_oracle_bf16_rne(x[h] * rstdx * mhc_oracle_bf16_to_double(gamma[h]))",
+                            "mhc_oracle_bf16_rne(x[h] * rstdR * mhc_oracle_bf16_to_double(gamma[h]))"),
+    "post_gate_of_stream0_everywhere": ("if (Y) v += (double)post_prev[t * 4 + i] *", "if (Y) v += (double)post_prev[t * 4] *"),
+    "bias_dropped_from_logits": ("l[k] = (double)alpha[g] * rstdR * d[k] + (double)bias[k];",
+                                 "l[k] = (double)alpha[g] * rstdR * d[k];"),
+    "comb_logits_shifted": ("for (int q = 0; q < 16; ++q) M[q] = exp(l[8 + q]);",
+                            "for (int q = 0; q < 16; ++q) M[q] = exp(l[8 + (q + 1) % 16]);"),
+    "sum_of_squares_halved": ("sR += rp[r] * rp[r];", "sR += 0.5 * rp[r] * rp[r];"),
     "unshifted_x_scaled": ("x_out[t * H + h] = mhc_oracle_bf16_rne(v);", "x_out[t * H + h] = mhc_oracle_bf16_rne(v * 1.0009765625);"),
 }
 
