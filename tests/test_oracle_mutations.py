@@ -46,6 +46,13 @@ MUTATIONS = {
     "comb_logits_shifted": ("for (int q = 0; q < 16; ++q) M[q] = exp(l[8 + q]);",
                             "for (int q = 0; q < 16; ++q) M[q] = exp(l[8 + (q + 1) % 16]);"),
     "sum_of_squares_halved": ("sR += rp[r] * rp[r];", "sR += 0.5 * rp[r] * rp[r];"),
+    "e4m3_ties_away_from_zero": ("double r = rint(a / spacing) * spacing;   /* r <= 448: 448 is on the grid */",
+                                 "double r = round(a / spacing) * spacing;   /* r <= 448: 448 is on the grid */"),
+    "e4m3_subnormal_spacing": ("        spacing = ldexp(1.0, -9);\n    } else {", "        spacing = ldexp(1.0, -8);\n    } else {"),
+    "amax_signed_not_abs": ("                double a = fabs(mhc_oracle_bf16_to_double(src[j]));\n                if (a > amax) amax = a;\n            }\n            int e = mhc_oracle_ue8m0_exponent(amax, amax_floor);\n            scales",
+                            "                double a = mhc_oracle_bf16_to_double(src[j]);\n                if (a > amax) amax = a;\n            }\n            int e = mhc_oracle_ue8m0_exponent(amax, amax_floor);\n            scales"),
+    "codes_scaled_up_not_down": ("codes[r * H + g * 32 + j] =\n                    mhc_oracle_e4m3_rne_satfinite(ldexp(mhc_oracle_bf16_to_double(src[j]), -e));",
+                                 "codes[r * H + g * 32 + j] =\n                    mhc_oracle_e4m3_rne_satfinite(ldexp(mhc_oracle_bf16_to_double(src[j]), e));"),
     "unshifted_x_scaled": ("x_out[t * H + h] = mhc_oracle_bf16_rne(v);", "x_out[t * H + h] = mhc_oracle_bf16_rne(v * 1.0009765625);"),
 }
 
@@ -92,9 +99,14 @@ def test_planted_slip_fails_a_pin(tmp_path, monkeypatch, name):
         except AssertionError:
             failed.append(pin.__name__)
     extra = []
-    if not failed:  # the brute force is the slowest pin; run it only if needed
+    # the slowest pins (the brute force, the exhaustive e4m3 sweep with its
+    # exact ties) run only if the quick ones missed the slip
+    for slow in (lambda: P.test_brute_force_T1_H8_asymmetric_comb(O, 31),
+                 lambda: P.test_e4m3_exhaustive_over_significands_and_exponents(O)):
+        if failed or extra:
+            break
         try:
-            P.test_brute_force_T1_H8_asymmetric_comb(O, 31)
+            slow()
         except AssertionError:
-            extra.append("brute_force")
+            extra.append("slow pin")
     assert failed or extra, f"no pin caught {name}"
