@@ -653,3 +653,31 @@ def test_fp8_grid_graph_replay_is_deterministic():
         graph.replay()
     rep = to_host(out)
     assert np.array_equal(rep["fp8_codes"], eager["fp8_codes"]) and np.array_equal(rep["norm"], eager["norm"])
+
+
+# ------------------------------------------- the NEXT rows at the full size --
+def test_full_size_fp8_grid_and_identity():
+    # T = 16384, in the launch configuration the benchmark times: sampled
+    # tokens against the oracle, the whole grid against the oracle's grid of
+    # the kernel's own norm
+    d = make_case(16384, 5120, 1004, grid=True, unique_tokens=2048)
+    h = to_host(run_gpu(d))
+    rep = compare(d, h, sample_tokens(16384, 24, 1004))
+    assert rep["grid_mismatch"] == 0
+    d = make_case(16384, 5120, 1004, ident=True, unique_tokens=2048)
+    h = to_host(run_gpu(d))
+    compare(d, h, sample_tokens(16384, 24, 1005))
+
+
+def test_full_size_unshifted():
+    d = make_case(16384, 5120, 1004, unique_tokens=2048)
+    h = _run_unshifted(d)
+    assert h["launches"] == 2
+    idx = sample_tokens(16384, 24, 1006)
+    t = torch.from_numpy(idx)
+    o = O.seam_unshifted(d["R"][t], d["Y"][t], d["post_prev"][t], d["comb_prev"][t], d["fn"], d["bias"],
+                         d["alpha"], d["eps"])
+    assert np.mean(ulp_diff(h["residual_out"][idx], o["residual_out"]) <= 1) >= 0.9999
+    check_unshifted_x(h["norm"][idx], h["pre_out"][idx], o, h["residual_out"][idx])
+    for gk, ok in (("pre_out", "pre"), ("post_out", "post"), ("comb_out", "comb")):
+        assert np.abs(h[gk][idx].astype(np.float64) - o[ok].reshape(h[gk][idx].shape)).max() <= GATE_TOL
