@@ -52,7 +52,7 @@ def test_config2_T1024_mxfp8_crafted():
     assert rep["codes_mismatch"] == 0
 
 
-@pytest.mark.parametrize("T", [4160])
+@pytest.mark.parametrize("T", [4159, 4160, 4161])
 def test_config3_wave_edge(T):
     d = make_case(T, 5120, 1003, unique_tokens=1024)
     h = to_host(run_gpu(d))
