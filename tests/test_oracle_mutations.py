@@ -53,10 +53,12 @@ MUTATIONS = {
                             "                double a = mhc_oracle_bf16_to_double(src[j]);\n                if (a > amax) amax = a;\n            }\n            int e = mhc_oracle_ue8m0_exponent(amax, amax_floor);\n            scales"),
     "codes_scaled_up_not_down": ("codes[r * H + g * 32 + j] =\n                    mhc_oracle_e4m3_rne_satfinite(ldexp(mhc_oracle_bf16_to_double(src[j]), -e));",
                                  "codes[r * H + g * 32 + j] =\n                    mhc_oracle_e4m3_rne_satfinite(ldexp(mhc_oracle_bf16_to_double(src[j]), e));"),
+    "x_pre_index_shifted": ("v += (double)pre[i] * rp[i * H + h];", "v += (double)pre[(i + 1) % N_HC] * rp[i * H + h];"),
     "unshifted_x_scaled": ("x_out[t * H + h] = mhc_oracle_bf16_rne(v);", "x_out[t * H + h] = mhc_oracle_bf16_rne(v * 1.0009765625);"),
 }
 
 PINS = [
+    lambda o: P.test_stream_permutation_equivariance(o, (1, 2, 3, 0)),
     P.test_unshifted_zero_fn_gives_half_sum_of_streams,
     lambda o: P.test_brute_force_T1_H8_unshifted(o, 37, True, False),
     P.test_identity_form_keeps_signed_zeros_and_subnormals,

@@ -321,6 +321,32 @@ def test_collapse_uses_carried_pre(oracle):
         assert np.array_equal(o["x"], rp[:, i])
 
 
+@pytest.mark.parametrize("perm", [(1, 0, 2, 3), (3, 2, 1, 0), (2, 3, 0, 1), (1, 2, 3, 0)])
+def test_stream_permutation_equivariance(oracle, perm):
+    # Relabel the four streams: R, the rows and columns of comb, post, pre and
+    # the fn row blocks all move together.  R' moves with them; the logits are
+    # sums over every (stream, column) pair, so the gates are unchanged, and
+    # so are x and the norm (the same terms, summed in another order: within
+    # rounding, and bit-identical here).
+    T, H = 3, 32
+    d = seam_inputs(T, H, 44, oracle=oracle)
+    d["comb_prev"] = d["comb_prev"] + np.float32(0.05) * np.arange(16, dtype=np.float32).reshape(1, 4, 4)
+    p = list(perm)
+    e = dict(d)
+    e["R"] = d["R"][:, p, :]
+    e["comb_prev"] = np.ascontiguousarray(d["comb_prev"][:, p, :][:, :, p])
+    e["post_prev"] = np.ascontiguousarray(d["post_prev"][:, p])
+    e["pre_prev"] = np.ascontiguousarray(d["pre_prev"][:, p])
+    e["fn"] = d["fn"].reshape(4, H, 24)[p].reshape(4 * H, 24)
+    a, b = run(oracle, d), run(oracle, e)
+    assert np.array_equal(b["residual_out"], a["residual_out"][:, p, :])
+    assert np.max(np.abs(b["pre"] - a["pre"])) < 1e-12
+    assert np.max(np.abs(b["post"] - a["post"])) < 1e-12
+    assert np.max(np.abs(b["comb"] - a["comb"])) < 1e-12
+    ulp = np.abs(b["norm"].astype(np.int64) - a["norm"].astype(np.int64))
+    assert ulp.max() <= 1 and np.mean(ulp == 0) > 0.99
+
+
 def test_zero_fn_gives_bias_gates(oracle):
     d = seam_inputs(2, 64, 17, oracle=oracle)
     d["fn"] = torch.zeros_like(d["fn"])
