@@ -9,13 +9,14 @@ bandwidth in TB/s (algorithmic bytes, 20 H per token, over the device time of
 the step), ``ms_per_step`` the seam time.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--no-e2e] [--no-cpu-baseline]
+                    [--workload NAME] [--no-e2e] [--no-cpu-baseline] [--no-copy-ceiling]
 
-Under torchrun every rank runs the full workload on its own GPU (the seam is
-per token, so ranks shard tokens with no exchange: weak scaling); rank 0
-prints the whole-job value.  ``--impl reference`` times the oracle (plain
-single-threaded C, fp64) on the host cores on a bounded token sample of the
-same workload.
+Under torchrun the job is a batch of N x T tokens and rank r takes its shard,
+tokens r T .. (r + 1) T - 1, on its own GPU: the seam is per token, so the
+shards need no exchange (weak scaling: T tokens per GPU whatever N).  Rank 0
+prints the whole-job value, all ranks' bytes over the slowest rank's time.
+``--impl reference`` times the oracle (plain single-threaded C, fp64) on the
+host cores on a bounded token sample of the same workload.
 """
 from __future__ import annotations
 
@@ -97,8 +98,18 @@ def carried_gates(pre_l, post_l, comb_l, iters: int = 20):
     return pre.float().contiguous(), post.float().contiguous(), M.float().contiguous()
 
 
-def make_workload(w: dict, device) -> dict:
-    d = I.seam_draws(w["T"], w["H"], w["seed"], post=w["post"], unique_tokens=UNIQUE_TOKENS)
+def token_shard(T_total: int, rank: int, world: int) -> tuple[int, int]:
+    """Tokens [t0, t1) of a batch of T_total that rank `rank` of `world` takes:
+    contiguous, as even as possible, the first T_total % world ranks one more."""
+    base, extra = divmod(T_total, world)
+    t0 = rank * base + min(rank, extra)
+    return t0, t0 + base + (1 if rank < extra else 0)
+
+
+def make_workload(w: dict, device, token_offset: int = 0, unique: int = UNIQUE_TOKENS) -> dict:
+    """The inputs of one shard: rows token_offset .. token_offset + T - 1 of
+    the job's batch (its `unique` distinct rows repeat along the batch)."""
+    d = I.seam_draws(w["T"], w["H"], w["seed"], post=w["post"], unique_tokens=unique, token_offset=token_offset)
     pre, post, comb = carried_gates(d["pre_logits"], d["post_logits"], d["comb_logits"])
     host = {"R": d["R"], "Y": d["Y"], "post_prev": post if w["post"] else None,
             "comb_prev": None if w.get("ident") else comb, "pre_prev": pre,
@@ -168,7 +179,9 @@ def run_ours(args, w: dict, rank: int, world: int, local_rank: int) -> dict | No
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
     B.lib()
-    wl = make_workload(w, device)
+    t0, t1 = token_shard(w["T"] * world, rank, world)   # this rank's shard of the job's batch
+    assert t1 - t0 == w["T"]
+    wl = make_workload(w, device, token_offset=t0)
     g, host = wl["dev"], wl["host"]
     T, H = w["T"], w["H"]
     mx = w["out"] == "mxfp8"
@@ -293,9 +306,44 @@ def run_ours(args, w: dict, rank: int, world: int, local_rank: int) -> dict | No
         e2e_ms = a0.elapsed_time(a1) / n_e2e
         e2e = {"ms": e2e_ms, "h2d": bi, "d2h": bo}
 
+    copy = None if args.no_copy_ceiling else copy_ceiling(
+        ACC.seam_bytes(T, H, post=w["post"], out=w["out"], ident=w.get("ident", False)), device, stream)
     ms_max, e2e_max = reduce_max([ms, e2e["ms"] if e2e else 0.0], world, device)
     return {"ms": ms_max, "e2e": e2e and dict(e2e, ms=e2e_max), "launches": launches, "clocks": clocks, "wl": wl,
+            "copy": copy,
             "calls": runs * per_graph}
+
+
+def copy_ceiling(seam_bytes: int, device, stream, reps: int = 10) -> dict:
+    """The copy ceiling of one seam call: a device-to-device copy whose read +
+    write bytes equal the seam's ("[FlyDSL] Single-launch Mega-mHC on gfx950",
+    Realistic Bandwidth Ceiling), as cudaMemcpyAsync (torch's copy of a dense
+    tensor) and as this library's 16-byte streaming copy kernel; best of
+    `reps` each, CUDA events on the launching stream.  Outside the seam's
+    timed region."""
+    from mhc_residual_seam_gb300 import binding as B
+
+    half = seam_bytes // 2 // 16 * 16
+    src = torch.empty(half, dtype=torch.uint8, device=device)
+    dst = torch.empty_like(src)
+    src.fill_(7)
+    res = {}
+    for name, fn in (("memcpy", lambda: dst.copy_(src)), ("mhc_copy", lambda: B.mhc_copy(src, dst, stream=stream))):
+        for _ in range(3):
+            fn()
+        best = float("inf")
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            best = min(best, e0.elapsed_time(e1) * 1e-3)
+        res[name + "_gbs"] = 2 * half / best / 1e9
+    del src, dst
+    res["bytes"] = 2 * half
+    res["best_gbs"] = max(res["memcpy_gbs"], res["mhc_copy_gbs"])
+    return res
 
 
 def cpu_baseline(w: dict, wl: dict | None, budget_s: float = 15.0, steps: int = 1) -> dict:
@@ -368,6 +416,8 @@ def main():
                     help="where the nvidia-smi samples of the timed region go ({rank} is replaced); default: a temp file")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-copy-ceiling", action="store_true",
+                    help="skip the device-to-device copy of the seam's bytes (the copy ceiling)")
     ap.add_argument("--projection", choices=["auto", "mma", "tcgen05"], default="auto",
                     help="streaming path's gate projection (auto = the library's policy)")
     ap.add_argument("--path", choices=["auto", "split", "stream", "stream16"], default="auto",
@@ -385,7 +435,8 @@ def main():
     config = {"workload": args.workload, "T": w["T"], "H": w["H"], "n_hc": 4,
               "form": "identity" if w.get("ident") else ("post" if w["post"] else "no_post"), "out": w["out"],
               "ordering": "unshifted" if w.get("unshifted") else "delayed",
-              "tokens_per_rank": w["T"], "parallelism": f"token-shard x{args.gpus} (independent)",
+              "tokens_per_rank": w["T"], "global_batch": w["T"] * world,
+              "parallelism": f"token-shard x{world} (rank r: tokens r*T .. (r+1)*T-1, no exchange)",
               "projection": args.projection, "path": args.path,
               "timing": (f"cuda-graph replay ({GRAPH_CALLS} calls per graph)" if args.graph
                          else "back-to-back launches"),
@@ -434,6 +485,9 @@ def main():
                      "launches_per_step": r["launches"]},
         "clocks": r["clocks"],
     }
+    if r["copy"]:
+        c = r["copy"]
+        line["copy_ceiling"] = dict(c, seam_frac=achieved_gbs / c["best_gbs"])
     if r["e2e"]:
         e = r["e2e"]
         line["e2e"] = {"value": job_value(world, step_bytes, e["ms"]), "unit": UNIT,

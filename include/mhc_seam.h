@@ -92,7 +92,13 @@ typedef struct {
     int cols_per_cta;    /* path 1: columns of H per CTA, a multiple of 32; 0 = policy */
     int sinkhorn_iters;  /* Sinkhorn rounds; 0 = 20 */
     float amax_floor;    /* ue8m0 amax floor; 0 = 1e-10 */
-    long long spin_limit;/* iteration cap of every device-side wait; 0 = default (about 1 s) */
+    long long spin_limit;/* limit of every device-side wait, in units of about 100 ns; 0 = default
+                            (10^7: about 1 s).  Split path: a wait past it gives up (status
+                            bit 0).  Streaming paths: a wait past it is reported (status
+                            bit 1) and goes on; a wait one second past it abandons the call
+                            (the kernel stops issuing work, waits for its copies and MMAs in
+                            flight, frees tensor memory and returns).  Either way
+                            mhc_check_status() then returns MHC_ERR_TIMEOUT */
     int projection;      /* streaming path's gate projection: 0 = policy (2 when H <= 5120, else 1);
                             1 = warp-level tensor-core MMA (m16n8k16) in the compute warps;
                             2 = tcgen05 MMA issued by one thread into tensor memory (H <= 5120) */
@@ -115,8 +121,9 @@ size_t mhc_workspace_bytes_unshifted(int64_t T, int H, const mhc_config* cfg);
 int mhc_workspace_init(void* ws, size_t bytes, void* stream);
 
 /* Read and clear the device status word of `ws` (synchronises `stream`).
- * Returns MHC_OK, or MHC_ERR_TIMEOUT when a bounded device wait of an earlier
- * call on this workspace ran out (its outputs are then unspecified). */
+ * Returns MHC_OK, or MHC_ERR_TIMEOUT when a device wait of an earlier call on
+ * this workspace ran past cfg->spin_limit (that call's outputs are then
+ * unspecified). */
 int mhc_check_status(void* ws, void* stream);
 
 /* Bytes of the packed gate weight for width H: fn transposed to [48, 4H]
@@ -219,15 +226,24 @@ int mhc_copy(const void* src, void* dst, size_t bytes, void* stream);
  * the default policy: T above 480).  It calls no cudaMalloc/cudaFree or
  * allocating routine.  The first call on a device resolves the array's
  * address (cudaGetSymbolAddress) and should be made before any stream
- * capture.  Every call first clears the part of the array it uses
- * (cudaMemsetAsync on `stream`); all calls share the array, so calls that can
- * overlap on the GPU race on it and must be serialised by the caller.  A
- * bounded wait that runs out is not reported by this entry point. */
+ * capture.  Every call first clears the partial sums and arrival counters it
+ * uses (cudaMemsetAsync on `stream`); all calls share the array, so calls that
+ * can overlap on the GPU race on it and must be serialised by the caller.  The
+ * array's status word is not cleared by a call: mhc_noalloc_check_status()
+ * reports a bounded wait that ran out in any earlier call. */
 int mhc_seam_noalloc(const void* R, const void* Y, const float* post_prev, const float* comb_prev,
                      const float* pre_prev, const float* fn, const float* bias, const float* alpha,
                      const void* gamma, float eps, int64_t T, int H, mhc_out_mode out_mode, void* residual_out,
                      void* norm, uint8_t* fp8_codes, uint8_t* e8m0_scales, float* pre_out, float* post_out,
                      float* comb_out, const mhc_config* cfg, void* stream);
+
+/* mhc_check_status() for the static scratch of mhc_seam_noalloc() on the
+ * current device: reads and clears its status word (synchronises `stream`).
+ * Returns MHC_OK, or MHC_ERR_TIMEOUT when a bounded device wait of an earlier
+ * mhc_seam_noalloc() call ran out (that call's outputs are unspecified).  Like
+ * the entry point it serves, it has no counterpart in the method's pages and
+ * allocates nothing. */
+int mhc_noalloc_check_status(void* stream);
 
 /* Number of kernel launches the last successful mhc_seam() on this host
  * thread issued (1 for every non-empty call). */

@@ -66,6 +66,8 @@ def lib():
         L.mhc_seam_unshifted.argtypes = [P] * 8 + [C.c_float, I64, I] + [P] * 6 + [C.c_size_t, P, P]
         L.mhc_seam_noalloc.restype = I
         L.mhc_seam_noalloc.argtypes = [P] * 9 + [C.c_float, I64, I, I] + [P] * 7 + [P, P]
+        L.mhc_noalloc_check_status.restype = I
+        L.mhc_noalloc_check_status.argtypes = [P]
         L.mhc_quant_ue8m0.restype = I
         L.mhc_quant_ue8m0.argtypes = [P, I64, I, C.c_float, P, P, P]
         L.mhc_copy.restype = I
@@ -186,6 +188,10 @@ def mhc_seam_noalloc(R, Y, post_prev, comb_prev, pre_prev, fn, bias, alpha, gamm
                                   _ptr(bias), _ptr(alpha), _ptr(gamma), float(eps), int(T), int(H), int(out_mode),
                                   _ptr(residual_out), _ptr(norm), _ptr(fp8_codes), _ptr(e8m0_scales),
                                   _ptr(pre_out), _ptr(post_out), _ptr(comb_out), _cfg(cfg), _stream(stream)))
+
+
+def mhc_noalloc_check_status(stream=None) -> None:
+    _check(lib().mhc_noalloc_check_status(_stream(stream)))
 
 
 def mhc_quant_ue8m0(x, codes, scales, amax_floor: float = 0.0, stream=None) -> None:

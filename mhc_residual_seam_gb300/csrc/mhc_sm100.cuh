@@ -178,6 +178,8 @@ __device__ __forceinline__ void tc_st_x8(uint32_t taddr, const float* v) {
       : "memory");
 }
 __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// Wait for every tensor-memory load this thread issued (no register use follows).
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // TMEM load without the wait: tc_wait_ld_x8 on the same registers must come
 // before any use of them.

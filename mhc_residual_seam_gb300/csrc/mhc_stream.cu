@@ -46,9 +46,14 @@
 // residual store).  A call with no norm pointer stores no norm: the first
 // pass of the unshifted ordering, which needs only R' and the gates.
 //
-// Every wait is bounded; after the first wait that runs out, the CTA records
-// the error (bit 1 of the status word) and every later wait returns at once,
-// so the kernel always terminates.
+// Every wait is bounded, in two tiers.  A wait longer than the caller's limit
+// sets bit 1 of the status word and goes on waiting, so a short limit only
+// flags the call and the work completes as usual.  A wait one second longer
+// abandons the call: the CTA stops issuing copies, MMAs and stores, and before
+// it frees tensor memory and exits it waits (with a fixed cap) for the ones in
+// flight: the last TMA load of every input, fn and gate buffer (a buffer is
+// refilled only after its previous load was seen complete), every MMA (one
+// final tcgen05.commit) and every bulk store (bulk wait_group).
 
 #include "mhc_common.cuh"
 #include "mhc_sm100.cuh"
@@ -124,8 +129,10 @@ struct Geo {
     uint64_t in_full[kNIMax], in_empty[kNIMax], fn_full[kNF], fn_empty[kNF], out_full[kNO], out_empty[kNO];
     uint64_t d_full, xs_full[2], recv_full[2], recv_free[2], gates_full, gates_empty;
     uint64_t red_full[2], dbuf_full, dbuf_free, d_free;
+    uint64_t mma_fin;                      // exit drain: completion of every MMA issued
+    uint64_t fold_full;                    // warp-MMA form: warps 4-7 have written their partial projections
     uint32_t tmem_base;
-    volatile int err;
+    volatile int reported, aborted;
     float2 red[2][8][kBM];                 // [block parity][compute warp][token]: s_R, s_x partials
     float dbuf[4][kBM][kDPad];             // the block's projection per stream (hi + lo): [stream][token][logit]
     float xs[2][KCL][kBM];                 // [block parity][source CTA][token]: s_x partial
@@ -140,38 +147,69 @@ struct Geo {
 
 struct Ctx {
   const SeamArgs* a;
-  volatile int* err;  // the CTA's error flag in shared memory
-  uint64_t limit_ns;
+  volatile int* reported;  // the CTA has set the status bit of a slow wait
+  volatile int* aborted;   // the CTA abandons the call: no new copies, MMAs or stores
+  uint64_t report_ns;      // a wait longer than this is reported (status bit 1) and goes on
+  uint64_t abort_ns;       // a wait longer than this abandons the call
 };
 
-__device__ __forceinline__ void flag_error(const Ctx& x) {
-  if (!*x.err) {
-    *x.err = 1;
+// Fixed cap of the exit drain (waits for copies and MMAs this CTA issued,
+// which complete on their own); independent of the caller's limit and of any
+// earlier error.
+constexpr uint64_t kDrainNs = 200000000ull;
+
+__device__ __forceinline__ void report_slow(const Ctx& x) {
+  if (!*x.reported) {
+    *x.reported = 1;
     atomicOr(x.a->status, 2u);
   }
 }
-// Bounded wait on a CTA-local barrier; returns at once after an earlier error.
-__device__ __forceinline__ void wait_local(const Ctx& x, uint64_t* bar, uint32_t parity) {
-  if (mbar_test_wait(bar, parity)) return;
+// Wait on a phase of a CTA-local barrier.  Past report_ns the call is
+// reported and the wait goes on, so a short limit only flags the call; past
+// abort_ns, or at once once the CTA has abandoned the call, it returns false
+// and the caller stops issuing work (it never arrives on a barrier whose
+// phase it did not see complete).
+__device__ __forceinline__ bool wait_local(const Ctx& x, uint64_t* bar, uint32_t parity) {
+  if (mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity, 20000)) {
-    if (*x.err) return;
-    if (globaltimer_ns() - t0 > x.limit_ns) {
-      flag_error(x);
-      return;
+    if (*x.aborted) return false;
+    const uint64_t dt = globaltimer_ns() - t0;
+    if (dt > x.report_ns) report_slow(x);
+    if (dt > x.abort_ns) {
+      *x.aborted = 1;
+      return false;
     }
   }
+  return true;
 }
-__device__ __forceinline__ void wait_remote(const Ctx& x, uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait_cluster(bar, parity, 0)) return;
+// The same on a barrier that cluster peers arrive on (acquire at cluster scope).
+__device__ __forceinline__ bool wait_remote(const Ctx& x, uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait_cluster(bar, parity, 0)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait_cluster(bar, parity, 20000)) {
-    if (*x.err) return;
-    if (globaltimer_ns() - t0 > x.limit_ns) {
-      flag_error(x);
-      return;
+    if (*x.aborted) return false;
+    const uint64_t dt = globaltimer_ns() - t0;
+    if (dt > x.report_ns) report_slow(x);
+    if (dt > x.abort_ns) {
+      *x.aborted = 1;
+      return false;
     }
   }
+  return true;
+}
+// A wait every lane of a warp makes: the warp goes on only if all lanes saw
+// the phase complete, so the warp leaves its loop as one.
+__device__ __forceinline__ bool wait_warp(const Ctx& x, uint64_t* bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, wait_local(x, bar, parity));
+}
+__device__ __forceinline__ bool wait_warp_remote(const Ctx& x, uint64_t* bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, wait_remote(x, bar, parity));
+}
+// Exit drain: wait for the phase that a copy or MMA this CTA issued
+// completes, at most kDrainNs, whatever happened before.
+__device__ __forceinline__ void drain(const Ctx& x, uint64_t* bar, uint32_t parity) {
+  if (!mbar_wait(bar, parity, kDrainNs)) report_slow(x);
 }
 
 }  // namespace
@@ -195,7 +233,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
                        const __grid_constant__ CUtensorMap tmFn, const __grid_constant__ CUtensorMap tmN,
                        const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmGc,
                        const __grid_constant__ CUtensorMap tmGp, const __grid_constant__ CUtensorMap tmGq,
-                       int block0, int n_blocks, unsigned long long limit_ns) {
+                       int block0, int n_blocks, unsigned long long report_ns, unsigned long long abort_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   using G = Geo<KCL>;
@@ -207,7 +245,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
   constexpr int kCl = G::kCl, kSlots = G::kSlots;
   constexpr uint32_t kOffIn = G::kOffIn, kXsBytes = G::kXsBytes, kRecvBytes = G::kRecvBytes;
   typename G::Tail* tl = reinterpret_cast<typename G::Tail*>(sm + G::kOffTail);
-  const Ctx X{&a, &tl->err, limit_ns};
+  const Ctx X{&a, &tl->reported, &tl->aborted, report_ns, abort_ns};
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_ctarank();
@@ -242,6 +280,8 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
     mbar_init(&tl->dbuf_full, 4);  // the four D readers (or folders)
     mbar_init(&tl->dbuf_free, 1);  // the exchange warp
     mbar_init(&tl->d_free, 4);     // the four D readers
+    mbar_init(&tl->mma_fin, 1);
+    mbar_init(&tl->fold_full, 4);  // warps 4-7 (warp-MMA form)
     for (int p = 0; p < 2; ++p) {
       mbar_init(&tl->xs_full[p], 1);    // + kXsBytes of st.async from the cluster
       mbar_init(&tl->recv_full[p], 1);  // + kRecvBytes of st.async from the cluster
@@ -249,7 +289,8 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
 
       mbar_init(&tl->red_full[p], 8);
     }
-    tl->err = 0;
+    tl->reported = 0;
+    tl->aborted = 0;
     mbar_fence_init();
   }
   if (warp == 8 && lane == 0) {
@@ -286,19 +327,20 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
       // L2 lines at about the same time)
       const uint64_t pol = l2_evict_normal();
       const uint32_t bytes = (POST ? 5 : 4) * kRTile;
-      int j = 0;
-      for (int lb = 0; lb < nblk; ++lb) {
+      int j = 0, ng = 0;  // input-stage loads and gate loads issued
+      bool ok = true;
+      for (int lb = 0; lb < nblk && ok; ++lb) {
         const int t0 = (bb + lb * ncl) * kBM;
-        {  // the block's carried gates, consumed at the top of its compute
-          wait_local(X, &tl->gates_empty, (lb & 1) ^ 1);
-          mbar_arrive_expect_tx(&tl->gates_full, (IDENT ? 4 : POST ? 24 : 20) * kBM * 4);
-          if (!IDENT) tma_load_2d(&tl->gates.comb[0][0], &tmGc, &tl->gates_full, 0, t0, pol);
-          tma_load_2d(&tl->gates.pre[0][0], &tmGp, &tl->gates_full, 0, t0, pol);
-          if (POST) tma_load_2d(&tl->gates.post[0][0], &tmGq, &tl->gates_full, 0, t0, pol);
-        }
+        // the block's carried gates, consumed at the top of its compute
+        if (!(ok = wait_local(X, &tl->gates_empty, (lb & 1) ^ 1))) break;
+        mbar_arrive_expect_tx(&tl->gates_full, (IDENT ? 4 : POST ? 24 : 20) * kBM * 4);
+        if (!IDENT) tma_load_2d(&tl->gates.comb[0][0], &tmGc, &tl->gates_full, 0, t0, pol);
+        tma_load_2d(&tl->gates.pre[0][0], &tmGp, &tl->gates_full, 0, t0, pol);
+        if (POST) tma_load_2d(&tl->gates.post[0][0], &tmGq, &tl->gates_full, 0, t0, pol);
+        ++ng;
         for (int c = 0; c < nch; ++c, ++j) {
           const int s = j % kNI;
-          wait_local(X, &tl->in_empty[s], ((j / kNI) & 1) ^ 1);
+          if (!(ok = wait_local(X, &tl->in_empty[s], ((j / kNI) & 1) ^ 1))) break;
           uint8_t* st = sm + kOffIn + s * kInStageF;
           const int h = (c * kCl + (int)rank) * kChunk;
           mbar_arrive_expect_tx(&tl->in_full[s], bytes);
@@ -307,20 +349,23 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
           if (POST) tma_load_2d(st + 4 * kRTile, &tmY, &tl->in_full[s], h, t0, pol);
         }
       }
-      // every load issued has landed before the CTA can exit
-      for (int jj = (j > kNI ? j - kNI : 0); jj < j; ++jj) {
-        if (!mbar_wait(&tl->in_full[jj % kNI], (jj / kNI) & 1, limit_ns)) flag_error(X);
-      }
+      // Every load issued lands before the CTA exits.  A stage is refilled
+      // only after all eight compute warps released it, and they release it
+      // only after seeing its previous load complete, so only the last load
+      // of each stage (and of the gate buffer) can still be in flight.
+      for (int jj = (j > kNI ? j - kNI : 0); jj < j; ++jj) drain(X, &tl->in_full[jj % kNI], (jj / kNI) & 1);
+      if (ng > 0) drain(X, &tl->gates_full, (ng - 1) & 1);
     }
   } else if (warp == 10) {
     // ------------------------------------------------------ fn producer --
     if (lane == 0) {
       const uint64_t pol = l2_evict_last();
       int j = 0;
-      for (int lb = 0; lb < nblk; ++lb) {
+      bool ok = true;
+      for (int lb = 0; lb < nblk && ok; ++lb) {
         for (int c = 0; c < nch; ++c, ++j) {
           const int f = j % kNF;
-          wait_local(X, &tl->fn_empty[f], ((j / kNF) & 1) ^ 1);
+          if (!(ok = wait_local(X, &tl->fn_empty[f], ((j / kNF) & 1) ^ 1))) break;
           uint8_t* st = sm + kOffFn + f * kFnStage;
           const int h = (c * kCl + (int)rank) * kChunk;
           mbar_arrive_expect_tx(&tl->fn_full[f], kFnStage);
@@ -328,29 +373,29 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
           for (int i = 0; i < 4; ++i) tma_load_3d(st + i * kFnTile, &tmFn, &tl->fn_full[f], h, i, 0, pol);
         }
       }
-      for (int jj = (j > kNF ? j - kNF : 0); jj < j; ++jj) {
-        if (!mbar_wait(&tl->fn_full[jj % kNF], (jj / kNF) & 1, limit_ns)) flag_error(X);
-      }
+      // as for the input ring: only the last load of each fn stage can still be in flight
+      for (int jj = (j > kNF ? j - kNF : 0); jj < j; ++jj) drain(X, &tl->fn_full[jj % kNF], (jj / kNF) & 1);
     }
   } else if (warp == 9) {
     // -------------------------------------- tcgen05 projection (one thread) --
     if (!MS && lane == 0) {
       int j = 0, jr = 0;
-      for (int lb = 0; lb <= nblk; ++lb) {
+      bool ok = true;
+      for (int lb = 0; lb <= nblk && ok; ++lb) {
         if (lb == nblk) {  // the normalise-only pass: one stage per group of chunks, no MMA
           for (int c0 = 0; c0 < nch; c0 += norm_group<OUT>(), ++j) {
-            wait_local(X, &tl->out_full[j % kNO], (j / kNO) & 1);
+            if (!wait_local(X, &tl->out_full[j % kNO], (j / kNO) & 1)) break;
             mbar_arrive(&tl->out_empty[j % kNO]);
           }
           break;
         }
         for (int c = 0; c < nch; ++c, ++j) {
           const int o = j % kNO;
-          wait_local(X, &tl->out_full[o], (j / kNO) & 1);
           const int f = jr % kNF;
+          if (!(ok = wait_local(X, &tl->out_full[o], (j / kNO) & 1))) break;
           // the first MMA of a block overwrites D: the previous block's D must have been read
-          if (c == 0 && lb > 0) wait_local(X, &tl->d_free, (lb - 1) & 1);
-          wait_local(X, &tl->fn_full[f], (jr / kNF) & 1);
+          if (c == 0 && lb > 0 && !(ok = wait_local(X, &tl->d_free, (lb - 1) & 1))) break;
+          if (!(ok = wait_local(X, &tl->fn_full[f], (jr / kNF) & 1))) break;
           tc_fence_after();
           const uint32_t ra = smem_u32(sm + kOffOut + o * kOutStage);   // R' of the 4 streams [128 x 64]
           const uint32_t fb = smem_u32(sm + kOffFn + f * kFnStage);     // fn of the 4 streams [192 x 64]
@@ -363,6 +408,10 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
           ++jr;
         }
       }
+      // every MMA issued (and the commits before it) completes before the CTA
+      // exits and tensor memory is freed
+      tc_commit(&tl->mma_fin);
+      drain(X, &tl->mma_fin, 0);
     }
   } else if (warp == 12) {
     // ---------------------------- stores: R' tiles, norm tile, e4m3 codes --
@@ -390,7 +439,8 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
         if (tt < T) a.scales[tt * (H / 32) + (h + 32 * half) / 32] = sb;
       }
     };
-    for (int lb = 0; lb <= nblk; ++lb) {
+    bool ok = true;
+    for (int lb = 0; lb <= nblk && ok; ++lb) {
       const bool real = lb < nblk, prev = lb > 0;
       const int t0 = (bb + lb * ncl) * kBM, tp = (bb + (lb - 1) * ncl) * kBM;
       if (!real) {  // the normalise-only pass: the norm tiles of a group of chunks per stage
@@ -398,7 +448,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
         for (int c0 = 0; c0 < nch && prev; c0 += G, ++j) {
           const int o = j % kNO;
           uint8_t* ost = sm + kOffOut + o * kOutStage;
-          wait_local(X, &tl->out_full[o], (j / kNO) & 1);
+          if (!wait_warp(X, &tl->out_full[o], (j / kNO) & 1)) break;
           const int ng = min(G, nch - c0);
           if (OUT == 1) {  // codes tiles in stage slot 4
             for (int g = 0; g < ng; ++g)
@@ -424,7 +474,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
         const int o = j % kNO;
         uint8_t* ost = sm + kOffOut + o * kOutStage;
         const int h = (c * kCl + (int)rank) * kChunk;
-        wait_local(X, &tl->out_full[o], (j / kNO) & 1);
+        if (!(ok = wait_warp(X, &tl->out_full[o], (j / kNO) & 1))) break;
         if (OUT == 1 && prev) {
           quant_tile(ost + kOffNormT, ost + kOffCodesT, tp, h);
           fence_proxy_async_smem();
@@ -446,6 +496,8 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
         __syncwarp();
       }
     }
+    // every bulk store issued has read its shared memory and written global
+    // memory before the CTA exits (the hardware wait always ends)
     if (lane == 0) tma_store_wait_all();
   } else if (OUT == 2 && warp >= 13) {
     // ------------------------------------------------------ grid warps --
@@ -473,7 +525,8 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
       }
     };
     int j = 0;
-    for (int lb = 0; lb <= nblk; ++lb) {
+    bool ok = true;
+    for (int lb = 0; lb <= nblk && ok; ++lb) {
       const bool real = lb < nblk, prev = lb > 0;
       const int64_t tp = (int64_t)(bb + (lb - 1) * ncl) * kBM;
       if (!real) {  // the normalise-only pass: the norm tiles of a group of chunks per stage
@@ -482,7 +535,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
           const int o = j % kNO;
           if (o != me) continue;
           const uint8_t* ost = sm + kOffOut + o * kOutStage;
-          wait_local(X, &tl->out_full[o], (j / kNO) & 1);
+          if (!wait_warp(X, &tl->out_full[o], (j / kNO) & 1)) break;
           const int ng = min(G, nch - c0);
           for (int g = 0; g < ng; ++g) {
             uint32_t nb[32], gw[32];
@@ -500,7 +553,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
         const int o = j % kNO;
         if (o != me) continue;
         const uint8_t* ost = sm + kOffOut + o * kOutStage;
-        wait_local(X, &tl->out_full[o], (j / kNO) & 1);
+        if (!(ok = wait_warp(X, &tl->out_full[o], (j / kNO) & 1))) break;
         uint32_t nb[32];
         if (prev) load_row(ost + kOffNormT, nb);
         __syncwarp();
@@ -526,7 +579,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
     __syncwarp();
     for (int lb = 0; lb < nblk; ++lb) {
       const int b = bb + lb * ncl, par = lb & 1;
-      wait_local(X, &tl->red_full[par], (lb >> 1) & 1);
+      if (!wait_warp(X, &tl->red_full[par], (lb >> 1) & 1)) break;
       float sx = 0.f, sR = 0.f;
 #pragma unroll
       for (int w = 0; w < 8; ++w) {
@@ -541,8 +594,8 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
         for (int dst = 0; dst < kCl; ++dst)
           st_async_f32(mapa_shared(xa, (uint32_t)dst), sx, mapa_shared(xb, (uint32_t)dst));
       }
-      wait_local(X, &tl->dbuf_full, lb & 1);
-      if (lb >= 2) wait_remote(X, &tl->recv_free[par], ((lb >> 1) & 1) ^ 1);
+      if (!wait_warp(X, &tl->dbuf_full, lb & 1)) break;
+      if (lb >= 2 && !wait_warp_remote(X, &tl->recv_free[par], ((lb >> 1) & 1) ^ 1)) break;
       {
         const uint32_t dst = (uint32_t)(lane % kCl);
         const uint32_t ra = mapa_shared(smem_u32(&tl->recv[par][rank][lane / kCl][0]), dst);
@@ -563,7 +616,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
       if (lane == 0) mbar_arrive(&tl->dbuf_free);
 
       if (lane == 0) mbar_arrive_expect_tx(&tl->recv_full[par], kRecvBytes);
-      wait_local(X, &tl->recv_full[par], (lb >> 1) & 1);
+      if (!wait_warp(X, &tl->recv_full[par], (lb >> 1) & 1)) break;
       // sums over the cluster, one (owned token, part) pair per lane and round
       for (int i = lane; i < kSlots * kOwnerParts; i += 32) {
         const int sl = i / kOwnerParts, k = i - sl * kOwnerParts;
@@ -591,10 +644,10 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
     // . (fn_hi + fn_lo)[32 x 24], m16n8k16 MMAs with fp32 accumulation, one
     // chunk behind the R' writes of all eight warps.
     float acc[2][3][4];
-    auto mma_chunk = [&](int jj, int jr) {
+    auto mma_chunk = [&](int jj, int jr) -> bool {
       const int oo = jj % kNO, ff = jr % kNF;
-      wait_local(X, &tl->out_full[oo], (jj / kNO) & 1);
-      wait_local(X, &tl->fn_full[ff], (jr / kNF) & 1);
+      if (!wait_warp(X, &tl->out_full[oo], (jj / kNO) & 1)) return false;
+      if (!wait_warp(X, &tl->fn_full[ff], (jr / kNF) & 1)) return false;
       const uint32_t rt = smem_u32(sm + kOffOut + oo * kOutStage + (warp & 3) * kRTile);
       const uint32_t ft = smem_u32(sm + kOffFn + ff * kFnStage + (warp & 3) * kFnTile);
       const int mi = lane >> 3, rr = lane & 7;
@@ -629,30 +682,32 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
         mbar_arrive(&tl->out_empty[oo]);
         mbar_arrive(&tl->fn_empty[ff]);
       }
+      return true;
     };
 
 
     float rprev = 0.f;
     // rstd_x of block lbp from the s_x partials the four CTAs sent (same sum
     // order in every CTA, so all four hold the same value)
-    auto take_rstd = [&](int lbp) {
+    auto take_rstd = [&](int lbp) -> bool {
       const int pp = lbp & 1;
-      wait_local(X, &tl->xs_full[pp], (lbp >> 1) & 1);
+      if (!wait_warp(X, &tl->xs_full[pp], (lbp >> 1) & 1)) return false;
       float sx = 0.f;
 #pragma unroll
       for (int src = 0; src < kCl; ++src) sx += tl->xs[pp][src][lane];
       const int64_t tt = (int64_t)(bb + lbp * ncl) * kBM + lane;
       rprev = tt < T ? 1.0f / sqrtf(sx / (float)H + a.eps) : 0.f;
+      return true;
     };
 
     // tcgen05 projection: warp q reads stream q's diagonal block of block
     // lbp's D (TMEM lanes 32 q .., columns 48 q .. 48 q + 47) during the next
     // block's first chunk, frees D for that block's MMAs, and hands the
     // hi + lo sums to the exchange warp through dbuf.
-    auto read_d = [&](int lbp) {
+    auto read_d = [&](int lbp) -> bool {
       float dv[48];
       if (nch > 0) {
-        wait_local(X, &tl->d_full, lbp & 1);
+        if (!wait_warp(X, &tl->d_full, lbp & 1)) return false;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 6; ++k)
@@ -664,24 +719,25 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tl->d_free);
-      wait_local(X, &tl->dbuf_free, (lbp & 1) ^ 1);
+      if (!wait_warp(X, &tl->dbuf_free, (lbp & 1) ^ 1)) return false;
       float* r0 = &tl->dbuf[warp][lane][0];
 #pragma unroll
       for (int k = 0; k < 24; ++k) r0[k] = dv[k] + dv[24 + k];
       __syncwarp();
       if (lane == 0) mbar_arrive(&tl->dbuf_full);
+      return true;
     };
 
     int j = 0, ji = 0;
-    for (int lb = 0; lb <= nblk; ++lb) {  // the last pass only normalises the last block
+    bool ok = true;
+    for (int lb = 0; lb <= nblk && ok; ++lb) {  // the last pass only normalises the last block
       const bool real = lb < nblk, prev = lb > 0;
       if (!real) {  // the normalise-only pass: the norm tiles of a group of chunks per output stage
-        if (prev) {
-          take_rstd(lb - 1);
+        if (prev && take_rstd(lb - 1)) {
           constexpr int NG = norm_group<OUT>();
           for (int c0 = 0; c0 < nch; c0 += NG, ++j) {
             const int o = j % kNO;
-            wait_local(X, &tl->out_empty[o], ((j / kNO) & 1) ^ 1);
+            if (!wait_warp(X, &tl->out_empty[o], ((j / kNO) & 1) ^ 1)) break;
             uint8_t* ost = sm + kOffOut + o * kOutStage;
             const int ng = min(NG, nch - c0);
             for (int g = 0; g < ng; ++g) {
@@ -720,7 +776,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
 #pragma unroll
         for (int k = 0; k < 4; ++k) gc[k] = gp;
         {  // rows past T arrive as zeros
-          wait_local(X, &tl->gates_full, lb & 1);
+          if (!(ok = wait_warp(X, &tl->gates_full, lb & 1))) break;
           const GateTile& gt = tl->gates;
           if (!IDENT) {
 #pragma unroll
@@ -764,7 +820,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
         }
         {
           const int s = ji % kNI;
-          wait_local(X, &tl->in_full[s], (ji / kNI) & 1);
+          if (!(ok = wait_warp(X, &tl->in_full[s], (ji / kNI) & 1))) break;
           const uint8_t* st = sm + kOffIn + s * kInStageF;
           uint4 rin[4], yin = make_uint4(0, 0, 0, 0);
 #pragma unroll
@@ -803,8 +859,8 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
             sx2 = __ffma2_rn(xx, xx, sx2);
           }
         }
-        if (prev && c == 0) take_rstd(lb - 1);
-        wait_local(X, &tl->out_empty[o], ((j / kNO) & 1) ^ 1);
+        if (prev && c == 0 && !(ok = take_rstd(lb - 1))) break;
+        if (!(ok = wait_warp(X, &tl->out_empty[o], ((j / kNO) & 1) ^ 1))) break;
         uint8_t* ost = sm + kOffOut + o * kOutStage;
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -826,14 +882,15 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tl->out_full[o]);
-        if (!MS && prev && c == 0 && warp < 4) read_d(lb - 1);
-        if (MS && c > 0) mma_chunk(j - 1, ji - 2);
+        if (!MS && prev && c == 0 && warp < 4 && !(ok = read_d(lb - 1))) break;
+        if (MS && c > 0 && !(ok = mma_chunk(j - 1, ji - 2))) break;
       }
+      if (!ok) break;
       if (prev && nch == 0) {  // no columns here: only consume the phases
-        take_rstd(lb - 1);
-        if (!MS && warp < 4) read_d(lb - 1);
+        if (!(ok = take_rstd(lb - 1))) break;
+        if (!MS && warp < 4 && !(ok = read_d(lb - 1))) break;
       }
-      if (MS && nch > 0) mma_chunk(j - 1, ji - 1);
+      if (MS && nch > 0 && !(ok = mma_chunk(j - 1, ji - 1))) break;
       tc_wait_st();
 
       // ------------ block finish: hand the partials to the exchange warp --
@@ -842,11 +899,11 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&tl->red_full[par]);
       // no MMA follows the last block: its D is read now, not in the normalise-only pass
-      if (!MS && lb == nblk - 1 && warp < 4) read_d(lb);
+      if (!MS && lb == nblk - 1 && warp < 4 && !(ok = read_d(lb))) break;
       if (MS) {  // warps w and w + 4 both hold stream w % 4: fold them into dbuf[w % 4]
         const int g = lane >> 2, t4 = lane & 3;
         if (warp >= 4) {
-          wait_local(X, &tl->dbuf_free, (lb & 1) ^ 1);
+          if (!(ok = wait_warp(X, &tl->dbuf_free, (lb & 1) ^ 1))) break;
 #pragma unroll
           for (int m = 0; m < 2; ++m) {
 #pragma unroll
@@ -858,9 +915,10 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
               r0[8 * kDPad + 1] = acc[m][n][3];
             }
           }
-          named_bar_arrive(2, kComputeThreads);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tl->fold_full);
         } else {
-          named_bar_sync(2, kComputeThreads);
+          if (!(ok = wait_warp(X, &tl->fold_full, lb & 1))) break;
 #pragma unroll
           for (int m = 0; m < 2; ++m) {
 #pragma unroll
@@ -877,11 +935,26 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
         }
       }
     }
+    // no tensor-memory load or store of this warp is outstanding at exit
+    tc_wait_ld();
+    tc_wait_st();
   }
 
   tc_fence_before();
   __syncwarp();
-  cluster_sync_all();  // no CTA leaves while a peer may still write into it
+  // No CTA leaves while a peer may still write into it: every CTA arrives here
+  // after its last send, and the cluster barrier's release/acquire orders the
+  // peers' stores into this CTA before it goes on.
+  cluster_sync_all();
+  if (*X.aborted) {
+    // A CTA that abandoned the call may not have seen every partial a peer
+    // sent it arrive on its barriers: before its shared memory is released it
+    // also waits a fixed 20 us, far longer than a store into a cluster peer
+    // takes to land.
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 20000) {
+    }
+  }
   if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -985,35 +1058,42 @@ static int max_clusters(int form, int out, bool ms, int kcl) {
 }
 
 static cudaError_t launch_with_maps(const SeamArgs& a, const CUtensorMap* m, bool tcgen05_proj, int kcl,
-                                    cudaStream_t stream, unsigned long long limit_ns, int* launches);
+                                    cudaStream_t stream, unsigned long long report_ns, int* launches);
 static cudaError_t launch_range(const SeamArgs& a, const CUtensorMap* m, bool tcgen05_proj, int kcl, int block0,
-                                int n_blocks, cudaStream_t stream, unsigned long long limit_ns, int* launches);
+                                int n_blocks, cudaStream_t stream, unsigned long long report_ns, int* launches);
 
 // Returns cudaSuccess, or cudaErrorInvalidValue when a tensor map cannot be
 // encoded or no cluster fits (the caller reports it).  kcl: CTAs per cluster
 // (4, or 16 with the tcgen05 projection).
+// report_ns: a device wait longer than this sets status bit 1 and goes on; a
+// wait one second longer than that abandons the call (the kernel stops issuing
+// work, drains what is in flight and returns).
 cudaError_t stream_launch(const SeamArgs& a, bool tcgen05_proj, int kcl, cudaStream_t stream,
-                          unsigned long long limit_ns, int* launches) {
+                          unsigned long long report_ns, int* launches) {
   const int H = a.H;
   if (stream_cols(H) == 0 || (kcl != 4 && kcl != 16) || (kcl == 16 && !tcgen05_proj)) return cudaErrorInvalidValue;
   const cuuint64_t T = (cuuint64_t)a.T;
-  // The nine tensor maps depend only on the buffers and (T, H): a caller that
-  // repeats a call with the same buffers (a decode loop) reuses them instead of
-  // encoding them again on the host.
+  // The nine tensor maps depend only on the buffers, (T, H) and the output
+  // mode (the quantised-output map is bf16 with 2H-byte rows for the fp8_grid
+  // and u8 with H-byte rows for mxfp8, on possibly the same buffer): a caller
+  // that repeats a call with the same buffers and mode (a decode loop) reuses
+  // them instead of encoding them again on the host.
   struct MapSet {
     const void* key[9];
     int64_t T;
     int H;
+    int out;
     CUtensorMap m[9];
   };
   thread_local MapSet cache[4];
   thread_local int cache_next = 0;
+  const int out_mode = a.grid ? 2 : a.codes ? 1 : 0;
   const void* key[9] = {a.R, a.Y, a.res_out, a.fn_packed, a.norm, a.grid ? (const void*)a.grid : (const void*)a.codes,
                         a.comb_prev, a.pre_prev, a.post_prev};
   for (const MapSet& c : cache) {
-    bool hit = c.T == a.T && c.H == H;
+    bool hit = c.T == a.T && c.H == H && c.out == out_mode;
     for (int i = 0; hit && i < 9; ++i) hit = c.key[i] == key[i];
-    if (hit) return launch_with_maps(a, c.m, tcgen05_proj, kcl, stream, limit_ns, launches);
+    if (hit) return launch_with_maps(a, c.m, tcgen05_proj, kcl, stream, report_ns, launches);
   }
   CUtensorMap mR, mY, mRo, mFn, mN, mC;
   const cuuint64_t d3[3] = {(cuuint64_t)H, 4, T};
@@ -1057,23 +1137,25 @@ cudaError_t stream_launch(const SeamArgs& a, bool tcgen05_proj, int kcl, cudaStr
   cache_next = (cache_next + 1) % 4;
   c.T = a.T;
   c.H = H;
+  c.out = out_mode;
   for (int i = 0; i < 9; ++i) c.key[i] = key[i];
   c.m[0] = mR; c.m[1] = mY; c.m[2] = mRo; c.m[3] = mFn; c.m[4] = mN; c.m[5] = mC; c.m[6] = mGc; c.m[7] = mGp;
   c.m[8] = mGq;
-  return launch_with_maps(a, c.m, tcgen05_proj, kcl, stream, limit_ns, launches);
+  return launch_with_maps(a, c.m, tcgen05_proj, kcl, stream, report_ns, launches);
 }
 
 // One seam call, one launch.  (Running a partial last round as a second
 // launch over larger clusters was measured slower than the partial round.)
 static cudaError_t launch_with_maps(const SeamArgs& a, const CUtensorMap* m, bool tcgen05_proj, int kcl,
-                                    cudaStream_t stream, unsigned long long limit_ns, int* launches) {
+                                    cudaStream_t stream, unsigned long long report_ns, int* launches) {
   const int n_blocks = (int)((a.T + kBM - 1) / kBM);
-  return launch_range(a, m, tcgen05_proj, kcl, 0, n_blocks, stream, limit_ns, launches);
+  return launch_range(a, m, tcgen05_proj, kcl, 0, n_blocks, stream, report_ns, launches);
 }
 
 static cudaError_t launch_range(const SeamArgs& a, const CUtensorMap* m, bool tcgen05_proj, int kcl, int block0,
-                                int n_blocks, cudaStream_t stream, unsigned long long limit_ns, int* launches) {
+                                int n_blocks, cudaStream_t stream, unsigned long long report_ns, int* launches) {
   const bool ms = !tcgen05_proj;
+  unsigned long long abort_ns = report_ns + 1000000000ull;
   const int form = a.comb_prev == nullptr ? 2 : a.Y != nullptr ? 1 : 0;
   const int mx = a.grid ? 2 : a.codes ? 1 : 0;
   void* k = stream_kernel_ptr(form, mx, ms, kcl);
@@ -1096,7 +1178,7 @@ static cudaError_t launch_range(const SeamArgs& a, const CUtensorMap* m, bool tc
   void* args[] = {const_cast<SeamArgs*>(&a),    const_cast<CUtensorMap*>(m),     const_cast<CUtensorMap*>(m + 1),
                   const_cast<CUtensorMap*>(m + 2), const_cast<CUtensorMap*>(m + 3), const_cast<CUtensorMap*>(m + 4),
                   const_cast<CUtensorMap*>(m + 5), const_cast<CUtensorMap*>(m + 6), const_cast<CUtensorMap*>(m + 7),
-                  const_cast<CUtensorMap*>(m + 8), &b0, &nb, &limit_ns};
+                  const_cast<CUtensorMap*>(m + 8), &b0, &nb, &report_ns, &abort_ns};
   cudaError_t e = cudaLaunchKernelExC(&cfg, k, args);
   if (e == cudaSuccess) ++*launches;
   return e;

@@ -88,7 +88,8 @@ N_HC = 4
 N_LOGITS = 24
 
 
-def seam_draws(T: int, H: int, seed: int, post: bool = True, unique_tokens: int | None = None) -> dict:
+def seam_draws(T: int, H: int, seed: int, post: bool = True, unique_tokens: int | None = None,
+               token_offset: int = 0) -> dict:
     """All random inputs of one seam call (CPU tensors).
 
     Returns bf16 ``R [T,4,H]``, ``Y [T,H]`` (absent when ``post`` is False),
@@ -99,18 +100,23 @@ def seam_draws(T: int, H: int, seed: int, post: bool = True, unique_tokens: int 
     ``unique_tokens``: draw only that many tokens and repeat them along T (the
     per-token inputs of token t are those of token t mod unique_tokens).  Large
     workloads use this to keep the CPU draw short; the device still streams
-    every byte of the full T.
+    every byte of the full T.  ``token_offset`` (with ``unique_tokens``): the
+    T rows returned are rows token_offset .. token_offset + T - 1 of that
+    repeated sequence, i.e. one shard of a larger batch.
     """
-    if unique_tokens is not None and 0 < unique_tokens < T:
+    if unique_tokens is not None and 0 < unique_tokens and (unique_tokens != T or token_offset):
         d = seam_draws(unique_tokens, H, seed, post=post)
-        reps = (T + unique_tokens - 1) // unique_tokens
+        rows = (token_offset + np.arange(T, dtype=np.int64)) % unique_tokens
+        idx = torch.from_numpy(rows)
         for k in ("R", "Y"):
             if d[k] is not None:
-                d[k] = d[k].repeat((reps,) + (1,) * (d[k].dim() - 1))[:T].contiguous()
+                d[k] = d[k][idx].contiguous()
         for k in ("pre_logits", "post_logits", "comb_logits"):
-            d[k] = np.concatenate([d[k]] * reps, axis=0)[:T]
+            d[k] = d[k][rows]
         d["T"] = T
         return d
+    if token_offset:
+        raise ValueError("token_offset needs unique_tokens")
     K = N_HC * H
     d = {
         "T": T,

@@ -127,11 +127,48 @@ def compare(d: dict, h: dict, idx: np.ndarray | None = None, check_quant: bool =
     return rep
 
 
-def sample_tokens(T: int, n: int, seed: int, must: np.ndarray | None = None) -> np.ndarray:
-    """Token sample for the full-size cases: the first and last few tokens
-    (ragged tails) plus seeded picks, plus any tokens in `must`."""
-    picks = I.stream_bits(seed, 99, n) % np.uint64(max(T, 1))
-    s = set(range(min(T, 4))) | set(range(max(0, T - 4), T)) | set(int(p) for p in picks)
-    if must is not None:
-        s |= set(int(v) for v in must)
-    return np.array(sorted(s), dtype=np.int64)
+def compare_all_tokens(d: dict, h: dict, unique: int, check_quant: bool = True, slice_tokens: int = 512) -> dict:
+    """Every element of every token against the oracle, for a workload drawn
+    with ``unique_tokens=unique`` (the inputs of token t are those of token
+    t mod unique).  The oracle runs once on the distinct tokens; each GPU row
+    is compared with the oracle row of its token class, so the acceptance bar
+    (1 ulp on >= 99.99 % of all elements, gates within 1e-3, quantised outputs
+    bit-exact) is asserted over the whole output."""
+    T = d["T"]
+    U = min(unique, T)
+    o = oracle_on(d, np.arange(U))
+    rep = {}
+    for k in ("residual_out", "norm"):
+        if k not in h:
+            continue
+        within = exact = total = 0
+        worst = 0
+        for t0 in range(0, T, slice_tokens):
+            t1 = min(T, t0 + slice_tokens)
+            cls = np.arange(t0, t1) % U
+            u = ulp_diff(h[k][t0:t1], o[k][cls])
+            within += int(np.sum(u <= 1))
+            exact += int(np.sum(u == 0))
+            total += u.size
+            worst = max(worst, int(u.max()) if u.size else 0)
+        rep[k + "_within1"] = within / max(total, 1)
+        rep[k + "_exact"] = exact / max(total, 1)
+        rep[k + "_maxulp"] = worst
+        rep[k + "_elements"] = total
+        assert rep[k + "_within1"] >= ULP_FRAC, (k, rep)
+    cls = np.arange(T) % U
+    for gk, ok in (("pre_out", "pre"), ("post_out", "post"), ("comb_out", "comb")):
+        ref = o[ok][cls].reshape(h[gk].shape)
+        err = np.abs(h[gk].astype(np.float64) - ref)
+        rep[ok + "_maxerr"] = float(err.max()) if err.size else 0.0
+        assert rep[ok + "_maxerr"] <= GATE_TOL, (ok, rep)
+    if d["out_mode"] == B.MHC_OUT_MXFP8 and check_quant:
+        codes, scales = O.quant_ue8m0(h["norm"])
+        rep["codes_mismatch"] = int(np.sum(codes != h["fp8_codes"]))
+        rep["scales_mismatch"] = int(np.sum(scales != h["e8m0_scales"]))
+        assert rep["codes_mismatch"] == 0 and rep["scales_mismatch"] == 0, rep
+    if d["out_mode"] == B.MHC_OUT_FP8_GRID and check_quant:
+        grid = O.grid_ue8m0(h["norm"])
+        rep["grid_mismatch"] = int(np.sum(grid != h["fp8_codes"]))
+        assert rep["grid_mismatch"] == 0, rep
+    return rep

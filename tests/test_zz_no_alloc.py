@@ -46,12 +46,19 @@ def test_noalloc_matches_workspace_entry_two_calls_in_a_row(T, mx, post):
     g = to_dev(d)
     ref = to_host(run_gpu(d, g=g, cfg=B.MhcConfig(path=1)))
     out = B.alloc_outputs(T, 5120, d["out_mode"], "cuda")
+    _noalloc(d, g, out)  # the first call on the device resolves the scratch address
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
     for _ in range(2):
         for v in out.values():
             if v is not None and v is not out["workspace"]:
                 v.zero_()
         _noalloc(d, g, out)
+        B.mhc_noalloc_check_status()
         _close(to_host(out), ref)
+    # the calls took no device memory (cudaMalloc works in 2 MiB pages, so one would show)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
 
 
 def test_noalloc_refuses_calls_beyond_its_scratch():
@@ -64,6 +71,32 @@ def test_noalloc_refuses_calls_beyond_its_scratch():
     with pytest.raises(B.MhcError) as e:
         _noalloc(d, g, out, cfg=B.MhcConfig(path=2))
     assert e.value.code == -10
+
+
+def test_noalloc_reports_a_wait_that_ran_out():
+    # A spin limit of one makes the split path's non-finishing CTAs give up
+    # waiting: the status word in the static scratch keeps that until
+    # mhc_noalloc_check_status() reads it (later calls do not clear it), and a
+    # normal call afterwards is correct again.
+    d = make_case(8, 5120, 9300)
+    g = to_dev(d)
+    out = B.alloc_outputs(8, 5120, d["out_mode"], "cuda")
+    B.mhc_noalloc_check_status()  # start from a clear status word
+    hit = False
+    for _ in range(5):
+        _noalloc(d, g, out, cfg=B.MhcConfig(path=1, spin_limit=1))
+        _noalloc(d, g, out)       # a normal call in between leaves the record alone
+        try:
+            B.mhc_noalloc_check_status()
+        except B.MhcError as e:
+            assert e.code == -7
+            hit = True
+            break
+    assert hit
+    ref = to_host(run_gpu(d, g=g, cfg=B.MhcConfig(path=1)))
+    _noalloc(d, g, out)
+    B.mhc_noalloc_check_status()
+    _close(to_host(out), ref)
 
 
 def test_noalloc_identity_form():
