@@ -102,11 +102,23 @@ typedef struct {
     int projection;      /* streaming path's gate projection: 0 = policy (2 when H <= 5120, else 1);
                             1 = warp-level tensor-core MMA (m16n8k16) in the compute warps;
                             2 = tcgen05 MMA issued by one thread into tensor memory (H <= 5120) */
+    int wave_split;      /* streaming paths: column parts per token block of the last, partial
+                            round of blocks ("[FlyDSL] Single-launch Mega-mHC on gfx950", Kernel
+                            Architecture: the split-K fallback at the wave edge).  When the
+                            blocks left for that round are fewer than the clusters that fit,
+                            each is cut into k column parts on k clusters, whose partial
+                            sums meet in the workspace (cooperative launch: every cluster is
+                            resident).  0 = the policy picks k from an estimate of the round's
+                            time, 1 = never split, k >= 2 = k parts where they fit (at most two
+                            parts per cluster; H a multiple of 64 x cluster size) */
 } mhc_config;
 
 /* Bytes of the per-stream workspace for a call of T tokens of width H with
  * `cfg` (NULL = defaults): a status word plus, on the split path, the
- * per-CTA partial sums and the arrival counters of every token group.  One
+ * per-CTA partial sums and the arrival counters of every token group, and on
+ * the streaming paths the partial sums and counters of the split last round
+ * (776 KiB).  Where the policy's path depends on whether fn_packed is given,
+ * the size covers both.  One
  * workspace per stream whose calls can overlap on the GPU; it needs
  * mhc_workspace_init() once, after which the counters reset themselves and any
  * call (T' <= T, same H and cfg) may follow any other. */
@@ -248,6 +260,11 @@ int mhc_noalloc_check_status(void* stream);
 /* Number of kernel launches the last successful mhc_seam() on this host
  * thread issued (1 for every non-empty call). */
 int mhc_last_launch_count(void);
+
+/* Column parts per block of the partial last round in the last successful
+ * mhc_seam() or mhc_seam_unshifted() on this host thread (cfg->wave_split):
+ * 1 when that round was not split (or the call took the split path). */
+int mhc_last_wave_parts(void);
 
 /* Human-readable text of the last error on this host thread ("" if none). */
 const char* mhc_last_error_string(void);

@@ -35,7 +35,8 @@ class MhcError(RuntimeError):
 class MhcConfig(C.Structure):
     """mhc_config: zero in a field means the policy decides."""
     _fields_ = [("path", C.c_int), ("block_m", C.c_int), ("cols_per_cta", C.c_int), ("sinkhorn_iters", C.c_int),
-                ("amax_floor", C.c_float), ("spin_limit", C.c_longlong), ("projection", C.c_int)]
+                ("amax_floor", C.c_float), ("spin_limit", C.c_longlong), ("projection", C.c_int),
+                ("wave_split", C.c_int)]
 
 
 _lib = None
@@ -74,6 +75,8 @@ def lib():
         L.mhc_copy.argtypes = [P, P, C.c_size_t, P]
         L.mhc_last_launch_count.restype = I
         L.mhc_last_launch_count.argtypes = []
+        L.mhc_last_wave_parts.restype = I
+        L.mhc_last_wave_parts.argtypes = []
         L.mhc_last_error_string.restype = C.c_char_p
         L.mhc_last_error_string.argtypes = []
         _lib = L
@@ -207,6 +210,10 @@ def mhc_copy(src, dst, nbytes: int | None = None, stream=None) -> None:
 
 def mhc_last_launch_count() -> int:
     return int(lib().mhc_last_launch_count())
+
+
+def mhc_last_wave_parts() -> int:
+    return int(lib().mhc_last_wave_parts())
 
 
 def mhc_last_error_string() -> str:

@@ -21,7 +21,9 @@ cudaError_t stream_init();
 int stream_cols(int H);
 bool stream_tc_fits(int H);
 cudaError_t stream_launch(const SeamArgs& a, bool tcgen05_proj, int kcl, cudaStream_t stream,
-                          unsigned long long limit_ns, int* launches);
+                          unsigned long long report_ns, int* launches, void* wsx, int wave_split);
+size_t stream_split_bytes();
+int stream_last_parts();
 // mhc_aux.cu
 cudaError_t pack_fn_launch(const float* fn, void* out, int H, cudaStream_t s);
 cudaError_t quant_launch(const void* x, int64_t rows, int H, float floor_, uint8_t* codes, uint8_t* scales,
@@ -41,6 +43,7 @@ constexpr int64_t kStreamMinT = 1024;  // auto policy: clusters of 4 from this m
 
 thread_local std::string g_err;
 thread_local int g_launches = 0;
+thread_local int g_last_parts_api = 1;
 
 struct DeviceState {
   bool ready = false;
@@ -102,9 +105,9 @@ int next_pow2(int64_t v) {
 }
 
 // Launch policy: a pure function of (T, H, cfg, whether fn_packed is given,
-// the ordering).  Workspace sizing asks with have_packed = false, so a
-// workspace sized for the automatic policy also fits the split path it falls
-// back to without fn_packed.  The unshifted ordering takes the same paths (on
+// the ordering).  Workspace sizing asks with and without fn_packed and takes
+// the larger, so a workspace sized for the automatic policy fits whichever
+// path the call takes.  The unshifted ordering takes the same paths (on
 // the streaming path as two launches) but needs twice the split path's shared
 // memory per CTA.
 int make_plan(int64_t T, int H, const mhc_config* cfg, bool have_packed, Plan* p, bool unshifted = false) {
@@ -119,6 +122,7 @@ int make_plan(int64_t T, int H, const mhc_config* cfg, bool have_packed, Plan* p
   if (!(c.amax_floor >= 0.f) || c.amax_floor > 1e30f) return fail(MHC_ERR_CONFIG, "cfg.amax_floor out of range");
   if (c.spin_limit < 0) return fail(MHC_ERR_CONFIG, "cfg.spin_limit must be >= 0");
   if (c.projection < 0 || c.projection > 2) return fail(MHC_ERR_CONFIG, "cfg.projection must be 0, 1 or 2");
+  if (c.wave_split < 0 || c.wave_split > 64) return fail(MHC_ERR_CONFIG, "cfg.wave_split must be in [0, 64]");
   const bool stream_ok = mhc::stream_cols(H) > 0;
   p->path = c.path;
   if (p->path == 0) {  // a split-path knob (block_m, cols_per_cta) picks the split path
@@ -162,7 +166,7 @@ int make_plan(int64_t T, int H, const mhc_config* cfg, bool have_packed, Plan* p
 }
 
 size_t plan_workspace(int64_t T, int H, const Plan& p) {
-  if (p.path != 1) return kHeaderBytes;
+  if (p.path != 1) return kHeaderBytes + mhc::stream_split_bytes();  // status word + the split partial round
   const int Gh = (H + p.Wd - 1) / p.Wd;
   const int64_t groups = (T + p.BT - 1) / p.BT;
   return kHeaderBytes + mhc::split_slot_bytes(Gh, p.BT) * (size_t)(groups > 0 ? groups : 1);
@@ -181,16 +185,22 @@ bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.hi > a.l
 
 extern "C" {
 
-size_t mhc_workspace_bytes(int64_t T, int H, const mhc_config* cfg) {
-  Plan p;
-  if (T < 0 || H <= 0 || make_plan(T, H, cfg, false, &p) != MHC_OK) return kHeaderBytes;
-  return plan_workspace(T, H, p);
+// The policy may pick another path when fn_packed is given: size for both.
+static size_t workspace_for(int64_t T, int H, const mhc_config* cfg, bool unshifted) {
+  Plan p, q;
+  if (T < 0 || H <= 0 || make_plan(T, H, cfg, false, &p, unshifted) != MHC_OK) return kHeaderBytes;
+  size_t n = plan_workspace(T, H, p);
+  if (make_plan(T, H, cfg, true, &q, unshifted) == MHC_OK) {
+    const size_t m = plan_workspace(T, H, q);
+    if (m > n) n = m;
+  }
+  return n;
 }
 
+size_t mhc_workspace_bytes(int64_t T, int H, const mhc_config* cfg) { return workspace_for(T, H, cfg, false); }
+
 size_t mhc_workspace_bytes_unshifted(int64_t T, int H, const mhc_config* cfg) {
-  Plan p;
-  if (T < 0 || H <= 0 || make_plan(T, H, cfg, false, &p, true) != MHC_OK) return kHeaderBytes;
-  return plan_workspace(T, H, p);
+  return workspace_for(T, H, cfg, true);
 }
 
 int mhc_workspace_init(void* ws, size_t bytes, void* stream) {
@@ -231,6 +241,7 @@ static int seam_impl(bool unsh, const void* R, const void* Y, const float* post_
                      float* post_out, float* comb_out, void* workspace, size_t ws_bytes, const mhc_config* cfg,
                      void* stream) {
   g_launches = 0;
+  g_last_parts_api = 1;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (out_mode != MHC_OUT_BF16 && out_mode != MHC_OUT_MXFP8 && out_mode != MHC_OUT_FP8_GRID)
     return fail(MHC_ERR_CONFIG, "unknown out_mode");
@@ -334,9 +345,11 @@ static int seam_impl(bool unsh, const void* R, const void* Y, const float* post_
       a1.unshifted = 0;
     }
     cudaError_t e = mhc::stream_launch(a1, plan.tc_proj, plan.path == 3 ? 16 : 4, s,
-                                       (unsigned long long)a.spin_limit * 100ull, &launches);
+                                       (unsigned long long)a.spin_limit * 100ull, &launches,
+                                       static_cast<char*>(workspace) + kHeaderBytes, cfg ? cfg->wave_split : 0);
     if (e == cudaErrorInvalidValue) return fail(MHC_ERR_CUDA, "tensor map encoding failed (streaming path)");
     if (e != cudaSuccess) return cuda_fail(e, "seam launch (streaming path)");
+    g_last_parts_api = mhc::stream_last_parts();
     if (unsh) {  // second pass: x = sum_i pre[i] R'[i] with the fresh pre
       e = mhc::unshifted_x_launch(ident ? R : residual_out, pre_out, T, H, norm, dev->num_sms, s);
       if (e != cudaSuccess) return cuda_fail(e, "x launch (unshifted ordering)");
@@ -405,6 +418,8 @@ int mhc_copy(const void* src, void* dst, size_t bytes, void* stream) {
 }
 
 int mhc_last_launch_count(void) { return g_launches; }
+
+int mhc_last_wave_parts(void) { return g_last_parts_api; }
 
 const char* mhc_last_error_string(void) { return g_err.c_str(); }
 

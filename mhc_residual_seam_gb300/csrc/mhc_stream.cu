@@ -65,8 +65,7 @@ namespace {
 constexpr int kBM = 32;                // tokens per block
 constexpr int kChunk = 64;             // columns per chunk
 constexpr int kNF = 2, kNO = 3;
-constexpr int kComputeThreads = 256;   // warps 0-7
-// + 8 input producer, 9 MMA issuer, 10 fn producer, 11 finisher, 12 store,
+// warps 0-7 compute, 8 input producer, 9 MMA issuer, 10 fn producer, 11 finisher, 12 store,
 // and with the fp8_grid output 13-15 grid warps (warp 13 + o takes output
 // stage o).  16 warps still leave each thread 128 registers (4 warps per SM
 // sub-partition, as with 13).
@@ -222,6 +221,91 @@ __device__ __noinline__ void finish_store_gates(const SeamArgs& a, int64_t t, co
   store_gates(a, t, pre, post, cb);
 }
 
+namespace {
+
+// What one cluster works on, in order ("items").  Whole rounds first: cluster
+// cid takes blocks cid, cid + ncl, ... (nfull of them).  The last, partial
+// round of R < ncl blocks either goes whole to clusters 0 .. R-1 (k == 1), or
+// each of its blocks is cut into k column parts ("units"): unit u = p R + r is
+// part p of block r of that round and covers column groups [p G / k,
+// (p + 1) G / k) (a group is KCL adjacent 64-column chunks, one per CTA of
+// the cluster); cluster cid takes units cid, cid + ncl (at most two).  The
+// units of a block are summed through the global workspace, so a partial
+// round keeps most clusters busy instead of one block's latency on few of them
+// ("[FlyDSL] Single-launch Mega-mHC on gfx950", Kernel Architecture: the
+// split-K fallback at the wave edge).
+struct Sched {
+  int cid, ncl, block0, nfull, R, k, G;
+  __device__ __forceinline__ int nunits() const {
+    const int ku = k * R;
+    return (k > 1 && cid < ku) ? (ku - cid + ncl - 1) / ncl : 0;
+  }
+  __device__ __forceinline__ int nitems() const { return nfull + (k > 1 ? nunits() : (cid < R ? 1 : 0)); }
+  __device__ __forceinline__ bool is_unit(int i) const { return k > 1 && i >= nfull; }
+  __device__ __forceinline__ int unit(int i) const { return cid + (i - nfull) * ncl; }
+  __device__ __forceinline__ int rblk(int i) const { return unit(i) % R; }  // the unit's block in the partial round
+  __device__ __forceinline__ int block(int i) const {
+    return block0 + (i < nfull ? cid + i * ncl : nfull * ncl + (k > 1 ? rblk(i) : cid));
+  }
+  __device__ __forceinline__ int g0(int i) const { return is_unit(i) ? (unit(i) / R) * G / k : 0; }
+  __device__ __forceinline__ int g1(int i) const { return is_unit(i) ? (unit(i) / R + 1) * G / k : G; }
+  // The items normalised in a pass of their own right after compute item i
+  // (the last whole block before the units, and at the end every unit, or the
+  // last whole block): [qa, qb).  Any other item's norm is fused into the
+  // next item's chunks, which cover the same columns.
+  __device__ __forceinline__ void norm_after(int nit, int i, int& qa, int& qb) const {
+    qa = qb = 0;
+    if (i == nit - 1) {
+      qa = is_unit(i) ? nfull : i;
+      qb = nit;
+    } else if (!is_unit(i) && is_unit(i + 1)) {
+      qa = i;
+      qb = i + 1;
+    }
+  }
+  __device__ __forceinline__ bool fused(int i) const { return i > 0 && !is_unit(i); }
+};
+
+// Global workspace of the split partial round: per partial-round block r a row
+// of counters (s_x arrivals, s_x reads, one owner-arrival count per CTA rank),
+// per unit the s_x partials of each CTA and the owner CTAs' summed projections.
+constexpr int kMaxSplitBlocks = 64;
+constexpr int kMaxUnits = 128;
+constexpr int kCntStride = 32;
+constexpr size_t kSplitCntBytes = (size_t)kMaxSplitBlocks * kCntStride * 4;
+constexpr size_t kSplitSxFloats = (size_t)kMaxUnits * 16 * 32;  // [unit][rank][token]
+constexpr size_t kSplitPpFloats = (size_t)kMaxUnits * 32 * 32;  // [unit][rank * slots + slot][part]
+
+struct SplitWs {
+  unsigned* cnt;
+  float* sxp;
+  float* pp;
+  __device__ __forceinline__ SplitWs(char* w)
+      : cnt(reinterpret_cast<unsigned*>(w)),
+        sxp(reinterpret_cast<float*>(w + kSplitCntBytes)),
+        pp(reinterpret_cast<float*>(w + kSplitCntBytes) + kSplitSxFloats) {}
+};
+
+// Bounded wait for a global counter to reach `target` (acquire); the same
+// two tiers as the barrier waits.
+__device__ __forceinline__ bool wait_count(const Ctx& x, const unsigned* p, unsigned target) {
+  if (ld_acquire_gpu(p) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (ld_acquire_gpu(p) < target) {
+    if (*x.aborted) return false;
+    const uint64_t dt = globaltimer_ns() - t0;
+    if (dt > x.report_ns) report_slow(x);
+    if (dt > x.abort_ns) {
+      *x.aborted = 1;
+      return false;
+    }
+    __nanosleep(100);
+  }
+  return true;
+}
+
+}  // namespace
+
 // FORM: 0 no_post (R' = comb . R), 1 post (+ post (x) Y), 2 identity: the
 // first block's form, R' = R, no residual write.
 // OUT: 0 bf16 norm, 1 mxfp8 (+ e4m3 codes, e8m0 scales), 2 fp8_grid (+ the
@@ -233,7 +317,8 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
                        const __grid_constant__ CUtensorMap tmFn, const __grid_constant__ CUtensorMap tmN,
                        const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmGc,
                        const __grid_constant__ CUtensorMap tmGp, const __grid_constant__ CUtensorMap tmGq,
-                       int block0, int n_blocks, unsigned long long report_ns, unsigned long long abort_ns) {
+                       int block0, int n_blocks, int k_parts, char* wsx, unsigned long long report_ns,
+                       unsigned long long abort_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   using G = Geo<KCL>;
@@ -251,15 +336,30 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
   const uint32_t rank = cluster_ctarank();
   const int H = a.H;
   const int64_t T = a.T;
-  // CTA r owns the 64-column chunks r, r + 4, r + 8, ... of H: at any time the
-  // four CTAs of a cluster touch adjacent 128-byte pieces of the same rows
+  // CTA r owns the 64-column chunks r, r + KCL, r + 2 KCL, ... of H (group g
+  // holds chunks g KCL .. g KCL + KCL - 1): at any time the CTAs of a cluster
+  // touch adjacent 128-byte pieces of the same rows
   const int n64 = H / kChunk;
   const int nch = n64 > (int)rank ? (n64 - (int)rank + kCl - 1) / kCl : 0;
-  const int cid = blockIdx.x / kCl, ncl = gridDim.x / kCl;
-  // this launch's blocks are block0 .. block0 + n_blocks - 1; cluster cid takes
-  // every ncl-th of them, starting with its own index
-  const int nblk = cid < n_blocks ? (n_blocks - cid + ncl - 1) / ncl : 0;
-  const int bb = block0 + cid;
+  const int ncl = gridDim.x / kCl;
+  Sched S;
+  S.cid = blockIdx.x / kCl;
+  S.ncl = ncl;
+  S.block0 = block0;
+  S.nfull = n_blocks / ncl;
+  S.R = n_blocks - S.nfull * ncl;
+  S.k = S.R > 0 ? k_parts : 1;
+  S.G = (n64 + kCl - 1) / kCl;
+  const int nit = S.nitems();
+  // chunks of this CTA in item i (a unit covers whole groups only)
+  auto nchi = [&](int i) { return S.is_unit(i) ? S.g1(i) - S.g0(i) : nch; };
+  // first tensor-memory x slot of item i (the units of a cluster side by side)
+  auto sbase = [&](int i) {
+    int s = 0;
+    for (int q = S.nfull; q < i; ++q) s += S.g1(q) - S.g0(q);
+    return S.is_unit(i) ? s : 0;
+  };
+  const SplitWs W(wsx);
 
   if (tid == 0) {
     for (int s = 0; s < kNI; ++s) {
@@ -286,7 +386,6 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
       mbar_init(&tl->xs_full[p], 1);    // + kXsBytes of st.async from the cluster
       mbar_init(&tl->recv_full[p], 1);  // + kRecvBytes of st.async from the cluster
       mbar_init(&tl->recv_free[p], kCl);
-
       mbar_init(&tl->red_full[p], 8);
     }
     tl->reported = 0;
@@ -306,7 +405,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
     prefetch_tmap(&tmN);
     if (OUT == 1) prefetch_tmap(&tmC);
   }
-  // gamma of this CTA's first chunks, staged once (read by every block)
+  // gamma of this CTA's first chunks (groups), staged once (read by every item)
   for (int i = tid; i < min(nch, G::kGamChunks) * 8; i += kThreads)
     tl->gam[i >> 3][i & 7] = __ldg(reinterpret_cast<const uint4*>(a.gamma + ((i >> 3) * kCl + (int)rank) * kChunk) + (i & 7));
   if (warp == 9) {
@@ -329,23 +428,23 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
       const uint32_t bytes = (POST ? 5 : 4) * kRTile;
       int j = 0, ng = 0;  // input-stage loads and gate loads issued
       bool ok = true;
-      for (int lb = 0; lb < nblk && ok; ++lb) {
-        const int t0 = (bb + lb * ncl) * kBM;
-        // the block's carried gates, consumed at the top of its compute
-        if (!(ok = wait_local(X, &tl->gates_empty, (lb & 1) ^ 1))) break;
+      for (int i = 0; i < nit && ok; ++i) {
+        const int t0 = S.block(i) * kBM, gb = S.g0(i), ni = nchi(i);
+        // the item's carried gates, consumed at the top of its compute
+        if (!(ok = wait_local(X, &tl->gates_empty, (i & 1) ^ 1))) break;
         mbar_arrive_expect_tx(&tl->gates_full, (IDENT ? 4 : POST ? 24 : 20) * kBM * 4);
         if (!IDENT) tma_load_2d(&tl->gates.comb[0][0], &tmGc, &tl->gates_full, 0, t0, pol);
         tma_load_2d(&tl->gates.pre[0][0], &tmGp, &tl->gates_full, 0, t0, pol);
         if (POST) tma_load_2d(&tl->gates.post[0][0], &tmGq, &tl->gates_full, 0, t0, pol);
         ++ng;
-        for (int c = 0; c < nch; ++c, ++j) {
+        for (int c = 0; c < ni; ++c, ++j) {
           const int s = j % kNI;
           if (!(ok = wait_local(X, &tl->in_empty[s], ((j / kNI) & 1) ^ 1))) break;
           uint8_t* st = sm + kOffIn + s * kInStageF;
-          const int h = (c * kCl + (int)rank) * kChunk;
+          const int h = ((gb + c) * kCl + (int)rank) * kChunk;
           mbar_arrive_expect_tx(&tl->in_full[s], bytes);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) tma_load_3d(st + i * kRTile, &tmR, &tl->in_full[s], h, i, t0, pol);
+          for (int q = 0; q < 4; ++q) tma_load_3d(st + q * kRTile, &tmR, &tl->in_full[s], h, q, t0, pol);
           if (POST) tma_load_2d(st + 4 * kRTile, &tmY, &tl->in_full[s], h, t0, pol);
         }
       }
@@ -362,15 +461,16 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
       const uint64_t pol = l2_evict_last();
       int j = 0;
       bool ok = true;
-      for (int lb = 0; lb < nblk && ok; ++lb) {
-        for (int c = 0; c < nch; ++c, ++j) {
+      for (int i = 0; i < nit && ok; ++i) {
+        const int gb = S.g0(i), ni = nchi(i);
+        for (int c = 0; c < ni; ++c, ++j) {
           const int f = j % kNF;
           if (!(ok = wait_local(X, &tl->fn_empty[f], ((j / kNF) & 1) ^ 1))) break;
           uint8_t* st = sm + kOffFn + f * kFnStage;
-          const int h = (c * kCl + (int)rank) * kChunk;
+          const int h = ((gb + c) * kCl + (int)rank) * kChunk;
           mbar_arrive_expect_tx(&tl->fn_full[f], kFnStage);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) tma_load_3d(st + i * kFnTile, &tmFn, &tl->fn_full[f], h, i, 0, pol);
+          for (int q = 0; q < 4; ++q) tma_load_3d(st + q * kFnTile, &tmFn, &tl->fn_full[f], h, q, 0, pol);
         }
       }
       // as for the input ring: only the last load of each fn stage can still be in flight
@@ -381,20 +481,14 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
     if (!MS && lane == 0) {
       int j = 0, jr = 0;
       bool ok = true;
-      for (int lb = 0; lb <= nblk && ok; ++lb) {
-        if (lb == nblk) {  // the normalise-only pass: one stage per group of chunks, no MMA
-          for (int c0 = 0; c0 < nch; c0 += norm_group<OUT>(), ++j) {
-            if (!wait_local(X, &tl->out_full[j % kNO], (j / kNO) & 1)) break;
-            mbar_arrive(&tl->out_empty[j % kNO]);
-          }
-          break;
-        }
-        for (int c = 0; c < nch; ++c, ++j) {
+      for (int i = 0; i < nit && ok; ++i) {
+        const int ni = nchi(i);
+        for (int c = 0; c < ni; ++c, ++j) {
           const int o = j % kNO;
           const int f = jr % kNF;
           if (!(ok = wait_local(X, &tl->out_full[o], (j / kNO) & 1))) break;
-          // the first MMA of a block overwrites D: the previous block's D must have been read
-          if (c == 0 && lb > 0 && !(ok = wait_local(X, &tl->d_free, (lb - 1) & 1))) break;
+          // the first MMA of an item overwrites D: the previous item's D must have been read
+          if (c == 0 && i > 0 && !(ok = wait_local(X, &tl->d_free, (i - 1) & 1))) break;
           if (!(ok = wait_local(X, &tl->fn_full[f], (jr / kNF) & 1))) break;
           tc_fence_after();
           const uint32_t ra = smem_u32(sm + kOffOut + o * kOutStage);   // R' of the 4 streams [128 x 64]
@@ -404,8 +498,17 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
             tc_mma_bf16(tmem + kColD, sdesc_k_sw128(ra + kk * 32), sdesc_k_sw128(fb + kk * 32), kIdesc, (c | kk) != 0);
           tc_commit(&tl->fn_empty[f]);
           tc_commit(&tl->out_empty[o]);
-          if (c == nch - 1) tc_commit(&tl->d_full);
+          if (c == ni - 1) tc_commit(&tl->d_full);
           ++jr;
+        }
+        // normalise-only passes after this item: one stage per group of chunks, no MMA
+        int qa, qb;
+        S.norm_after(nit, i, qa, qb);
+        for (int q = qa; q < qb && ok; ++q) {
+          for (int c0 = 0; c0 < nchi(q); c0 += norm_group<OUT>(), ++j) {
+            if (!(ok = wait_local(X, &tl->out_full[j % kNO], (j / kNO) & 1))) break;
+            mbar_arrive(&tl->out_empty[j % kNO]);
+          }
         }
       }
       // every MMA issued (and the commits before it) completes before the CTA
@@ -440,40 +543,13 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
       }
     };
     bool ok = true;
-    for (int lb = 0; lb <= nblk && ok; ++lb) {
-      const bool real = lb < nblk, prev = lb > 0;
-      const int t0 = (bb + lb * ncl) * kBM, tp = (bb + (lb - 1) * ncl) * kBM;
-      if (!real) {  // the normalise-only pass: the norm tiles of a group of chunks per stage
-        constexpr int G = norm_group<OUT>();
-        for (int c0 = 0; c0 < nch && prev; c0 += G, ++j) {
-          const int o = j % kNO;
-          uint8_t* ost = sm + kOffOut + o * kOutStage;
-          if (!wait_warp(X, &tl->out_full[o], (j / kNO) & 1)) break;
-          const int ng = min(G, nch - c0);
-          if (OUT == 1) {  // codes tiles in stage slot 4
-            for (int g = 0; g < ng; ++g)
-              quant_tile(ost + g * kRTile, ost + kOffNormT + g * 2048, tp, ((c0 + g) * kCl + (int)rank) * kChunk);
-            fence_proxy_async_smem();
-            __syncwarp();
-          }
-          if (lane == 0) {
-            for (int g = 0; g < ng; ++g) {
-              const int h = ((c0 + g) * kCl + (int)rank) * kChunk;
-              if (store_norm) tma_store_2d(&tmN, ost + g * kRTile, h, tp);
-              if (OUT == 1) tma_store_2d(&tmC, ost + kOffNormT + g * 2048, h, tp);
-            }
-            tma_store_commit();
-            tma_store_wait_read_all();
-            mbar_arrive(&tl->out_empty[o]);
-          }
-          __syncwarp();
-        }
-        break;
-      }
-      for (int c = 0; c < nch; ++c, ++j) {
+    for (int i = 0; i < nit && ok; ++i) {
+      const bool prev = S.fused(i);
+      const int t0 = S.block(i) * kBM, tp = prev ? S.block(i - 1) * kBM : 0, gb = S.g0(i), ni = nchi(i);
+      for (int c = 0; c < ni; ++c, ++j) {
         const int o = j % kNO;
         uint8_t* ost = sm + kOffOut + o * kOutStage;
-        const int h = (c * kCl + (int)rank) * kChunk;
+        const int h = ((gb + c) * kCl + (int)rank) * kChunk;
         if (!(ok = wait_warp(X, &tl->out_full[o], (j / kNO) & 1))) break;
         if (OUT == 1 && prev) {
           quant_tile(ost + kOffNormT, ost + kOffCodesT, tp, h);
@@ -483,7 +559,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
         if (lane == 0) {
           if (!IDENT) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) tma_store_3d(&tmRo, ost + i * kRTile, h, i, t0);
+            for (int q = 0; q < 4; ++q) tma_store_3d(&tmRo, ost + q * kRTile, h, q, t0);
           }
           if (prev) {
             if (store_norm) tma_store_2d(&tmN, ost + kOffNormT, h, tp);
@@ -494,6 +570,37 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
         }
         if (lane == 0) mbar_arrive(&tl->out_empty[o]);
         __syncwarp();
+      }
+      if (!ok) break;
+      // normalise-only passes: the norm tiles of a group of chunks per stage
+      int qa, qb;
+      S.norm_after(nit, i, qa, qb);
+      constexpr int NG = norm_group<OUT>();
+      for (int q = qa; q < qb && ok; ++q) {
+        const int tq = S.block(q) * kBM, gq = S.g0(q), nq = nchi(q);
+        for (int c0 = 0; c0 < nq; c0 += NG, ++j) {
+          const int o = j % kNO;
+          uint8_t* ost = sm + kOffOut + o * kOutStage;
+          if (!(ok = wait_warp(X, &tl->out_full[o], (j / kNO) & 1))) break;
+          const int ng = min(NG, nq - c0);
+          if (OUT == 1) {  // codes tiles in stage slot 4
+            for (int g = 0; g < ng; ++g)
+              quant_tile(ost + g * kRTile, ost + kOffNormT + g * 2048, tq, ((gq + c0 + g) * kCl + (int)rank) * kChunk);
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+          if (lane == 0) {
+            for (int g = 0; g < ng; ++g) {
+              const int h = ((gq + c0 + g) * kCl + (int)rank) * kChunk;
+              if (store_norm) tma_store_2d(&tmN, ost + g * kRTile, h, tq);
+              if (OUT == 1) tma_store_2d(&tmC, ost + kOffNormT + g * 2048, h, tq);
+            }
+            tma_store_commit();
+            tma_store_wait_read_all();
+            mbar_arrive(&tl->out_empty[o]);
+          }
+          __syncwarp();
+        }
       }
     }
     // every bulk store issued has read its shared memory and written global
@@ -515,41 +622,28 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
       }
     };
     // the grid row of token tp + lane, columns h .. h + 63, straight from
-    // registers: each lane writes its own 128 contiguous bytes
-    auto store_grid = [&](int64_t tp, int h, const uint32_t* gw) {
+    // registers, one 32-group at a time: each lane writes its own 128
+    // contiguous bytes
+    auto grid_row = [&](int64_t tp, int h, const uint32_t* nb) {
       const int64_t tt = tp + lane;
-      if (tt < T) {
-        uint4* dst = reinterpret_cast<uint4*>(a.grid + tt * H + h);
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) st_stream(dst + ch, make_uint4(gw[4 * ch], gw[4 * ch + 1], gw[4 * ch + 2], gw[4 * ch + 3]));
+      for (int half = 0; half < 2; ++half) {
+        uint32_t gw[16];
+        grid_group32(nb + 16 * half, gw, a.amax_floor);
+        if (tt < T) {
+          uint4* dst = reinterpret_cast<uint4*>(a.grid + tt * H + h + 32 * half);
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) st_stream(dst + ch, make_uint4(gw[4 * ch], gw[4 * ch + 1], gw[4 * ch + 2], gw[4 * ch + 3]));
+        }
       }
     };
     int j = 0;
     bool ok = true;
-    for (int lb = 0; lb <= nblk && ok; ++lb) {
-      const bool real = lb < nblk, prev = lb > 0;
-      const int64_t tp = (int64_t)(bb + (lb - 1) * ncl) * kBM;
-      if (!real) {  // the normalise-only pass: the norm tiles of a group of chunks per stage
-        constexpr int G = norm_group<OUT>();
-        for (int c0 = 0; c0 < nch && prev; c0 += G, ++j) {
-          const int o = j % kNO;
-          if (o != me) continue;
-          const uint8_t* ost = sm + kOffOut + o * kOutStage;
-          if (!wait_warp(X, &tl->out_full[o], (j / kNO) & 1)) break;
-          const int ng = min(G, nch - c0);
-          for (int g = 0; g < ng; ++g) {
-            uint32_t nb[32], gw[32];
-            load_row(ost + g * kRTile, nb);
-            __syncwarp();
-            if (g == ng - 1 && lane == 0) mbar_arrive(&tl->out_empty[o]);
-            grid_group32(nb, gw, a.amax_floor);
-            grid_group32(nb + 16, gw + 16, a.amax_floor);
-            store_grid(tp, ((c0 + g) * kCl + (int)rank) * kChunk, gw);
-          }
-        }
-        break;
-      }
-      for (int c = 0; c < nch; ++c, ++j) {
+    for (int i = 0; i < nit && ok; ++i) {
+      const bool prev = S.fused(i);
+      const int64_t tp = prev ? (int64_t)S.block(i - 1) * kBM : 0;
+      const int gb = S.g0(i), ni = nchi(i);
+      for (int c = 0; c < ni; ++c, ++j) {
         const int o = j % kNO;
         if (o != me) continue;
         const uint8_t* ost = sm + kOffOut + o * kOutStage;
@@ -558,34 +652,62 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
         if (prev) load_row(ost + kOffNormT, nb);
         __syncwarp();
         if (lane == 0) mbar_arrive(&tl->out_empty[o]);
-        if (prev) {
-          uint32_t gw[32];
-          grid_group32(nb, gw, a.amax_floor);
-          grid_group32(nb + 16, gw + 16, a.amax_floor);
-          store_grid(tp, (c * kCl + (int)rank) * kChunk, gw);
+        if (prev) grid_row(tp, ((gb + c) * kCl + (int)rank) * kChunk, nb);
+      }
+      if (!ok) break;
+      // normalise-only passes: the norm tiles of a group of chunks per stage
+      int qa, qb;
+      S.norm_after(nit, i, qa, qb);
+      constexpr int NG = norm_group<OUT>();
+      for (int q = qa; q < qb && ok; ++q) {
+        const int64_t tq = (int64_t)S.block(q) * kBM;
+        const int gq = S.g0(q), nq = nchi(q);
+        for (int c0 = 0; c0 < nq; c0 += NG, ++j) {
+          const int o = j % kNO;
+          if (o != me) continue;
+          const uint8_t* ost = sm + kOffOut + o * kOutStage;
+          if (!(ok = wait_warp(X, &tl->out_full[o], (j / kNO) & 1))) break;
+          const int ng = min(NG, nq - c0);
+          for (int g = 0; g < ng; ++g) {
+            uint32_t nb[32];
+            load_row(ost + g * kRTile, nb);
+            __syncwarp();
+            if (g == ng - 1 && lane == 0) mbar_arrive(&tl->out_empty[o]);
+            grid_row(tq, ((gq + c0 + g) * kCl + (int)rank) * kChunk, nb);
+          }
         }
       }
     }
   } else if (warp == 11) {
     // ------------------------------------ exchange and gate finish warp --
-    // Per block: (1) this CTA's s_x partials to every CTA of the cluster (each
+    // Per item: (1) this CTA's s_x partials to every CTA of the cluster (each
     // forms rstd_x itself), (2) the 24 projections and s_R of each token to
-    // its owner CTA (token % 4), (3) the gates of the 8 tokens this CTA owns.
+    // its owner CTA (token % KCL), (3) the gates of the tokens this CTA owns.
     // Sends are st.async completing bytes on the receiver's mbarrier; the
     // compute warps only hand their partials over and go on.  recv_free keeps
-    // the partials of block lb + 2 out of a slot until every owner has read
-    // block lb from it.
+    // the partials of item i + 2 out of a slot until every owner has read
+    // item i from it.  A unit (a column part of a block) also publishes its
+    // s_x partials and its owners' sums in the global workspace; the owner
+    // that completes a block's parts last finishes its tokens' gates.
     if (lane < 27) tl->ab[lane] = lane < 3 ? a.alpha[lane] : a.bias[lane - 3];
     __syncwarp();
-    for (int lb = 0; lb < nblk; ++lb) {
-      const int b = bb + lb * ncl, par = lb & 1;
-      if (!wait_warp(X, &tl->red_full[par], (lb >> 1) & 1)) break;
+    for (int i = 0; i < nit; ++i) {
+      const int b = S.block(i), par = i & 1;
+      const bool unit = S.is_unit(i);
+      if (!wait_warp(X, &tl->red_full[par], (i >> 1) & 1)) break;
       float sx = 0.f, sR = 0.f;
 #pragma unroll
       for (int w = 0; w < 8; ++w) {
         const float2 v = tl->red[par][w][lane];
         sR += v.x;
         sx += v.y;
+      }
+      if (unit) {  // this CTA's s_x partials of the unit, for every part's rstd_x
+        const int u = S.unit(i), r = S.rblk(i);
+        W.sxp[(u * kCl + (int)rank) * 32 + lane] = sx;
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(&W.cnt[r * kCntStride], 1u);
       }
       if (lane == 0) mbar_arrive_expect_tx(&tl->xs_full[par], kXsBytes);
       {
@@ -594,8 +716,8 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
         for (int dst = 0; dst < kCl; ++dst)
           st_async_f32(mapa_shared(xa, (uint32_t)dst), sx, mapa_shared(xb, (uint32_t)dst));
       }
-      if (!wait_warp(X, &tl->dbuf_full, lb & 1)) break;
-      if (lb >= 2 && !wait_warp_remote(X, &tl->recv_free[par], ((lb >> 1) & 1) ^ 1)) break;
+      if (!wait_warp(X, &tl->dbuf_full, i & 1)) break;
+      if (i >= 2 && !wait_warp_remote(X, &tl->recv_free[par], ((i >> 1) & 1) ^ 1)) break;
       {
         const uint32_t dst = (uint32_t)(lane % kCl);
         const uint32_t ra = mapa_shared(smem_u32(&tl->recv[par][rank][lane / kCl][0]), dst);
@@ -616,10 +738,10 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
       if (lane == 0) mbar_arrive(&tl->dbuf_free);
 
       if (lane == 0) mbar_arrive_expect_tx(&tl->recv_full[par], kRecvBytes);
-      if (!wait_warp(X, &tl->recv_full[par], (lb >> 1) & 1)) break;
+      if (!wait_warp(X, &tl->recv_full[par], (i >> 1) & 1)) break;
       // sums over the cluster, one (owned token, part) pair per lane and round
-      for (int i = lane; i < kSlots * kOwnerParts; i += 32) {
-        const int sl = i / kOwnerParts, k = i - sl * kOwnerParts;
+      for (int e = lane; e < kSlots * kOwnerParts; e += 32) {
+        const int sl = e / kOwnerParts, k = e - sl * kOwnerParts;
         float s = 0.f;
 #pragma unroll
         for (int src = 0; src < kCl; ++src) s += tl->recv[par][src][sl][k];
@@ -627,18 +749,55 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
       }
       __syncwarp();
       if (lane < kCl) mbar_arrive_remote(mapa_shared(smem_u32(&tl->recv_free[par]), lane));
-      if (lane < kSlots) {
-        const int64_t tt = (int64_t)b * kBM + (int)rank + kCl * lane;
-        if (tt < T) finish_store_gates(a, tt, &tl->pbuf[lane][0], tl->ab, H);
+      if (!unit) {
+        if (lane < kSlots) {
+          const int64_t tt = (int64_t)b * kBM + (int)rank + kCl * lane;
+          if (tt < T) finish_store_gates(a, tt, &tl->pbuf[lane][0], tl->ab, H);
+        }
+      } else {
+        // publish this owner's sums of the unit; the owner completing the
+        // block's k parts last adds them (parts in order, so the result does
+        // not depend on who is last) and finishes its tokens' gates
+        const int u = S.unit(i), r = S.rblk(i);
+        for (int e = lane; e < kSlots * kOwnerParts; e += 32) {
+          const int sl = e / kOwnerParts, k = e - sl * kOwnerParts;
+          W.pp[((size_t)u * 32 + (int)rank * kSlots + sl) * 32 + k] = tl->pbuf[sl][k];
+        }
+        __threadfence();
+        __syncwarp();
+        unsigned old = 0;
+        if (lane == 0) old = atom_add_acq_rel_gpu(&W.cnt[r * kCntStride + 2 + (int)rank], 1u);
+        old = __shfl_sync(0xffffffffu, old, 0);
+        if (old == (unsigned)S.k - 1) {
+          (void)ld_acquire_gpu(&W.cnt[r * kCntStride + 2 + (int)rank]);
+          for (int e = lane; e < kSlots * kOwnerParts; e += 32) {
+            const int sl = e / kOwnerParts, k = e - sl * kOwnerParts;
+            float s = 0.f;
+            for (int p = 0; p < S.k; ++p)
+              s += __ldcg(&W.pp[((size_t)(p * S.R + r) * 32 + (int)rank * kSlots + sl) * 32 + k]);
+            tl->pbuf[sl][k] = s;
+          }
+          __syncwarp();
+          if (lane < kSlots) {
+            const int64_t tt = (int64_t)b * kBM + (int)rank + kCl * lane;
+            if (tt < T) finish_store_gates(a, tt, &tl->pbuf[lane][0], tl->ab, H);
+          }
+          if (lane == 0) W.cnt[r * kCntStride + 2 + (int)rank] = 0;  // every part has arrived: reset for the next call
+        }
       }
       __syncwarp();
     }
   } else if (warp < 8) {
     // ---------------------------------------------------- compute warps --
-    const int q = warp & 3, wq = warp >> 2;
+    const int q4 = warp & 3, wq = warp >> 2;
     const uint32_t colx = MS ? 0u : kDCols;
-    const uint32_t xaddr = tmem + ((uint32_t)(32 * q) << 16) + colx + 8 * wq;
+    const uint32_t xaddr = tmem + ((uint32_t)(32 * q4) << 16) + colx + 8 * wq;
     const uint32_t off = lane * 128 + ((warp ^ (lane & 7)) << 4);  // row = token, 16-byte chunk = warp
+    // gamma of the 8 columns of this warp in chunk c of group g
+    auto gamma8 = [&](int g) -> uint4 {
+      return g < G::kGamChunks ? tl->gam[g][warp]
+                               : __ldg(reinterpret_cast<const uint4*>(a.gamma + (g * kCl + (int)rank) * kChunk + 8 * warp));
+    };
     // Warp-level projection (MS): warp w owns stream w % 4 and the 32 columns
     // [32 (w / 4), +32) of every chunk: D[32 tokens x 24 logits] += R'[32 x 32]
     // . (fn_hi + fn_lo)[32 x 24], m16n8k16 MMAs with fp32 accumulation, one
@@ -685,29 +844,46 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
       return true;
     };
 
-
     float rprev = 0.f;
-    // rstd_x of block lbp from the s_x partials the four CTAs sent (same sum
-    // order in every CTA, so all four hold the same value)
-    auto take_rstd = [&](int lbp) -> bool {
-      const int pp = lbp & 1;
-      if (!wait_warp(X, &tl->xs_full[pp], (lbp >> 1) & 1)) return false;
+    // rstd_x of item q from the s_x partials the CTAs of the cluster sent (same
+    // sum order in every CTA, so all hold the same value); for a unit, from the
+    // partials every CTA of every part of its block published
+    auto take_rstd = [&](int q) -> bool {
+      const int pp = q & 1;
+      if (!wait_warp(X, &tl->xs_full[pp], (q >> 1) & 1)) return false;
       float sx = 0.f;
 #pragma unroll
       for (int src = 0; src < kCl; ++src) sx += tl->xs[pp][src][lane];
-      const int64_t tt = (int64_t)(bb + lbp * ncl) * kBM + lane;
+      if (S.is_unit(q)) {
+        const int r = S.rblk(q);
+        const unsigned target = (unsigned)(S.k * kCl);
+        if (!__all_sync(0xffffffffu, wait_count(X, &W.cnt[r * kCntStride], target))) return false;
+        sx = 0.f;
+        for (int p = 0; p < S.k; ++p)
+#pragma unroll
+          for (int src = 0; src < kCl; ++src) sx += __ldcg(&W.sxp[((p * S.R + r) * kCl + src) * 32 + lane]);
+        __syncwarp();
+        if (lane == 0) {  // the last of the block's readers resets its counters for the next call
+          const unsigned old = atomicAdd(&W.cnt[r * kCntStride + 1], 1u);
+          if (old == target * 8 - 1) {
+            W.cnt[r * kCntStride] = 0;
+            W.cnt[r * kCntStride + 1] = 0;
+          }
+        }
+      }
+      const int64_t tt = (int64_t)S.block(q) * kBM + lane;
       rprev = tt < T ? 1.0f / sqrtf(sx / (float)H + a.eps) : 0.f;
       return true;
     };
 
-    // tcgen05 projection: warp q reads stream q's diagonal block of block
-    // lbp's D (TMEM lanes 32 q .., columns 48 q .. 48 q + 47) during the next
-    // block's first chunk, frees D for that block's MMAs, and hands the
+    // tcgen05 projection: warp q4 reads stream q4's diagonal block of item
+    // ip's D (TMEM lanes 32 q4 .., columns 48 q4 .. 48 q4 + 47) during the
+    // next item's first chunk, frees D for that item's MMAs, and hands the
     // hi + lo sums to the exchange warp through dbuf.
-    auto read_d = [&](int lbp) -> bool {
+    auto read_d = [&](int ip) -> bool {
       float dv[48];
-      if (nch > 0) {
-        if (!wait_warp(X, &tl->d_full, lbp & 1)) return false;
+      if (nchi(ip) > 0) {
+        if (!wait_warp(X, &tl->d_full, ip & 1)) return false;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 6; ++k)
@@ -719,7 +895,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tl->d_free);
-      if (!wait_warp(X, &tl->dbuf_free, (lbp & 1) ^ 1)) return false;
+      if (!wait_warp(X, &tl->dbuf_free, (ip & 1) ^ 1)) return false;
       float* r0 = &tl->dbuf[warp][lane][0];
 #pragma unroll
       for (int k = 0; k < 24; ++k) r0[k] = dv[k] + dv[24 + k];
@@ -730,53 +906,16 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
 
     int j = 0, ji = 0;
     bool ok = true;
-    for (int lb = 0; lb <= nblk && ok; ++lb) {  // the last pass only normalises the last block
-      const bool real = lb < nblk, prev = lb > 0;
-      if (!real) {  // the normalise-only pass: the norm tiles of a group of chunks per output stage
-        if (prev && take_rstd(lb - 1)) {
-          constexpr int NG = norm_group<OUT>();
-          for (int c0 = 0; c0 < nch; c0 += NG, ++j) {
-            const int o = j % kNO;
-            if (!wait_warp(X, &tl->out_empty[o], ((j / kNO) & 1) ^ 1)) break;
-            uint8_t* ost = sm + kOffOut + o * kOutStage;
-            const int ng = min(NG, nch - c0);
-            for (int g = 0; g < ng; ++g) {
-              const int c = c0 + g;
-              uint32_t xr[8];
-              tc_ld_x8_issue(xaddr + 16 * c, xr);
-              const uint4 gv = c < G::kGamChunks
-                                   ? tl->gam[c][warp]
-                                   : __ldg(reinterpret_cast<const uint4*>(a.gamma + (c * kCl + (int)rank) * kChunk + 8 * warp));
-              tc_wait_ld_x8(xr);
-              float xv[8], gm[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) xv[e] = __uint_as_float(xr[e]);
-              unpack8(gv, gm);
-              uint4 nv;
-              nv.x = pack_bf16x2(xv[0] * rprev * gm[0], xv[1] * rprev * gm[1]);
-              nv.y = pack_bf16x2(xv[2] * rprev * gm[2], xv[3] * rprev * gm[3]);
-              nv.z = pack_bf16x2(xv[4] * rprev * gm[4], xv[5] * rprev * gm[5]);
-              nv.w = pack_bf16x2(xv[6] * rprev * gm[6], xv[7] * rprev * gm[7]);
-              *reinterpret_cast<uint4*>(ost + g * kRTile + off) = nv;
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tl->out_full[o]);
-            if (MS) {  // the warp-level projection warps count in the stage's release
-              __syncwarp();
-              if (lane == 0 && warp < 8) mbar_arrive(&tl->out_empty[o]);
-            }
-          }
-        }
-        break;
-      }
+    for (int i = 0; i < nit && ok; ++i) {
+      const bool prev = S.fused(i);  // this item's chunks normalise the previous item's x (same columns)
+      const int ni = nchi(i), gb = S.g0(i), sb = sbase(i);
       float2 comb2[16], post2[4], pre2[4];  // each gate duplicated for the fp32x2 FMAs
       {
         float4 gc[4], gp = make_float4(0.f, 0.f, 0.f, 0.f), gq = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < 4; ++k) gc[k] = gp;
         {  // rows past T arrive as zeros
-          if (!(ok = wait_warp(X, &tl->gates_full, lb & 1))) break;
+          if (!(ok = wait_warp(X, &tl->gates_full, i & 1))) break;
           const GateTile& gt = tl->gates;
           if (!IDENT) {
 #pragma unroll
@@ -805,18 +944,17 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc[m][n][e] = 0.f;
 
-      for (int c = 0; c < nch; ++c, ++j) {
+      for (int c = 0; c < ni; ++c, ++j) {
         const int o = j % kNO;
         uint32_t ow[4][4];
         float x[8];
-        // the previous block's x and gamma of these columns, fetched now so
+        // the previous item's x and gamma of these columns, fetched now so
         // their latency hides behind this chunk's post-mix
         uint32_t xr[8];
         uint4 gv = make_uint4(0, 0, 0, 0);
         if (prev) {
           tc_ld_x8_issue(xaddr + 16 * c, xr);
-          gv = c < G::kGamChunks ? tl->gam[c][warp]
-                                : __ldg(reinterpret_cast<const uint4*>(a.gamma + (c * kCl + (int)rank) * kChunk + 8 * warp));
+          gv = gamma8(gb + c);
         }
         {
           const int s = ji % kNI;
@@ -824,7 +962,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
           const uint8_t* st = sm + kOffIn + s * kInStageF;
           uint4 rin[4], yin = make_uint4(0, 0, 0, 0);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) rin[i] = *reinterpret_cast<const uint4*>(st + i * kRTile + off);
+          for (int q = 0; q < 4; ++q) rin[q] = *reinterpret_cast<const uint4*>(st + q * kRTile + off);
           if (POST) yin = *reinterpret_cast<const uint4*>(st + 4 * kRTile + off);
           __syncwarp();
           if (lane == 0) mbar_arrive(&tl->in_empty[s]);
@@ -837,35 +975,35 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
             const float2 yy = bf16pair((&yin.x)[wd]);
             float2 xx = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int q = 0; q < 4; ++q) {
               uint32_t w;
               if (IDENT) {
-                w = (&rin[i].x)[wd];  // R' = R, bit for bit
+                w = (&rin[q].x)[wd];  // R' = R, bit for bit
               } else {
-                float2 v = __fmul2_rn(comb2[4 * i], r0);
-                v = __ffma2_rn(comb2[4 * i + 1], r1, v);
-                v = __ffma2_rn(comb2[4 * i + 2], r2, v);
-                v = __ffma2_rn(comb2[4 * i + 3], r3, v);
-                if (POST) v = __ffma2_rn(post2[i], yy, v);
+                float2 v = __fmul2_rn(comb2[4 * q], r0);
+                v = __ffma2_rn(comb2[4 * q + 1], r1, v);
+                v = __ffma2_rn(comb2[4 * q + 2], r2, v);
+                v = __ffma2_rn(comb2[4 * q + 3], r3, v);
+                if (POST) v = __ffma2_rn(post2[q], yy, v);
                 w = pack_bf16x2(v.x, v.y);
               }
-              ow[i][wd] = w;
+              ow[q][wd] = w;
               const float2 rr2 = bf16pair(w);
               sR2 = __ffma2_rn(rr2, rr2, sR2);
-              xx = __ffma2_rn(pre2[i], rr2, xx);
+              xx = __ffma2_rn(pre2[q], rr2, xx);
             }
             x[2 * wd] = xx.x;
             x[2 * wd + 1] = xx.y;
             sx2 = __ffma2_rn(xx, xx, sx2);
           }
         }
-        if (prev && c == 0 && !(ok = take_rstd(lb - 1))) break;
+        if (prev && c == 0 && !(ok = take_rstd(i - 1))) break;
         if (!(ok = wait_warp(X, &tl->out_empty[o], ((j / kNO) & 1) ^ 1))) break;
         uint8_t* ost = sm + kOffOut + o * kOutStage;
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          *reinterpret_cast<uint4*>(ost + i * kRTile + off) = make_uint4(ow[i][0], ow[i][1], ow[i][2], ow[i][3]);
-        if (prev) {  // norm of the previous block's x in these columns, before x is overwritten
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<uint4*>(ost + q * kRTile + off) = make_uint4(ow[q][0], ow[q][1], ow[q][2], ow[q][3]);
+        if (prev) {  // norm of the previous item's x in these columns, before x is overwritten
           float xv[8], gm[8];
           tc_wait_ld_x8(xr);
 #pragma unroll
@@ -878,32 +1016,32 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
           nv.w = pack_bf16x2(xv[6] * rprev * gm[6], xv[7] * rprev * gm[7]);
           *reinterpret_cast<uint4*>(ost + kOffNormT + off) = nv;
         }
-        tc_st_x8(xaddr + 16 * c, x);
+        tc_st_x8(xaddr + 16 * (sb + c), x);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tl->out_full[o]);
-        if (!MS && prev && c == 0 && warp < 4 && !(ok = read_d(lb - 1))) break;
+        if (!MS && i > 0 && c == 0 && warp < 4 && !(ok = read_d(i - 1))) break;
         if (MS && c > 0 && !(ok = mma_chunk(j - 1, ji - 2))) break;
       }
       if (!ok) break;
-      if (prev && nch == 0) {  // no columns here: only consume the phases
-        if (!(ok = take_rstd(lb - 1))) break;
-        if (!MS && warp < 4 && !(ok = read_d(lb - 1))) break;
+      if (i > 0 && ni == 0) {  // no columns here: only consume the phases
+        if (prev && !(ok = take_rstd(i - 1))) break;
+        if (!MS && warp < 4 && !(ok = read_d(i - 1))) break;
       }
-      if (MS && nch > 0 && !(ok = mma_chunk(j - 1, ji - 1))) break;
+      if (MS && ni > 0 && !(ok = mma_chunk(j - 1, ji - 1))) break;
       tc_wait_st();
 
-      // ------------ block finish: hand the partials to the exchange warp --
-      const int par = lb & 1;
+      // ------------- item finish: hand the partials to the exchange warp --
+      const int par = i & 1;
       tl->red[par][warp][lane] = make_float2(sR2.x + sR2.y, sx2.x + sx2.y);
       __syncwarp();
       if (lane == 0) mbar_arrive(&tl->red_full[par]);
-      // no MMA follows the last block: its D is read now, not in the normalise-only pass
-      if (!MS && lb == nblk - 1 && warp < 4 && !(ok = read_d(lb))) break;
+      // no MMA follows the last item: its D is read now
+      if (!MS && i == nit - 1 && warp < 4 && !(ok = read_d(i))) break;
       if (MS) {  // warps w and w + 4 both hold stream w % 4: fold them into dbuf[w % 4]
         const int g = lane >> 2, t4 = lane & 3;
         if (warp >= 4) {
-          if (!(ok = wait_warp(X, &tl->dbuf_free, (lb & 1) ^ 1))) break;
+          if (!(ok = wait_warp(X, &tl->dbuf_free, (i & 1) ^ 1))) break;
 #pragma unroll
           for (int m = 0; m < 2; ++m) {
 #pragma unroll
@@ -918,7 +1056,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&tl->fold_full);
         } else {
-          if (!(ok = wait_warp(X, &tl->fold_full, lb & 1))) break;
+          if (!(ok = wait_warp(X, &tl->fold_full, i & 1))) break;
 #pragma unroll
           for (int m = 0; m < 2; ++m) {
 #pragma unroll
@@ -932,6 +1070,47 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&tl->dbuf_full);
+        }
+      }
+
+      // ------------- normalise-only passes: the norm tiles of a group of
+      // chunks per output stage (the last whole block before the units, and
+      // at the end every unit or the last whole block)
+      int qa, qb;
+      S.norm_after(nit, i, qa, qb);
+      constexpr int NG = norm_group<OUT>();
+      for (int q = qa; q < qb && ok; ++q) {
+        if (!(ok = take_rstd(q))) break;
+        const int nq = nchi(q), gq = S.g0(q), sq = sbase(q);
+        for (int c0 = 0; c0 < nq; c0 += NG, ++j) {
+          const int o = j % kNO;
+          if (!(ok = wait_warp(X, &tl->out_empty[o], ((j / kNO) & 1) ^ 1))) break;
+          uint8_t* ost = sm + kOffOut + o * kOutStage;
+          const int ng = min(NG, nq - c0);
+          for (int g = 0; g < ng; ++g) {
+            const int c = c0 + g;
+            uint32_t xr[8];
+            tc_ld_x8_issue(xaddr + 16 * (sq + c), xr);
+            const uint4 gv = gamma8(gq + c);
+            tc_wait_ld_x8(xr);
+            float xv[8], gm[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xv[e] = __uint_as_float(xr[e]);
+            unpack8(gv, gm);
+            uint4 nv;
+            nv.x = pack_bf16x2(xv[0] * rprev * gm[0], xv[1] * rprev * gm[1]);
+            nv.y = pack_bf16x2(xv[2] * rprev * gm[2], xv[3] * rprev * gm[3]);
+            nv.z = pack_bf16x2(xv[4] * rprev * gm[4], xv[5] * rprev * gm[5]);
+            nv.w = pack_bf16x2(xv[6] * rprev * gm[6], xv[7] * rprev * gm[7]);
+            *reinterpret_cast<uint4*>(ost + g * kRTile + off) = nv;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tl->out_full[o]);
+          if (MS) {  // the warp-level projection warps count in the stage's release
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tl->out_empty[o]);
+          }
         }
       }
     }
@@ -1057,19 +1236,68 @@ static int max_clusters(int form, int out, bool ms, int kcl) {
   return n;
 }
 
+// Column parts per block of the last streaming launch's partial round on this
+// host thread (1: no split).
+thread_local int g_last_parts = 1;
+int stream_last_parts() { return g_last_parts; }
+
+// Bytes of the global workspace the split partial round uses (after the
+// status header of the caller's workspace).
+size_t stream_split_bytes() { return kSplitCntBytes + (kSplitSxFloats + kSplitPpFloats) * sizeof(float); }
+
+// Column parts per block of the partial last round (1: no split).  A block
+// takes about G chunk steps per CTA (G column groups); cut into k parts, the
+// partial round takes ceil(k R / ncl) units of ceil(G / k) chunks on its
+// busiest cluster, plus the fixed cost of a part (an extra normalise-only
+// pass, the global exchange and its wait), counted as kSplitCostChunks chunk
+// steps.  At most two units per cluster (the two-deep exchange buffers), all
+// units' x in tensor memory at once, whole column groups only.  `force`: 0 the
+// estimate decides, 1 never split, k >= 2 that many parts where it fits.
+constexpr int kSplitCostChunks = 3;
+static int wave_parts(int n_blocks, int ncl, int n64, int kcl, bool tc_proj, int force) {
+  if (force == 1 || n64 % kcl != 0 || ncl <= 0) return 1;
+  const int G = n64 / kcl, R = n_blocks % ncl;
+  if (R == 0 || G < 2 || R > kMaxSplitBlocks) return 1;
+  const int cap = tc_proj ? kMaxChunksTC : kMaxChunks;
+  auto fits = [&](int k) {
+    const int per = (k * R + ncl - 1) / ncl;
+    return k * R <= 2 * ncl && k * R <= kMaxUnits && per * ((G + k - 1) / k) <= cap;
+  };
+  if (force >= 2) {
+    for (int k = force < G ? force : G; k >= 2; --k)
+      if (fits(k)) return k;
+    return 1;
+  }
+  int best_k = 1, best = G;
+  for (int k = 2; k <= G; ++k) {
+    if (!fits(k)) continue;
+    const int per = (k * R + ncl - 1) / ncl;
+    const int est = per * ((G + k - 1) / k) + kSplitCostChunks;
+    if (est < best) {
+      best = est;
+      best_k = k;
+    }
+  }
+  return best_k;
+}
+
 static cudaError_t launch_with_maps(const SeamArgs& a, const CUtensorMap* m, bool tcgen05_proj, int kcl,
-                                    cudaStream_t stream, unsigned long long report_ns, int* launches);
+                                    cudaStream_t stream, unsigned long long report_ns, int* launches, void* wsx,
+                                    int wave_split);
 static cudaError_t launch_range(const SeamArgs& a, const CUtensorMap* m, bool tcgen05_proj, int kcl, int block0,
-                                int n_blocks, cudaStream_t stream, unsigned long long report_ns, int* launches);
+                                int n_blocks, cudaStream_t stream, unsigned long long report_ns, int* launches,
+                                void* wsx, int wave_split);
 
 // Returns cudaSuccess, or cudaErrorInvalidValue when a tensor map cannot be
 // encoded or no cluster fits (the caller reports it).  kcl: CTAs per cluster
 // (4, or 16 with the tcgen05 projection).
 // report_ns: a device wait longer than this sets status bit 1 and goes on; a
 // wait one second longer than that abandons the call (the kernel stops issuing
-// work, drains what is in flight and returns).
+// work, drains what is in flight and returns).  wsx: stream_split_bytes() of
+// zeroed device memory (counters reset themselves after each call).
+// wave_split: parts per block of the partial last round (0 policy, 1 none).
 cudaError_t stream_launch(const SeamArgs& a, bool tcgen05_proj, int kcl, cudaStream_t stream,
-                          unsigned long long report_ns, int* launches) {
+                          unsigned long long report_ns, int* launches, void* wsx, int wave_split) {
   const int H = a.H;
   if (stream_cols(H) == 0 || (kcl != 4 && kcl != 16) || (kcl == 16 && !tcgen05_proj)) return cudaErrorInvalidValue;
   const cuuint64_t T = (cuuint64_t)a.T;
@@ -1093,7 +1321,7 @@ cudaError_t stream_launch(const SeamArgs& a, bool tcgen05_proj, int kcl, cudaStr
   for (const MapSet& c : cache) {
     bool hit = c.T == a.T && c.H == H && c.out == out_mode;
     for (int i = 0; hit && i < 9; ++i) hit = c.key[i] == key[i];
-    if (hit) return launch_with_maps(a, c.m, tcgen05_proj, kcl, stream, report_ns, launches);
+    if (hit) return launch_with_maps(a, c.m, tcgen05_proj, kcl, stream, report_ns, launches, wsx, wave_split);
   }
   CUtensorMap mR, mY, mRo, mFn, mN, mC;
   const cuuint64_t d3[3] = {(cuuint64_t)H, 4, T};
@@ -1141,19 +1369,22 @@ cudaError_t stream_launch(const SeamArgs& a, bool tcgen05_proj, int kcl, cudaStr
   for (int i = 0; i < 9; ++i) c.key[i] = key[i];
   c.m[0] = mR; c.m[1] = mY; c.m[2] = mRo; c.m[3] = mFn; c.m[4] = mN; c.m[5] = mC; c.m[6] = mGc; c.m[7] = mGp;
   c.m[8] = mGq;
-  return launch_with_maps(a, c.m, tcgen05_proj, kcl, stream, report_ns, launches);
+  return launch_with_maps(a, c.m, tcgen05_proj, kcl, stream, report_ns, launches, wsx, wave_split);
 }
 
 // One seam call, one launch.  (Running a partial last round as a second
-// launch over larger clusters was measured slower than the partial round.)
+// launch over larger clusters was measured slower than the partial round; the
+// column split of that round runs inside the one launch.)
 static cudaError_t launch_with_maps(const SeamArgs& a, const CUtensorMap* m, bool tcgen05_proj, int kcl,
-                                    cudaStream_t stream, unsigned long long report_ns, int* launches) {
+                                    cudaStream_t stream, unsigned long long report_ns, int* launches, void* wsx,
+                                    int wave_split) {
   const int n_blocks = (int)((a.T + kBM - 1) / kBM);
-  return launch_range(a, m, tcgen05_proj, kcl, 0, n_blocks, stream, report_ns, launches);
+  return launch_range(a, m, tcgen05_proj, kcl, 0, n_blocks, stream, report_ns, launches, wsx, wave_split);
 }
 
 static cudaError_t launch_range(const SeamArgs& a, const CUtensorMap* m, bool tcgen05_proj, int kcl, int block0,
-                                int n_blocks, cudaStream_t stream, unsigned long long report_ns, int* launches) {
+                                int n_blocks, cudaStream_t stream, unsigned long long report_ns, int* launches,
+                                void* wsx, int wave_split) {
   const bool ms = !tcgen05_proj;
   unsigned long long abort_ns = report_ns + 1000000000ull;
   const int form = a.comb_prev == nullptr ? 2 : a.Y != nullptr ? 1 : 0;
@@ -1162,25 +1393,35 @@ static cudaError_t launch_range(const SeamArgs& a, const CUtensorMap* m, bool tc
   const int fit = max_clusters(form, mx, ms, kcl);
   if (fit <= 0) return cudaErrorInvalidValue;
   const int ncl = n_blocks < fit ? n_blocks : fit;
+  int parts = wsx ? wave_parts(n_blocks, ncl, a.H / kChunk, kcl, tcgen05_proj, wave_split) : 1;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)kcl;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // The parts of a split block wait for each other's partial sums: every
+  // cluster of the grid must be resident at once, which a cooperative launch
+  // guarantees (the grid is at most the clusters that fit).
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
   cfg.gridDim = dim3((unsigned)(ncl * kcl), 1, 1);
   cfg.blockDim = dim3(mx == 2 ? threads_of<2>() : threads_of<0>(), 1, 1);
   cfg.dynamicSmemBytes = smem_bytes(kcl);
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = parts > 1 ? 2 : 1;
   int b0 = block0, nb = n_blocks;
+  char* w = static_cast<char*>(wsx);
   void* args[] = {const_cast<SeamArgs*>(&a),    const_cast<CUtensorMap*>(m),     const_cast<CUtensorMap*>(m + 1),
                   const_cast<CUtensorMap*>(m + 2), const_cast<CUtensorMap*>(m + 3), const_cast<CUtensorMap*>(m + 4),
                   const_cast<CUtensorMap*>(m + 5), const_cast<CUtensorMap*>(m + 6), const_cast<CUtensorMap*>(m + 7),
-                  const_cast<CUtensorMap*>(m + 8), &b0, &nb, &report_ns, &abort_ns};
+                  const_cast<CUtensorMap*>(m + 8), &b0, &nb, &parts, &w, &report_ns, &abort_ns};
   cudaError_t e = cudaLaunchKernelExC(&cfg, k, args);
-  if (e == cudaSuccess) ++*launches;
+  if (e == cudaSuccess) {
+    ++*launches;
+    g_last_parts = parts;
+  }
   return e;
 }
 

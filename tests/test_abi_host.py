@@ -31,6 +31,7 @@ def test_config_struct_layout_matches_c():
     assert C.sizeof(B.MhcConfig) == 40
     assert B.MhcConfig.spin_limit.offset == 24
     assert B.MhcConfig.projection.offset == 32
+    assert B.MhcConfig.wave_split.offset == 36
 
 
 def _seam(L, **over):
@@ -103,7 +104,8 @@ def test_unshifted_argument_rules(L):
     big = B.MhcConfig(block_m=32, cols_per_cta=640)
     assert _unsh(L, H=5120, cfg=C.byref(big)) == -10
     assert _seam(L, H=5120, cfg=C.byref(big), ws_bytes=1) == -5
-    assert L.mhc_workspace_bytes_unshifted(4096, 5120, None) == L.mhc_workspace_bytes(4096, 5120, None) == 256
+    # the streaming path's workspace: the status header and the split last round's 776 KiB
+    assert L.mhc_workspace_bytes_unshifted(4096, 5120, None) == L.mhc_workspace_bytes(4096, 5120, None) == 256 + 776 * 1024
     p1 = B.MhcConfig(path=1)
     need = L.mhc_workspace_bytes_unshifted(4096, 5120, C.byref(p1))
     assert need > 256 and _unsh(L, T=4096, H=5120, cfg=C.byref(p1), ws_bytes=need - 1) == -5
@@ -134,7 +136,8 @@ def test_workspace_rules(L):
 
 def test_config_validation(L):
     for bad in (dict(path=5), dict(path=-1), dict(block_m=3), dict(block_m=64), dict(cols_per_cta=48), dict(spin_limit=-1),
-                dict(sinkhorn_iters=-2), dict(amax_floor=-1.0), dict(projection=3)):
+                dict(sinkhorn_iters=-2), dict(amax_floor=-1.0), dict(projection=3), dict(wave_split=-1),
+                dict(wave_split=65)):
         cfg = B.MhcConfig(**bad)
         assert _seam(L, cfg=C.byref(cfg)) == -10, bad
     cfg = B.MhcConfig(path=3, projection=1)     # clusters of 16 run the tcgen05 projection only
@@ -145,14 +148,15 @@ def test_workspace_grows_with_tokens_and_columns(L):
     p1 = B.MhcConfig(path=1)
     a = L.mhc_workspace_bytes(4, 5120, C.byref(p1))      # split path forced
     b = L.mhc_workspace_bytes(64, 5120, C.byref(p1))
-    c = L.mhc_workspace_bytes(1024, 5120, None)          # streaming path: status word only
+    c = L.mhc_workspace_bytes(1024, 5120, None)          # streaming path: status word + split last round
     d = L.mhc_workspace_bytes(1024, 5120, C.byref(p1))
-    assert 256 < a < b < d and c == 256
-    # small T: the automatic policy's workspace also covers the split path it
-    # takes without fn_packed; clusters of 16 need only the status word
-    assert L.mhc_workspace_bytes(4, 5120, None) == a
+    stream = 256 + 776 * 1024
+    assert 256 < a < b < d and c == stream
+    # small T: the automatic policy's workspace covers both paths it may take
+    # (the split path without fn_packed, clusters of 16 with it)
+    assert L.mhc_workspace_bytes(4, 5120, None) == max(a, stream)
     p3 = B.MhcConfig(path=3)
-    assert L.mhc_workspace_bytes(4, 5120, C.byref(p3)) == 256
+    assert L.mhc_workspace_bytes(4, 5120, C.byref(p3)) == stream
     cfg = B.MhcConfig(block_m=8, cols_per_cta=64)
     assert L.mhc_workspace_bytes(64, 5120, C.byref(cfg)) == 256 + 8 * (((64 + 128 + 80 * 8 * 128) + 255) // 256 * 256)
 

@@ -738,3 +738,108 @@ def test_full_size_unshifted():
     for gk, ok in (("pre_out", "pre"), ("post_out", "post"), ("comb_out", "comb")):
         ref = o[ok][np.arange(16384) % U].reshape(h[gk].shape)
         assert np.abs(h[gk].astype(np.float64) - ref).max() <= GATE_TOL
+
+
+# -------------------------------------- split partial round (the wave edge) --
+# A GB300 holds 36 clusters of 4 (9 of 16) of the streaming kernel at once, so
+# token blocks beyond a whole number of rounds leave a partial last round; its
+# blocks are cut into column parts whose sums meet in the workspace.
+@pytest.mark.parametrize("T,k", [(1184, 0), (1184, 2), (1184, 7), (1184, 20), (1600, 0), (2336, 0), (4160, 0),
+                                 (4161, 0), (4161, 2)])
+def test_wave_split_partial_round(T, k):
+    d = make_case(T, 5120, 9800 + T + k, unique_tokens=512)
+    g = to_dev(d)
+    h = to_host(run_gpu(d, g=g, cfg=B.MhcConfig(path=2, wave_split=k)))
+    parts = B.mhc_last_wave_parts()
+    assert parts == k if k else parts >= 2, parts
+    compare_all_tokens(d, h, 512)
+    # the same call without the split: R' does not depend on it (bit for bit),
+    # the gates and norm agree within the parity bar
+    n = to_host(run_gpu(d, g=g, cfg=B.MhcConfig(path=2, wave_split=1)))
+    assert B.mhc_last_wave_parts() == 1
+    assert np.array_equal(h["residual_out"], n["residual_out"])
+    assert np.mean(ulp_diff(h["norm"], n["norm"]) <= 1) >= 0.9999
+    for gk in ("pre_out", "post_out", "comb_out"):
+        assert np.abs(h[gk] - n[gk]).max() <= GATE_TOL, gk
+
+
+@pytest.mark.parametrize("form", ["no_post", "identity", "mxfp8", "fp8_grid", "in_place"])
+def test_wave_split_forms_and_outputs(form):
+    T = 1184
+    d = make_case(T, 5120, 9900, post=form != "no_post", ident=form == "identity", mxfp8=form == "mxfp8",
+                  grid=form == "fp8_grid", craft=form == "mxfp8", unique_tokens=512)
+    cfg = B.MhcConfig(path=2, wave_split=5)
+    out = None
+    if form == "identity":
+        out = B.alloc_outputs(T, 5120, d["out_mode"], "cuda", cfg)
+        out["residual_out"] = None
+    h = to_host(run_gpu(d, cfg=cfg, out=out, inplace=form == "in_place"))
+    assert B.mhc_last_wave_parts() == 5
+    rep = compare_all_tokens(d, h, 512)
+    assert rep.get("codes_mismatch", 0) == 0 and rep.get("grid_mismatch", 0) == 0
+
+
+@pytest.mark.parametrize("T,k", [(300, 0), (300, 3), (1000, 2)])
+def test_wave_split_clusters_of_16(T, k):
+    # 9 clusters of 16 fit: T = 300 is 10 blocks (one left for a second round),
+    # T = 1000 is 32 blocks (5 left)
+    d = make_case(T, 5120, 9950 + T + k, unique_tokens=256)
+    h = to_host(run_gpu(d, cfg=B.MhcConfig(path=3, wave_split=k)))
+    parts = B.mhc_last_wave_parts()
+    assert parts == k if k else parts >= 2, parts
+    compare_all_tokens(d, h, 256)
+
+
+def test_wave_split_warp_mma_projection_and_unshifted():
+    # H = 7168 runs the warp-level projection (x alone fills tensor memory)
+    d = make_case(1184, 7168, 9970, unique_tokens=256)
+    h = to_host(run_gpu(d, cfg=B.MhcConfig(path=2, wave_split=4)))
+    assert B.mhc_last_wave_parts() == 4
+    compare_all_tokens(d, h, 256)
+    # the unshifted ordering's first launch takes the split too
+    d = make_case(1184, 5120, 9971)
+    hu = _run_unshifted(d, cfg=B.MhcConfig(path=2, wave_split=6))
+    o = O.seam_unshifted(d["R"], d["Y"], d["post_prev"], d["comb_prev"], d["fn"], d["bias"], d["alpha"], d["eps"])
+    assert np.mean(ulp_diff(hu["residual_out"], o["residual_out"]) <= 1) >= 0.9999
+    check_unshifted_x(hu["norm"], hu["pre_out"], o, hu["residual_out"])
+    for gk, ok in (("pre_out", "pre"), ("post_out", "post"), ("comb_out", "comb")):
+        assert np.abs(hu[gk].astype(np.float64) - o[ok].reshape(hu[gk].shape)).max() <= GATE_TOL
+
+
+def test_wave_split_repeat_graph_and_report():
+    # the split's workspace counters reset themselves: repeated calls and graph
+    # replays give the same bits; a forced report on a split call is flagged and
+    # the next call is clean
+    T = 2336
+    d = make_case(T, 5120, 9980, unique_tokens=512)
+    g = to_dev(d)
+    cfg = B.MhcConfig(path=2, wave_split=10)
+    out = B.alloc_outputs(T, 5120, d["out_mode"], "cuda", cfg)
+    a = to_host(run_gpu(d, g=g, out=out, cfg=cfg))
+    assert B.mhc_last_wave_parts() == 10
+    b = to_host(run_gpu(d, g=g, out=out, cfg=cfg))
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    for k in ("norm", "pre_out", "comb_out"):
+        out[k].zero_()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            run_gpu(d, g=g, out=out, cfg=cfg, stream=s)
+    for _ in range(3):
+        graph.replay()
+    c = to_host(out)
+    for k in a:
+        assert np.array_equal(a[k], c[k]), k
+    B.mhc_check_status(out["workspace"])
+    compare_all_tokens(d, c, 512)
+    run_gpu(d, g=g, out=out, cfg=B.MhcConfig(path=2, wave_split=10, spin_limit=1))
+    with pytest.raises(B.MhcError) as e:
+        B.mhc_check_status(out["workspace"])
+    assert e.value.code == -7
+    compare_all_tokens(d, to_host(out), 512)
+    run_gpu(d, g=g, out=out, cfg=cfg)
+    B.mhc_check_status(out["workspace"])
+    assert np.array_equal(to_host(out)["norm"], a["norm"])
