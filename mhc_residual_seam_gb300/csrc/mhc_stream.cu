@@ -76,16 +76,19 @@ constexpr uint32_t kRTile = kBM * 128;                 // 4 KB
 constexpr uint32_t kFnTile = kFnRows * 128;            // 6 KB
 constexpr uint32_t kFnStage = 4 * kFnTile;             // 24 KB: [192 x 64] bf16
 constexpr uint32_t kInStage = 5 * kRTile;              // 20 KB: R tiles 0-3, Y tile 4
-// The input ring holds 4 stages of R + Y, or, in the forms without Y, 5
-// stages of R in the same bytes (more loads in flight per SM).
+// The input ring of clusters of 4 holds 4 stages of R + Y, or, in the forms
+// without Y, 5 stages of R in the same bytes (more loads in flight per SM);
+// clusters of 16 (a CTA has at most 8 chunks per block) hold 3 stages.
 constexpr int kNIMax = 5;
-template <int FORM>
-__host__ __device__ constexpr int in_stages() { return FORM == 1 ? 4 : 5; }
+template <int FORM, int KCL>
+__host__ __device__ constexpr int in_stages() { return KCL == 16 ? 3 : FORM == 1 ? 4 : 5; }
 template <int FORM>
 __host__ __device__ constexpr uint32_t in_stage_bytes() { return FORM == 1 ? kInStage : 4 * kRTile; }
 constexpr uint32_t kOffNormT = 4 * kRTile;             // output stage: R' tiles 0-3, then the norm tile,
-constexpr uint32_t kOffCodesT = 5 * kRTile;            //   then the codes tile [32 x 64] u8
-constexpr uint32_t kOutStage = 5 * kRTile + kBM * 64;  // 22 KB (a multiple of 1 KB: swizzled tiles)
+constexpr uint32_t kOffCodesT = 5 * kRTile;            //   then (mxfp8) the codes tile [32 x 64] u8
+// 22 KB with the codes tile, else 20 KB (multiples of 1 KB: swizzled tiles)
+template <int OUT>
+__host__ __device__ constexpr uint32_t out_stage_bytes() { return OUT == 1 ? 5 * kRTile + kBM * 64 : 5 * kRTile; }
 // The normalise-only pass after a cluster's last block puts the norm tiles of
 // norm_group() chunks in one output stage (in the R' tile slots; with mxfp8
 // the codes tiles go where the norm tile sits in the other passes).
@@ -112,21 +115,26 @@ struct alignas(128) GateTile {
 };
 
 // Geometry of a cluster of KCL CTAs: 4 for large T (bandwidth), 16 for small T
-// (each CTA takes a quarter of the columns it would take in a cluster of 4).
-template <int KCL>
+// (each CTA takes a quarter of the columns it would take in a cluster of 4),
+// for output mode OUT (the mxfp8 output stages hold a codes tile more).
+template <int KCL, int OUT>
 struct Geo {
   static constexpr int kCl = KCL;
-  static constexpr uint32_t kInRing = 4 * kInStage;     // input ring: 80 KB
+  static constexpr uint32_t kInRing = (KCL == 16 ? 3 : 4) * kInStage;  // input ring: 80 KB (60 KB)
+  static constexpr uint32_t kOutStage = out_stage_bytes<OUT>();
   static constexpr int kSlots = kBM / KCL;              // tokens owned per CTA and block
-  static constexpr int kGamChunks = KCL == 4 ? kMaxChunksTC : (kMaxChunks * 4) / KCL;  // gamma staged in smem
+  // gamma of a CTA's first chunks, staged in shared memory (the mxfp8 form on
+  // clusters of 4 has no room left: its chunks read gamma through L1/L2)
+  static constexpr int kGamChunks = KCL == 4 ? (OUT == 1 ? 0 : kMaxChunksTC) : (kMaxChunks * 4) / KCL;
   static constexpr uint32_t kXsBytes = KCL * kBM * 4;   // s_x partials landing in each CTA per block
   static constexpr uint32_t kRecvBytes = KCL * kSlots * kOwnerParts * 4;  // owner partials per CTA per block
   static constexpr uint32_t kOffIn = kOffOut + kNO * kOutStage;
   static constexpr uint32_t kOffTail = kOffIn + kInRing;
   struct Tail {
-    GateTile gates;                        // one block's carried gates (the producer loads the next once compute has read them)
+    GateTile gates[2];                     // carried gates of items i (buffer i % 2), loaded an item ahead; a
+                                           // buffer is released only when its item's compute has finished
     uint64_t in_full[kNIMax], in_empty[kNIMax], fn_full[kNF], fn_empty[kNF], out_full[kNO], out_empty[kNO];
-    uint64_t d_full, xs_full[2], recv_full[2], recv_free[2], gates_full, gates_empty;
+    uint64_t d_full, xs_full[2], recv_full[2], recv_free[2], gates_full[2], gates_empty[2];
     uint64_t red_full[2], dbuf_full, dbuf_free, d_free;
     uint64_t mma_fin;                      // exit drain: completion of every MMA issued
     uint64_t fold_full;                    // warp-MMA form: warps 4-7 have written their partial projections
@@ -136,7 +144,7 @@ struct Geo {
     float dbuf[4][kBM][kDPad];             // the block's projection per stream (hi + lo): [stream][token][logit]
     float xs[2][KCL][kBM];                 // [block parity][source CTA][token]: s_x partial
     float recv[2][KCL][kSlots][kPartPad];  // [block parity][source CTA][owned token][part]
-    uint4 gam[kGamChunks][8];              // gamma of this CTA's first chunks (8 bf16 per compute warp)
+    uint4 gam[kGamChunks > 0 ? kGamChunks : 1][8];  // gamma of this CTA's first chunks (8 bf16 per compute warp)
     float pbuf[kSlots][kPartPad];          // the owned tokens' parts summed over the cluster
     float ab[27];                          // alpha[3], bias[24]
   };
@@ -317,14 +325,15 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
                        const __grid_constant__ CUtensorMap tmFn, const __grid_constant__ CUtensorMap tmN,
                        const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmGc,
                        const __grid_constant__ CUtensorMap tmGp, const __grid_constant__ CUtensorMap tmGq,
-                       int block0, int n_blocks, int k_parts, char* wsx, unsigned long long report_ns,
-                       unsigned long long abort_ns) {
+                       int block0, int nfull, int R, int k_parts, int G_groups, char* wsx,
+                       unsigned long long report_ns, unsigned long long abort_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  using G = Geo<KCL>;
+  using G = Geo<KCL, OUT>;
+  constexpr uint32_t kOutStage = G::kOutStage;
   constexpr int kThreads = threads_of<OUT>();
   constexpr bool POST = FORM == 1, IDENT = FORM == 2;
-  constexpr int kNI = in_stages<FORM>();
+  constexpr int kNI = in_stages<FORM, KCL>();
   constexpr uint32_t kInStageF = in_stage_bytes<FORM>();
   static_assert(kNI <= kNIMax && kNI * kInStageF <= G::kInRing, "input ring");
   constexpr int kCl = G::kCl, kSlots = G::kSlots;
@@ -342,14 +351,17 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
   const int n64 = H / kChunk;
   const int nch = n64 > (int)rank ? (n64 - (int)rank + kCl - 1) / kCl : 0;
   const int ncl = gridDim.x / kCl;
+  // the schedule's constants come from the host (they stay in the constant
+  // bank instead of registers): nfull whole rounds, R blocks left, k parts
+  // per left block (1 when R is 0), G column groups
   Sched S;
   S.cid = blockIdx.x / kCl;
   S.ncl = ncl;
   S.block0 = block0;
-  S.nfull = n_blocks / ncl;
-  S.R = n_blocks - S.nfull * ncl;
-  S.k = S.R > 0 ? k_parts : 1;
-  S.G = (n64 + kCl - 1) / kCl;
+  S.nfull = nfull;
+  S.R = R;
+  S.k = k_parts;
+  S.G = G_groups;
   const int nit = S.nitems();
   // chunks of this CTA in item i (a unit covers whole groups only)
   auto nchi = [&](int i) { return S.is_unit(i) ? S.g1(i) - S.g0(i) : nch; };
@@ -375,8 +387,10 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
       mbar_init(&tl->out_empty[s], (MS ? 9 : 2) + (OUT == 2 ? 1 : 0));
     }
     mbar_init(&tl->d_full, 1);
-    mbar_init(&tl->gates_full, 1);
-    mbar_init(&tl->gates_empty, 8);
+    for (int p = 0; p < 2; ++p) {
+      mbar_init(&tl->gates_full[p], 1);
+      mbar_init(&tl->gates_empty[p], 8);
+    }
     mbar_init(&tl->dbuf_full, 4);  // the four D readers (or folders)
     mbar_init(&tl->dbuf_free, 1);  // the exchange warp
     mbar_init(&tl->d_free, 4);     // the four D readers
@@ -405,9 +419,6 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
     prefetch_tmap(&tmN);
     if (OUT == 1) prefetch_tmap(&tmC);
   }
-  // gamma of this CTA's first chunks (groups), staged once (read by every item)
-  for (int i = tid; i < min(nch, G::kGamChunks) * 8; i += kThreads)
-    tl->gam[i >> 3][i & 7] = __ldg(reinterpret_cast<const uint4*>(a.gamma + ((i >> 3) * kCl + (int)rank) * kChunk) + (i & 7));
   if (warp == 9) {
     tmem_alloc(&tl->tmem_base, kTmemCols);
     tmem_relinquish();
@@ -417,6 +428,17 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
   cluster_sync_all();  // barriers initialised in every CTA of the cluster
   tc_fence_after();
   const uint32_t tmem = tl->tmem_base;
+  // Programmatic dependent launch: everything above (barriers, tensor memory,
+  // the cluster barrier, tensor-map prefetch) may overlap the previous kernel
+  // on the stream; every read of global memory comes after this wait, which
+  // returns once that kernel has completed and its writes are visible.  The
+  // next kernel may then begin its own set-up while this one runs.
+  griddep_wait();
+  if (tid == 0) griddep_launch_dependents();
+  // gamma of this CTA's first chunks (groups), staged once (read by every item)
+  for (int i = tid; i < min(nch, G::kGamChunks) * 8; i += kThreads)
+    tl->gam[i >> 3][i & 7] = __ldg(reinterpret_cast<const uint4*>(a.gamma + ((i >> 3) * kCl + (int)rank) * kChunk) + (i & 7));
+  __syncthreads();
 
   if (warp == 8) {
     // --------------------------------------------------- input producer --
@@ -430,12 +452,14 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
       bool ok = true;
       for (int i = 0; i < nit && ok; ++i) {
         const int t0 = S.block(i) * kBM, gb = S.g0(i), ni = nchi(i);
-        // the item's carried gates, consumed at the top of its compute
-        if (!(ok = wait_local(X, &tl->gates_empty, (i & 1) ^ 1))) break;
-        mbar_arrive_expect_tx(&tl->gates_full, (IDENT ? 4 : POST ? 24 : 20) * kBM * 4);
-        if (!IDENT) tma_load_2d(&tl->gates.comb[0][0], &tmGc, &tl->gates_full, 0, t0, pol);
-        tma_load_2d(&tl->gates.pre[0][0], &tmGp, &tl->gates_full, 0, t0, pol);
-        if (POST) tma_load_2d(&tl->gates.post[0][0], &tmGq, &tl->gates_full, 0, t0, pol);
+        // the item's carried gates, into buffer i % 2 once the item two
+        // before has finished with it
+        const int gbuf = i & 1;
+        if (!(ok = wait_local(X, &tl->gates_empty[gbuf], ((i >> 1) & 1) ^ 1))) break;
+        mbar_arrive_expect_tx(&tl->gates_full[gbuf], (IDENT ? 4 : POST ? 24 : 20) * kBM * 4);
+        if (!IDENT) tma_load_2d(&tl->gates[gbuf].comb[0][0], &tmGc, &tl->gates_full[gbuf], 0, t0, pol);
+        tma_load_2d(&tl->gates[gbuf].pre[0][0], &tmGp, &tl->gates_full[gbuf], 0, t0, pol);
+        if (POST) tma_load_2d(&tl->gates[gbuf].post[0][0], &tmGq, &tl->gates_full[gbuf], 0, t0, pol);
         ++ng;
         for (int c = 0; c < ni; ++c, ++j) {
           const int s = j % kNI;
@@ -451,9 +475,9 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
       // Every load issued lands before the CTA exits.  A stage is refilled
       // only after all eight compute warps released it, and they release it
       // only after seeing its previous load complete, so only the last load
-      // of each stage (and of the gate buffer) can still be in flight.
+      // of each stage (and of each gate buffer) can still be in flight.
       for (int jj = (j > kNI ? j - kNI : 0); jj < j; ++jj) drain(X, &tl->in_full[jj % kNI], (jj / kNI) & 1);
-      if (ng > 0) drain(X, &tl->gates_full, (ng - 1) & 1);
+      for (int q = (ng > 2 ? ng - 2 : 0); q < ng; ++q) drain(X, &tl->gates_full[q & 1], (q >> 1) & 1);
     }
   } else if (warp == 10) {
     // ------------------------------------------------------ fn producer --
@@ -914,17 +938,15 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
         float4 gc[4], gp = make_float4(0.f, 0.f, 0.f, 0.f), gq = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < 4; ++k) gc[k] = gp;
-        {  // rows past T arrive as zeros
-          if (!(ok = wait_warp(X, &tl->gates_full, i & 1))) break;
-          const GateTile& gt = tl->gates;
+        {  // rows past T arrive as zeros; the buffer is released at the item's end
+          if (!(ok = wait_warp(X, &tl->gates_full[i & 1], (i >> 1) & 1))) break;
+          const GateTile& gt = tl->gates[i & 1];
           if (!IDENT) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) gc[k] = *reinterpret_cast<const float4*>(&gt.comb[lane][4 * k]);
           }
           gp = *reinterpret_cast<const float4*>(&gt.pre[lane][0]);
           if (POST) gq = *reinterpret_cast<const float4*>(&gt.post[lane][0]);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&tl->gates_empty);
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -1035,7 +1057,12 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
       const int par = i & 1;
       tl->red[par][warp][lane] = make_float2(sR2.x + sR2.y, sx2.x + sx2.y);
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tl->red_full[par]);
+      if (lane == 0) {
+        mbar_arrive(&tl->red_full[par]);
+        // the item's gate buffer may now be refilled (for item i + 2): no read
+        // of it can still be pending, however the gates were kept or re-read
+        mbar_arrive(&tl->gates_empty[i & 1]);
+      }
       // no MMA follows the last item: its D is read now
       if (!MS && i == nit - 1 && warp < 4 && !(ok = read_d(i))) break;
       if (MS) {  // warps w and w + 4 both hold stream w % 4: fold them into dbuf[w % 4]
@@ -1156,7 +1183,11 @@ static void* stream_kernel_ptr(int form, int out, bool ms, int kcl) {
   if (kcl == 16) return kptr_<false, 16>(form, out);
   return ms ? kptr_<true, 4>(form, out) : kptr_<false, 4>(form, out);
 }
-static size_t smem_bytes(int kcl) { return kcl == 16 ? Geo<16>::kSmemBytes : Geo<4>::kSmemBytes; }
+static size_t smem_bytes(int kcl, int out) {
+  if (kcl == 16)
+    return out == 2 ? Geo<16, 2>::kSmemBytes : out == 1 ? Geo<16, 1>::kSmemBytes : Geo<16, 0>::kSmemBytes;
+  return out == 2 ? Geo<4, 2>::kSmemBytes : out == 1 ? Geo<4, 1>::kSmemBytes : Geo<4, 0>::kSmemBytes;
+}
 
 cudaError_t stream_init() {
   for (int p = 0; p < 3; ++p)        // form
@@ -1164,7 +1195,7 @@ cudaError_t stream_init() {
       for (int v = 0; v < 3; ++v) {  // v: 0 tcgen05 / 4, 1 warp MMA / 4, 2 tcgen05 / 16
         const int kcl = v == 2 ? 16 : 4;
         void* k = stream_kernel_ptr(p, m, v == 1, kcl);
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes(kcl));
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes(kcl, m));
         if (e == cudaSuccess && kcl == 16) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
       }
@@ -1227,7 +1258,7 @@ static int max_clusters(int form, int out, bool ms, int kcl) {
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3((unsigned)kcl, 1, 1);
   cfg.blockDim = dim3(out == 2 ? threads_of<2>() : threads_of<0>(), 1, 1);
-  cfg.dynamicSmemBytes = smem_bytes(kcl);
+  cfg.dynamicSmemBytes = smem_bytes(kcl, out);
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
@@ -1395,28 +1426,33 @@ static cudaError_t launch_range(const SeamArgs& a, const CUtensorMap* m, bool tc
   const int ncl = n_blocks < fit ? n_blocks : fit;
   int parts = wsx ? wave_parts(n_blocks, ncl, a.H / kChunk, kcl, tcgen05_proj, wave_split) : 1;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)kcl;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // The kernel's set-up may overlap the previous kernel on the stream (it
+  // waits for that kernel before touching global memory).
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   // The parts of a split block wait for each other's partial sums: every
   // cluster of the grid must be resident at once, which a cooperative launch
   // guarantees (the grid is at most the clusters that fit).
-  attr[1].id = cudaLaunchAttributeCooperative;
-  attr[1].val.cooperative = 1;
+  attr[2].id = cudaLaunchAttributeCooperative;
+  attr[2].val.cooperative = 1;
   cfg.gridDim = dim3((unsigned)(ncl * kcl), 1, 1);
   cfg.blockDim = dim3(mx == 2 ? threads_of<2>() : threads_of<0>(), 1, 1);
-  cfg.dynamicSmemBytes = smem_bytes(kcl);
+  cfg.dynamicSmemBytes = smem_bytes(kcl, mx);
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = parts > 1 ? 2 : 1;
-  int b0 = block0, nb = n_blocks;
+  cfg.numAttrs = parts > 1 ? 3 : 2;
+  int b0 = block0, nfull = n_blocks / ncl, rem = n_blocks - (n_blocks / ncl) * ncl;
+  int kpart = rem > 0 ? parts : 1, groups = (a.H / kChunk + kcl - 1) / kcl;
   char* w = static_cast<char*>(wsx);
   void* args[] = {const_cast<SeamArgs*>(&a),    const_cast<CUtensorMap*>(m),     const_cast<CUtensorMap*>(m + 1),
                   const_cast<CUtensorMap*>(m + 2), const_cast<CUtensorMap*>(m + 3), const_cast<CUtensorMap*>(m + 4),
                   const_cast<CUtensorMap*>(m + 5), const_cast<CUtensorMap*>(m + 6), const_cast<CUtensorMap*>(m + 7),
-                  const_cast<CUtensorMap*>(m + 8), &b0, &nb, &parts, &w, &report_ns, &abort_ns};
+                  const_cast<CUtensorMap*>(m + 8), &b0, &nfull, &rem, &kpart, &groups, &w, &report_ns, &abort_ns};
   cudaError_t e = cudaLaunchKernelExC(&cfg, k, args);
   if (e == cudaSuccess) {
     ++*launches;
