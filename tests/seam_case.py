@@ -136,8 +136,23 @@ def compare_all_tokens(d: dict, h: dict, unique: int, check_quant: bool = True, 
     bit-exact) is asserted over the whole output."""
     T = d["T"]
     U = min(unique, T)
+    cls = np.arange(T) % U
+    # tokens whose inputs differ from their class token's (rows planted after
+    # the draw, e.g. the crafted quantiser rows) get the oracle of their own
+    idx = torch.from_numpy(cls)
+    special = np.zeros(T, dtype=bool)
+    for key in ("R", "Y", "post_prev", "comb_prev", "pre_prev"):
+        x = d.get(key)
+        if x is not None:
+            special |= (x != x[idx]).reshape(T, -1).any(dim=1).numpy()
+    special = np.nonzero(special)[0]
     o = oracle_on(d, np.arange(U))
-    rep = {}
+    src = cls.copy()
+    if len(special):
+        os_ = oracle_on(d, special)
+        o = {k: np.concatenate([o[k], os_[k]]) for k in o}
+        src[special] = U + np.arange(len(special))
+    rep = {"tokens_with_own_oracle": int(len(special))}
     for k in ("residual_out", "norm"):
         if k not in h:
             continue
@@ -145,8 +160,7 @@ def compare_all_tokens(d: dict, h: dict, unique: int, check_quant: bool = True, 
         worst = 0
         for t0 in range(0, T, slice_tokens):
             t1 = min(T, t0 + slice_tokens)
-            cls = np.arange(t0, t1) % U
-            u = ulp_diff(h[k][t0:t1], o[k][cls])
+            u = ulp_diff(h[k][t0:t1], o[k][src[t0:t1]])
             within += int(np.sum(u <= 1))
             exact += int(np.sum(u == 0))
             total += u.size
@@ -156,9 +170,8 @@ def compare_all_tokens(d: dict, h: dict, unique: int, check_quant: bool = True, 
         rep[k + "_maxulp"] = worst
         rep[k + "_elements"] = total
         assert rep[k + "_within1"] >= ULP_FRAC, (k, rep)
-    cls = np.arange(T) % U
     for gk, ok in (("pre_out", "pre"), ("post_out", "post"), ("comb_out", "comb")):
-        ref = o[ok][cls].reshape(h[gk].shape)
+        ref = o[ok][src].reshape(h[gk].shape)
         err = np.abs(h[gk].astype(np.float64) - ref)
         rep[ok + "_maxerr"] = float(err.max()) if err.size else 0.0
         assert rep[ok + "_maxerr"] <= GATE_TOL, (ok, rep)
