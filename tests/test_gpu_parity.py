@@ -781,14 +781,15 @@ def test_wave_split_forms_and_outputs(form):
 
 @pytest.mark.parametrize("T,k", [(300, 0), (352, 5), (352, 2), (1000, 2)])
 def test_wave_split_clusters_of_16(T, k):
-    # about 9 clusters of 16 fit: T = 352 (11 blocks) and T = 1000 (32 blocks)
-    # leave a partial last round; the policy's own choice (k = 0) is checked
-    # for parity only
+    # 7 to 10 clusters of 16 fit (by variant): T = 352 (11 blocks) and
+    # T = 1000 (32 blocks) leave a partial last round, cut into at most k parts
+    # (fewer where two parts per cluster would not cover them); the policy's
+    # own choice (k = 0) is checked for parity only
     d = make_case(T, 5120, 9950 + T + k, unique_tokens=256)
     h = to_host(run_gpu(d, cfg=B.MhcConfig(path=3, wave_split=k)))
     parts = B.mhc_last_wave_parts()
     if k:
-        assert parts == k, parts
+        assert 2 <= parts <= k, parts
     compare_all_tokens(d, h, 256)
 
 
