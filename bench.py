@@ -191,7 +191,8 @@ def run_ours(args, w: dict, rank: int, world: int, local_rank: int) -> dict | No
     B.mhc_pack_fn(g["fn"], g["fn_packed"], stream=stream)  # once per weight update, outside the timed region
 
     cfg = B.MhcConfig(projection={"auto": 0, "mma": 1, "tcgen05": 2}[args.projection],
-                      path={"auto": 0, "split": 1, "stream": 2, "stream16": 3}[args.path])
+                      path={"auto": 0, "split": 1, "stream": 2, "stream16": 3}[args.path],
+                      wave_split=args.wave_split)
     unsh = bool(w.get("unshifted"))
     out = B.alloc_outputs(T, H, mode, device, cfg, unshifted=unsh)
     if w.get("ident"):  # the identity form writes no residual
@@ -216,6 +217,7 @@ def run_ours(args, w: dict, rank: int, world: int, local_rank: int) -> dict | No
         step()
     torch.cuda.synchronize(device)
     launches = B.mhc_last_launch_count()
+    parts = B.mhc_last_wave_parts()
     B.mhc_check_status(out["workspace"])
     run_step = step
     per_graph = 1  # seam calls per replay: a graph of several calls keeps host time out of small-T timings
@@ -310,7 +312,7 @@ def run_ours(args, w: dict, rank: int, world: int, local_rank: int) -> dict | No
         ACC.seam_bytes(T, H, post=w["post"], out=w["out"], ident=w.get("ident", False)), device, stream)
     ms_max, e2e_max = reduce_max([ms, e2e["ms"] if e2e else 0.0], world, device)
     return {"ms": ms_max, "e2e": e2e and dict(e2e, ms=e2e_max), "launches": launches, "clocks": clocks, "wl": wl,
-            "copy": copy,
+            "copy": copy, "parts": parts,
             "calls": runs * per_graph}
 
 
@@ -422,6 +424,8 @@ def main():
                     help="streaming path's gate projection (auto = the library's policy)")
     ap.add_argument("--path", choices=["auto", "split", "stream", "stream16"], default="auto",
                     help="kernel path (auto = the library's policy)")
+    ap.add_argument("--wave-split", type=int, default=0,
+                    help="column parts per block of a partial last round (0 = the library's policy, 1 = none)")
     ap.add_argument("--graph", action="store_true",
                     help="time replays of a CUDA graph holding one seam call (as the pages time small T)")
     args = ap.parse_args()
@@ -437,7 +441,7 @@ def main():
               "ordering": "unshifted" if w.get("unshifted") else "delayed",
               "tokens_per_rank": w["T"], "global_batch": w["T"] * world,
               "parallelism": f"token-shard x{world} (rank r: tokens r*T .. (r+1)*T-1, no exchange)",
-              "projection": args.projection, "path": args.path,
+              "projection": args.projection, "path": args.path, "wave_split": args.wave_split,
               "timing": (f"cuda-graph replay ({GRAPH_CALLS} calls per graph)" if args.graph
                          else "back-to-back launches"),
               "e2e_pipeline": "token slices (8 from T=2048, 4 from T=512) on two streams, copies overlapping seams",
@@ -482,7 +486,7 @@ def main():
                      "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": traffic,
                      "peak_src": f"{peaks['src']} hbm_gbs (copy)",
                      "algorithmic_bytes_per_launch": step_bytes / max(1, r["launches"]),
-                     "launches_per_step": r["launches"]},
+                     "launches_per_step": r["launches"], "wave_parts": r["parts"]},
         "clocks": r["clocks"],
     }
     if r["copy"]:
