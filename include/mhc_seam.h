@@ -108,16 +108,17 @@ typedef struct {
                             blocks left for that round are fewer than the clusters that fit,
                             each is cut into k column parts on k clusters, whose partial
                             sums meet in the workspace (cooperative launch: every cluster is
-                            resident).  0 = the policy picks k from an estimate of the round's
-                            time, 1 = never split, k >= 2 = k parts where they fit (at most two
-                            parts per cluster; H a multiple of 64 x cluster size) */
+                            resident).  0 = the policy: no split (a part's fixed cost, measured
+                            at about 24 chunk steps, exceeds what it saves at H = 5120), 1 = never
+                            split, k >= 2 = at most k parts where they fit (H a multiple of 64 x
+                            cluster size) */
 } mhc_config;
 
 /* Bytes of the per-stream workspace for a call of T tokens of width H with
  * `cfg` (NULL = defaults): a status word plus, on the split path, the
  * per-CTA partial sums and the arrival counters of every token group, and on
  * the streaming paths the partial sums and counters of the split last round
- * (776 KiB).  Where the policy's path depends on whether fn_packed is given,
+ * and the item scheduler's ticket counter (776 KiB + 128 bytes).  Where the policy's path depends on whether fn_packed is given,
  * the size covers both.  One
  * workspace per stream whose calls can overlap on the GPU; it needs
  * mhc_workspace_init() once, after which the counters reset themselves and any

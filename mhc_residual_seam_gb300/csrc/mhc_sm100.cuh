@@ -247,11 +247,21 @@ __device__ __forceinline__ void st_async_v2(uint32_t caddr, float v0, float v1, 
                "f"(v0), "f"(v1), "r"(cbar)
                : "memory");
 }
+__device__ __forceinline__ void st_async_v4(uint32_t caddr, int v0, int v1, int v2, int v3, uint32_t cbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(caddr),
+               "r"(v0), "r"(v1), "r"(v2), "r"(v3), "r"(cbar)
+               : "memory");
+}
 __device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t threads) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t caddr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+}
+// An arrive that orders nothing: for a reader giving back a slot whose
+// contents it has already consumed (its loads returned their values).
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t caddr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
 }
 __device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {

@@ -1,1187 +1,20 @@
-// Streaming path of the delayed mHC seam: bandwidth-tuned for large T, and
-// latency-tuned for small T with larger clusters.
-//
-// Persistent clusters of KCL CTAs (4, or 16 for small T; one CTA per SM).
-// CTA r of a cluster owns the 64-column chunks r, r + KCL, r + 2 KCL, ... of H
-// for all four streams (the cluster reads each row in long runs) and the
-// cluster walks blocks of 32 tokens.  Per 64-column chunk:
-//  - an input producer warp TMA-loads the four R tiles and the Y tile into a
-//    ring of 4 input stages (5 without Y; 128-byte swizzle), and each block's carried
-//    gates (comb, pre, post) into a buffer as it starts the block, so they
-//    wait in shared memory when compute gets there;
-//  - an fn producer warp TMA-loads the four hi/lo-packed fn tiles [48 x 64]
-//    into a ring of 2 fn stages (L2 evict-last: every cluster reuses them);
-//  - eight compute warps (thread = token, warp = 8-column slice; the swizzle
-//    makes the column reads conflict-free) read their inputs, release the
-//    input stage, post-mix in fp32 (packed fp32x2 FMAs), round R' to bf16 into
-//    a ring of 3 output stages, accumulate s_R and s_x, keep x in tensor
-//    memory, and normalise the previous block's x of the same chunk into the
-//    same output stage;
-//  - the gate projection runs on the tensor cores, in one of two forms:
-//    tcgen05 (one thread issues 4 MMAs per chunk: A = the four R' tiles
-//    stacked [128 x 64], B = the four fn tiles side by side [192 x 64], so
-//    D[128 x 192] holds stream i's 32 x 48 block on its diagonal, in TMEM
-//    lanes 32 i.. and columns 48 i..; the off-diagonal products are wasted,
-//    but each MMA instruction costs the same whatever its size), or, where x
-//    leaves no room for that accumulator in tensor memory, warp-level m16n8k16
-//    MMAs in the compute warps;
-//  - a store warp TMA-stores the R' tiles and the norm tile of each stage
-//    (and computes the e4m3 codes and ue8m0 scales of the norm tile); with
-//    the fp8_grid output three more warps each take every third stage and
-//    write the grid of its norm tile.
-// After the last chunk of a block the compute warps hand their partial sums
-// over in shared memory and go on; an exchange warp sends, through
-// distributed shared memory (st.async completing bytes on the receiver's
-// mbarrier):
-//  - the CTA's per-token s_x partials to every CTA of the cluster, which each
-//    sum them in the same order into rstd_x, needed by the next block's first
-//    chunk;
-//  - the 24 projection sums and s_R of each token to the token's owner CTA
-//    (token % KCL), whose exchange warp then computes the gates.
-// ("[FlyDSL] Single-launch Mega-mHC on gfx950", Kernel Architecture: split-K
-// with a distributed finish; here the cluster launch makes every CTA of a
-// split co-resident.)
-//
-// Forms: post, no_post, and identity (the first block's seam: R' = R, no
-// residual store).  A call with no norm pointer stores no norm: the first
-// pass of the unshifted ordering, which needs only R' and the gates.
-//
-// Every wait is bounded, in two tiers.  A wait longer than the caller's limit
-// sets bit 1 of the status word and goes on waiting, so a short limit only
-// flags the call and the work completes as usual.  A wait one second longer
-// abandons the call: the CTA stops issuing copies, MMAs and stores, and before
-// it frees tensor memory and exits it waits (with a fixed cap) for the ones in
-// flight: the last TMA load of every input, fn and gate buffer (a buffer is
-// refilled only after its previous load was seen complete), every MMA (one
-// final tcgen05.commit) and every bulk store (bulk wait_group).
+// Streaming path of the delayed mHC seam, host side: kernel variants, tensor
+// maps, the wave-edge split policy and the launch.  The kernel itself (and
+// its design notes) is in mhc_stream_kernel.cuh; the variants that split the
+// partial last round are instantiated in mhc_stream_split.cu.
 
-#include "mhc_common.cuh"
-#include "mhc_sm100.cuh"
+#include "mhc_stream_kernel.cuh"
 
 namespace mhc {
 
-namespace {
-
-constexpr int kBM = 32;                // tokens per block
-constexpr int kChunk = 64;             // columns per chunk
-constexpr int kNF = 2, kNO = 3;
-// warps 0-7 compute, 8 input producer, 9 MMA issuer, 10 fn producer, 11 finisher, 12 store,
-// and with the fp8_grid output 13-15 grid warps (warp 13 + o takes output
-// stage o).  16 warps still leave each thread 128 registers (4 warps per SM
-// sub-partition, as with 13).
-template <int OUT>
-__host__ __device__ constexpr int threads_of() { return OUT == 2 ? 512 : 416; }
-constexpr int kFnRows = 48;
-constexpr uint32_t kRTile = kBM * 128;                 // 4 KB
-constexpr uint32_t kFnTile = kFnRows * 128;            // 6 KB
-constexpr uint32_t kFnStage = 4 * kFnTile;             // 24 KB: [192 x 64] bf16
-constexpr uint32_t kInStage = 5 * kRTile;              // 20 KB: R tiles 0-3, Y tile 4
-// The input ring of clusters of 4 holds 4 stages of R + Y, or, in the forms
-// without Y, 5 stages of R in the same bytes (more loads in flight per SM);
-// clusters of 16 (a CTA has at most 8 chunks per block) hold 3 stages.
-constexpr int kNIMax = 5;
-template <int FORM, int KCL>
-__host__ __device__ constexpr int in_stages() { return KCL == 16 ? 3 : FORM == 1 ? 4 : 5; }
-template <int FORM>
-__host__ __device__ constexpr uint32_t in_stage_bytes() { return FORM == 1 ? kInStage : 4 * kRTile; }
-constexpr uint32_t kOffNormT = 4 * kRTile;             // output stage: R' tiles 0-3, then the norm tile,
-constexpr uint32_t kOffCodesT = 5 * kRTile;            //   then (mxfp8) the codes tile [32 x 64] u8
-// 22 KB with the codes tile, else 20 KB (multiples of 1 KB: swizzled tiles)
-template <int OUT>
-__host__ __device__ constexpr uint32_t out_stage_bytes() { return OUT == 1 ? 5 * kRTile + kBM * 64 : 5 * kRTile; }
-// The normalise-only pass after a cluster's last block puts the norm tiles of
-// norm_group() chunks in one output stage (in the R' tile slots; with mxfp8
-// the codes tiles go where the norm tile sits in the other passes).
-template <int OUT>
-__host__ __device__ constexpr int norm_group() { return OUT == 1 ? 2 : 4; }
-constexpr uint32_t kOffFn = 0;
-constexpr uint32_t kOffOut = kOffFn + kNF * kFnStage;
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColD = 0;                          // tcgen05 accumulator D[128 x 192]
-constexpr uint32_t kDCols = 4 * kFnRows;
-constexpr int kMaxChunksTC = (int)((kTmemCols - kDCols) / 16);  // x: 16 columns per chunk
-constexpr int kMaxChunks = (int)(kTmemCols / 16);
-constexpr uint32_t kIdesc = idesc_bf16_f32(128, kDCols);
-constexpr int kOwnerParts = 25;                        // sent to a token's owner: 24 projections, s_R
-constexpr int kPartPad = 26;                           // rows of 8-byte aligned pairs
-constexpr int kDPad = 25;                              // odd row stride: conflict-free columns
-
-// Carried gates of one block, TMA-loaded a block ahead: comb [32 x 16],
-// pre [32 x 4], post [32 x 4] fp32.
-struct alignas(128) GateTile {
-  float comb[kBM][16];
-  float pre[kBM][4];
-  float post[kBM][4];
-};
-
-// Geometry of a cluster of KCL CTAs: 4 for large T (bandwidth), 16 for small T
-// (each CTA takes a quarter of the columns it would take in a cluster of 4),
-// for output mode OUT (the mxfp8 output stages hold a codes tile more).
-template <int KCL, int OUT>
-struct Geo {
-  static constexpr int kCl = KCL;
-  static constexpr uint32_t kInRing = (KCL == 16 ? 3 : 4) * kInStage;  // input ring: 80 KB (60 KB)
-  static constexpr uint32_t kOutStage = out_stage_bytes<OUT>();
-  static constexpr int kSlots = kBM / KCL;              // tokens owned per CTA and block
-  // gamma of a CTA's first chunks, staged in shared memory (the mxfp8 form on
-  // clusters of 4 has no room left: its chunks read gamma through L1/L2)
-  static constexpr int kGamChunks = KCL == 4 ? (OUT == 1 ? 0 : kMaxChunksTC) : (kMaxChunks * 4) / KCL;
-  static constexpr uint32_t kXsBytes = KCL * kBM * 4;   // s_x partials landing in each CTA per block
-  static constexpr uint32_t kRecvBytes = KCL * kSlots * kOwnerParts * 4;  // owner partials per CTA per block
-  static constexpr uint32_t kOffIn = kOffOut + kNO * kOutStage;
-  static constexpr uint32_t kOffTail = kOffIn + kInRing;
-  struct Tail {
-    GateTile gates[2];                     // carried gates of items i (buffer i % 2), loaded an item ahead; a
-                                           // buffer is released only when its item's compute has finished
-    uint64_t in_full[kNIMax], in_empty[kNIMax], fn_full[kNF], fn_empty[kNF], out_full[kNO], out_empty[kNO];
-    uint64_t d_full, xs_full[2], recv_full[2], recv_free[2], gates_full[2], gates_empty[2];
-    uint64_t red_full[2], dbuf_full, dbuf_free, d_free;
-    uint64_t mma_fin;                      // exit drain: completion of every MMA issued
-    uint64_t fold_full;                    // warp-MMA form: warps 4-7 have written their partial projections
-    uint32_t tmem_base;
-    volatile int reported, aborted;
-    float2 red[2][8][kBM];                 // [block parity][compute warp][token]: s_R, s_x partials
-    float dbuf[4][kBM][kDPad];             // the block's projection per stream (hi + lo): [stream][token][logit]
-    float xs[2][KCL][kBM];                 // [block parity][source CTA][token]: s_x partial
-    float recv[2][KCL][kSlots][kPartPad];  // [block parity][source CTA][owned token][part]
-    uint4 gam[kGamChunks > 0 ? kGamChunks : 1][8];  // gamma of this CTA's first chunks (8 bf16 per compute warp)
-    float pbuf[kSlots][kPartPad];          // the owned tokens' parts summed over the cluster
-    float ab[27];                          // alpha[3], bias[24]
-  };
-  static constexpr size_t kSmemBytes = kOffTail + sizeof(Tail) + 1024;
-  static_assert(kSmemBytes <= 232448, "shared memory of the streaming kernel exceeds 227 KB");
-};
-
-struct Ctx {
-  const SeamArgs* a;
-  volatile int* reported;  // the CTA has set the status bit of a slow wait
-  volatile int* aborted;   // the CTA abandons the call: no new copies, MMAs or stores
-  uint64_t report_ns;      // a wait longer than this is reported (status bit 1) and goes on
-  uint64_t abort_ns;       // a wait longer than this abandons the call
-};
-
-// Fixed cap of the exit drain (waits for copies and MMAs this CTA issued,
-// which complete on their own); independent of the caller's limit and of any
-// earlier error.
-constexpr uint64_t kDrainNs = 200000000ull;
-
-__device__ __forceinline__ void report_slow(const Ctx& x) {
-  if (!*x.reported) {
-    *x.reported = 1;
-    atomicOr(x.a->status, 2u);
-  }
-}
-// Wait on a phase of a CTA-local barrier.  Past report_ns the call is
-// reported and the wait goes on, so a short limit only flags the call; past
-// abort_ns, or at once once the CTA has abandoned the call, it returns false
-// and the caller stops issuing work (it never arrives on a barrier whose
-// phase it did not see complete).
-__device__ __forceinline__ bool wait_local(const Ctx& x, uint64_t* bar, uint32_t parity) {
-  if (mbar_test_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity, 20000)) {
-    if (*x.aborted) return false;
-    const uint64_t dt = globaltimer_ns() - t0;
-    if (dt > x.report_ns) report_slow(x);
-    if (dt > x.abort_ns) {
-      *x.aborted = 1;
-      return false;
-    }
-  }
-  return true;
-}
-// The same on a barrier that cluster peers arrive on (acquire at cluster scope).
-__device__ __forceinline__ bool wait_remote(const Ctx& x, uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait_cluster(bar, parity, 0)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait_cluster(bar, parity, 20000)) {
-    if (*x.aborted) return false;
-    const uint64_t dt = globaltimer_ns() - t0;
-    if (dt > x.report_ns) report_slow(x);
-    if (dt > x.abort_ns) {
-      *x.aborted = 1;
-      return false;
-    }
-  }
-  return true;
-}
-// A wait every lane of a warp makes: the warp goes on only if all lanes saw
-// the phase complete, so the warp leaves its loop as one.
-__device__ __forceinline__ bool wait_warp(const Ctx& x, uint64_t* bar, uint32_t parity) {
-  return __all_sync(0xffffffffu, wait_local(x, bar, parity));
-}
-__device__ __forceinline__ bool wait_warp_remote(const Ctx& x, uint64_t* bar, uint32_t parity) {
-  return __all_sync(0xffffffffu, wait_remote(x, bar, parity));
-}
-// Exit drain: wait for the phase that a copy or MMA this CTA issued
-// completes, at most kDrainNs, whatever happened before.
-__device__ __forceinline__ void drain(const Ctx& x, uint64_t* bar, uint32_t parity) {
-  if (!mbar_wait(bar, parity, kDrainNs)) report_slow(x);
-}
-
-}  // namespace
-
-// Gate finish of one token on its owner CTA, kept out of line so its arrays
-// do not raise the register pressure of the kernel.
-__device__ __noinline__ void finish_store_gates(const SeamArgs& a, int64_t t, const float* p, const float* ab, int H) {
-  float pre[4], post[4], cb[16];
-  finish_gates(p[24], p, ab, ab + 3, kStreams * H, a.eps, a.sinkhorn_iters, pre, post, cb);
-  store_gates(a, t, pre, post, cb);
-}
-
-namespace {
-
-// What one cluster works on, in order ("items").  Whole rounds first: cluster
-// cid takes blocks cid, cid + ncl, ... (nfull of them).  The last, partial
-// round of R < ncl blocks either goes whole to clusters 0 .. R-1 (k == 1), or
-// each of its blocks is cut into k column parts ("units"): unit u = p R + r is
-// part p of block r of that round and covers column groups [p G / k,
-// (p + 1) G / k) (a group is KCL adjacent 64-column chunks, one per CTA of
-// the cluster); cluster cid takes units cid, cid + ncl (at most two).  The
-// units of a block are summed through the global workspace, so a partial
-// round keeps most clusters busy instead of one block's latency on few of them
-// ("[FlyDSL] Single-launch Mega-mHC on gfx950", Kernel Architecture: the
-// split-K fallback at the wave edge).
-struct Sched {
-  int cid, ncl, block0, nfull, R, k, G;
-  __device__ __forceinline__ int nunits() const {
-    const int ku = k * R;
-    return (k > 1 && cid < ku) ? (ku - cid + ncl - 1) / ncl : 0;
-  }
-  __device__ __forceinline__ int nitems() const { return nfull + (k > 1 ? nunits() : (cid < R ? 1 : 0)); }
-  __device__ __forceinline__ bool is_unit(int i) const { return k > 1 && i >= nfull; }
-  __device__ __forceinline__ int unit(int i) const { return cid + (i - nfull) * ncl; }
-  __device__ __forceinline__ int rblk(int i) const { return unit(i) % R; }  // the unit's block in the partial round
-  __device__ __forceinline__ int block(int i) const {
-    return block0 + (i < nfull ? cid + i * ncl : nfull * ncl + (k > 1 ? rblk(i) : cid));
-  }
-  __device__ __forceinline__ int g0(int i) const { return is_unit(i) ? (unit(i) / R) * G / k : 0; }
-  __device__ __forceinline__ int g1(int i) const { return is_unit(i) ? (unit(i) / R + 1) * G / k : G; }
-  // The items normalised in a pass of their own right after compute item i
-  // (the last whole block before the units, and at the end every unit, or the
-  // last whole block): [qa, qb).  Any other item's norm is fused into the
-  // next item's chunks, which cover the same columns.
-  __device__ __forceinline__ void norm_after(int nit, int i, int& qa, int& qb) const {
-    qa = qb = 0;
-    if (i == nit - 1) {
-      qa = is_unit(i) ? nfull : i;
-      qb = nit;
-    } else if (!is_unit(i) && is_unit(i + 1)) {
-      qa = i;
-      qb = i + 1;
-    }
-  }
-  __device__ __forceinline__ bool fused(int i) const { return i > 0 && !is_unit(i); }
-};
-
-// Global workspace of the split partial round: per partial-round block r a row
-// of counters (s_x arrivals, s_x reads, one owner-arrival count per CTA rank),
-// per unit the s_x partials of each CTA and the owner CTAs' summed projections.
-constexpr int kMaxSplitBlocks = 64;
-constexpr int kMaxUnits = 128;
-constexpr int kCntStride = 32;
-constexpr size_t kSplitCntBytes = (size_t)kMaxSplitBlocks * kCntStride * 4;
-constexpr size_t kSplitSxFloats = (size_t)kMaxUnits * 16 * 32;  // [unit][rank][token]
-constexpr size_t kSplitPpFloats = (size_t)kMaxUnits * 32 * 32;  // [unit][rank * slots + slot][part]
-
-struct SplitWs {
-  unsigned* cnt;
-  float* sxp;
-  float* pp;
-  __device__ __forceinline__ SplitWs(char* w)
-      : cnt(reinterpret_cast<unsigned*>(w)),
-        sxp(reinterpret_cast<float*>(w + kSplitCntBytes)),
-        pp(reinterpret_cast<float*>(w + kSplitCntBytes) + kSplitSxFloats) {}
-};
-
-// Bounded wait for a global counter to reach `target` (acquire); the same
-// two tiers as the barrier waits.
-__device__ __forceinline__ bool wait_count(const Ctx& x, const unsigned* p, unsigned target) {
-  if (ld_acquire_gpu(p) >= target) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (ld_acquire_gpu(p) < target) {
-    if (*x.aborted) return false;
-    const uint64_t dt = globaltimer_ns() - t0;
-    if (dt > x.report_ns) report_slow(x);
-    if (dt > x.abort_ns) {
-      *x.aborted = 1;
-      return false;
-    }
-    __nanosleep(100);
-  }
-  return true;
-}
-
-}  // namespace
-
-// FORM: 0 no_post (R' = comb . R), 1 post (+ post (x) Y), 2 identity: the
-// first block's form, R' = R, no residual write.
-// OUT: 0 bf16 norm, 1 mxfp8 (+ e4m3 codes, e8m0 scales), 2 fp8_grid (+ the
-// quantisation dequantised to bf16)
-template <int FORM, int OUT, bool MS, int KCL>
-__global__ void __launch_bounds__(threads_of<OUT>(), 1)
-    stream_seam_kernel(const SeamArgs a, const __grid_constant__ CUtensorMap tmR,
-                       const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmRo,
-                       const __grid_constant__ CUtensorMap tmFn, const __grid_constant__ CUtensorMap tmN,
-                       const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmGc,
-                       const __grid_constant__ CUtensorMap tmGp, const __grid_constant__ CUtensorMap tmGq,
-                       int block0, int nfull, int R, int k_parts, int G_groups, char* wsx,
-                       unsigned long long report_ns, unsigned long long abort_ns) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  using G = Geo<KCL, OUT>;
-  constexpr uint32_t kOutStage = G::kOutStage;
-  constexpr int kThreads = threads_of<OUT>();
-  constexpr bool POST = FORM == 1, IDENT = FORM == 2;
-  constexpr int kNI = in_stages<FORM, KCL>();
-  constexpr uint32_t kInStageF = in_stage_bytes<FORM>();
-  static_assert(kNI <= kNIMax && kNI * kInStageF <= G::kInRing, "input ring");
-  constexpr int kCl = G::kCl, kSlots = G::kSlots;
-  constexpr uint32_t kOffIn = G::kOffIn, kXsBytes = G::kXsBytes, kRecvBytes = G::kRecvBytes;
-  typename G::Tail* tl = reinterpret_cast<typename G::Tail*>(sm + G::kOffTail);
-  const Ctx X{&a, &tl->reported, &tl->aborted, report_ns, abort_ns};
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t rank = cluster_ctarank();
-  const int H = a.H;
-  const int64_t T = a.T;
-  // CTA r owns the 64-column chunks r, r + KCL, r + 2 KCL, ... of H (group g
-  // holds chunks g KCL .. g KCL + KCL - 1): at any time the CTAs of a cluster
-  // touch adjacent 128-byte pieces of the same rows
-  const int n64 = H / kChunk;
-  const int nch = n64 > (int)rank ? (n64 - (int)rank + kCl - 1) / kCl : 0;
-  const int ncl = gridDim.x / kCl;
-  // the schedule's constants come from the host (they stay in the constant
-  // bank instead of registers): nfull whole rounds, R blocks left, k parts
-  // per left block (1 when R is 0), G column groups
-  Sched S;
-  S.cid = blockIdx.x / kCl;
-  S.ncl = ncl;
-  S.block0 = block0;
-  S.nfull = nfull;
-  S.R = R;
-  S.k = k_parts;
-  S.G = G_groups;
-  const int nit = S.nitems();
-  // chunks of this CTA in item i (a unit covers whole groups only)
-  auto nchi = [&](int i) { return S.is_unit(i) ? S.g1(i) - S.g0(i) : nch; };
-  // first tensor-memory x slot of item i (the units of a cluster side by side)
-  auto sbase = [&](int i) {
-    int s = 0;
-    for (int q = S.nfull; q < i; ++q) s += S.g1(q) - S.g0(q);
-    return S.is_unit(i) ? s : 0;
-  };
-  const SplitWs W(wsx);
-
-  if (tid == 0) {
-    for (int s = 0; s < kNI; ++s) {
-      mbar_init(&tl->in_full[s], 1);
-      mbar_init(&tl->in_empty[s], 8);
-    }
-    for (int s = 0; s < kNF; ++s) {
-      mbar_init(&tl->fn_full[s], 1);
-      mbar_init(&tl->fn_empty[s], MS ? 8 : 1);
-    }
-    for (int s = 0; s < kNO; ++s) {
-      mbar_init(&tl->out_full[s], 8);
-      mbar_init(&tl->out_empty[s], (MS ? 9 : 2) + (OUT == 2 ? 1 : 0));
-    }
-    mbar_init(&tl->d_full, 1);
-    for (int p = 0; p < 2; ++p) {
-      mbar_init(&tl->gates_full[p], 1);
-      mbar_init(&tl->gates_empty[p], 8);
-    }
-    mbar_init(&tl->dbuf_full, 4);  // the four D readers (or folders)
-    mbar_init(&tl->dbuf_free, 1);  // the exchange warp
-    mbar_init(&tl->d_free, 4);     // the four D readers
-    mbar_init(&tl->mma_fin, 1);
-    mbar_init(&tl->fold_full, 4);  // warps 4-7 (warp-MMA form)
-    for (int p = 0; p < 2; ++p) {
-      mbar_init(&tl->xs_full[p], 1);    // + kXsBytes of st.async from the cluster
-      mbar_init(&tl->recv_full[p], 1);  // + kRecvBytes of st.async from the cluster
-      mbar_init(&tl->recv_free[p], kCl);
-      mbar_init(&tl->red_full[p], 8);
-    }
-    tl->reported = 0;
-    tl->aborted = 0;
-    mbar_fence_init();
-  }
-  if (warp == 8 && lane == 0) {
-    prefetch_tmap(&tmR);
-    if (POST) prefetch_tmap(&tmY);
-    if (!IDENT) prefetch_tmap(&tmGc);
-    prefetch_tmap(&tmGp);
-    if (POST) prefetch_tmap(&tmGq);
-  }
-  if (warp == 10 && lane == 0) prefetch_tmap(&tmFn);
-  if (warp == 12 && lane == 0) {
-    if (!IDENT) prefetch_tmap(&tmRo);
-    prefetch_tmap(&tmN);
-    if (OUT == 1) prefetch_tmap(&tmC);
-  }
-  if (warp == 9) {
-    tmem_alloc(&tl->tmem_base, kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncwarp();
-  cluster_sync_all();  // barriers initialised in every CTA of the cluster
-  tc_fence_after();
-  const uint32_t tmem = tl->tmem_base;
-  // Programmatic dependent launch: everything above (barriers, tensor memory,
-  // the cluster barrier, tensor-map prefetch) may overlap the previous kernel
-  // on the stream; every read of global memory comes after this wait, which
-  // returns once that kernel has completed and its writes are visible.  The
-  // next kernel may then begin its own set-up while this one runs.
-  griddep_wait();
-  if (tid == 0) griddep_launch_dependents();
-  // gamma of this CTA's first chunks (groups), staged once (read by every item)
-  for (int i = tid; i < min(nch, G::kGamChunks) * 8; i += kThreads)
-    tl->gam[i >> 3][i & 7] = __ldg(reinterpret_cast<const uint4*>(a.gamma + ((i >> 3) * kCl + (int)rank) * kChunk) + (i & 7));
-  __syncthreads();
-
-  if (warp == 8) {
-    // --------------------------------------------------- input producer --
-    if (lane == 0) {
-      // evict-normal, not evict-first: measured 5 % faster (the neighbouring
-      // CTAs of the cluster read the other halves of the promoted 256-byte
-      // L2 lines at about the same time)
-      const uint64_t pol = l2_evict_normal();
-      const uint32_t bytes = (POST ? 5 : 4) * kRTile;
-      int j = 0, ng = 0;  // input-stage loads and gate loads issued
-      bool ok = true;
-      for (int i = 0; i < nit && ok; ++i) {
-        const int t0 = S.block(i) * kBM, gb = S.g0(i), ni = nchi(i);
-        // the item's carried gates, into buffer i % 2 once the item two
-        // before has finished with it
-        const int gbuf = i & 1;
-        if (!(ok = wait_local(X, &tl->gates_empty[gbuf], ((i >> 1) & 1) ^ 1))) break;
-        mbar_arrive_expect_tx(&tl->gates_full[gbuf], (IDENT ? 4 : POST ? 24 : 20) * kBM * 4);
-        if (!IDENT) tma_load_2d(&tl->gates[gbuf].comb[0][0], &tmGc, &tl->gates_full[gbuf], 0, t0, pol);
-        tma_load_2d(&tl->gates[gbuf].pre[0][0], &tmGp, &tl->gates_full[gbuf], 0, t0, pol);
-        if (POST) tma_load_2d(&tl->gates[gbuf].post[0][0], &tmGq, &tl->gates_full[gbuf], 0, t0, pol);
-        ++ng;
-        for (int c = 0; c < ni; ++c, ++j) {
-          const int s = j % kNI;
-          if (!(ok = wait_local(X, &tl->in_empty[s], ((j / kNI) & 1) ^ 1))) break;
-          uint8_t* st = sm + kOffIn + s * kInStageF;
-          const int h = ((gb + c) * kCl + (int)rank) * kChunk;
-          mbar_arrive_expect_tx(&tl->in_full[s], bytes);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) tma_load_3d(st + q * kRTile, &tmR, &tl->in_full[s], h, q, t0, pol);
-          if (POST) tma_load_2d(st + 4 * kRTile, &tmY, &tl->in_full[s], h, t0, pol);
-        }
-      }
-      // Every load issued lands before the CTA exits.  A stage is refilled
-      // only after all eight compute warps released it, and they release it
-      // only after seeing its previous load complete, so only the last load
-      // of each stage (and of each gate buffer) can still be in flight.
-      for (int jj = (j > kNI ? j - kNI : 0); jj < j; ++jj) drain(X, &tl->in_full[jj % kNI], (jj / kNI) & 1);
-      for (int q = (ng > 2 ? ng - 2 : 0); q < ng; ++q) drain(X, &tl->gates_full[q & 1], (q >> 1) & 1);
-    }
-  } else if (warp == 10) {
-    // ------------------------------------------------------ fn producer --
-    if (lane == 0) {
-      const uint64_t pol = l2_evict_last();
-      int j = 0;
-      bool ok = true;
-      for (int i = 0; i < nit && ok; ++i) {
-        const int gb = S.g0(i), ni = nchi(i);
-        for (int c = 0; c < ni; ++c, ++j) {
-          const int f = j % kNF;
-          if (!(ok = wait_local(X, &tl->fn_empty[f], ((j / kNF) & 1) ^ 1))) break;
-          uint8_t* st = sm + kOffFn + f * kFnStage;
-          const int h = ((gb + c) * kCl + (int)rank) * kChunk;
-          mbar_arrive_expect_tx(&tl->fn_full[f], kFnStage);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) tma_load_3d(st + q * kFnTile, &tmFn, &tl->fn_full[f], h, q, 0, pol);
-        }
-      }
-      // as for the input ring: only the last load of each fn stage can still be in flight
-      for (int jj = (j > kNF ? j - kNF : 0); jj < j; ++jj) drain(X, &tl->fn_full[jj % kNF], (jj / kNF) & 1);
-    }
-  } else if (warp == 9) {
-    // -------------------------------------- tcgen05 projection (one thread) --
-    if (!MS && lane == 0) {
-      int j = 0, jr = 0;
-      bool ok = true;
-      for (int i = 0; i < nit && ok; ++i) {
-        const int ni = nchi(i);
-        for (int c = 0; c < ni; ++c, ++j) {
-          const int o = j % kNO;
-          const int f = jr % kNF;
-          if (!(ok = wait_local(X, &tl->out_full[o], (j / kNO) & 1))) break;
-          // the first MMA of an item overwrites D: the previous item's D must have been read
-          if (c == 0 && i > 0 && !(ok = wait_local(X, &tl->d_free, (i - 1) & 1))) break;
-          if (!(ok = wait_local(X, &tl->fn_full[f], (jr / kNF) & 1))) break;
-          tc_fence_after();
-          const uint32_t ra = smem_u32(sm + kOffOut + o * kOutStage);   // R' of the 4 streams [128 x 64]
-          const uint32_t fb = smem_u32(sm + kOffFn + f * kFnStage);     // fn of the 4 streams [192 x 64]
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc_mma_bf16(tmem + kColD, sdesc_k_sw128(ra + kk * 32), sdesc_k_sw128(fb + kk * 32), kIdesc, (c | kk) != 0);
-          tc_commit(&tl->fn_empty[f]);
-          tc_commit(&tl->out_empty[o]);
-          if (c == ni - 1) tc_commit(&tl->d_full);
-          ++jr;
-        }
-        // normalise-only passes after this item: one stage per group of chunks, no MMA
-        int qa, qb;
-        S.norm_after(nit, i, qa, qb);
-        for (int q = qa; q < qb && ok; ++q) {
-          for (int c0 = 0; c0 < nchi(q); c0 += norm_group<OUT>(), ++j) {
-            if (!(ok = wait_local(X, &tl->out_full[j % kNO], (j / kNO) & 1))) break;
-            mbar_arrive(&tl->out_empty[j % kNO]);
-          }
-        }
-      }
-      // every MMA issued (and the commits before it) completes before the CTA
-      // exits and tensor memory is freed
-      tc_commit(&tl->mma_fin);
-      drain(X, &tl->mma_fin, 0);
-    }
-  } else if (warp == 12) {
-    // ---------------------------- stores: R' tiles, norm tile, e4m3 codes --
-    // (no norm pointer: the first pass of the unshifted ordering, which keeps
-    // R' and the gates only)
-    const bool store_norm = a.norm != nullptr;
-    int j = 0;
-    // lane = token: the ue8m0 codes of one norm tile (two 32-column groups)
-    auto quant_tile = [&](const uint8_t* nt, uint8_t* ct, int64_t tp, int h) {
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t nb[16];
-#pragma unroll
-        for (int jq = 0; jq < 4; ++jq) {
-          const int ch = 4 * half + jq;
-          uint4 v = *reinterpret_cast<const uint4*>(nt + lane * 128 + ((ch ^ (lane & 7)) << 4));
-          nb[4 * jq] = v.x; nb[4 * jq + 1] = v.y; nb[4 * jq + 2] = v.z; nb[4 * jq + 3] = v.w;
-        }
-        uint32_t cw[8];
-        const uint8_t sb = quant_group32(nb, cw, a.amax_floor);
-        uint4* cd = reinterpret_cast<uint4*>(ct + lane * 64 + 32 * half);
-        cd[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-        cd[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-        const int64_t tt = tp + lane;
-        if (tt < T) a.scales[tt * (H / 32) + (h + 32 * half) / 32] = sb;
-      }
-    };
-    bool ok = true;
-    for (int i = 0; i < nit && ok; ++i) {
-      const bool prev = S.fused(i);
-      const int t0 = S.block(i) * kBM, tp = prev ? S.block(i - 1) * kBM : 0, gb = S.g0(i), ni = nchi(i);
-      for (int c = 0; c < ni; ++c, ++j) {
-        const int o = j % kNO;
-        uint8_t* ost = sm + kOffOut + o * kOutStage;
-        const int h = ((gb + c) * kCl + (int)rank) * kChunk;
-        if (!(ok = wait_warp(X, &tl->out_full[o], (j / kNO) & 1))) break;
-        if (OUT == 1 && prev) {
-          quant_tile(ost + kOffNormT, ost + kOffCodesT, tp, h);
-          fence_proxy_async_smem();
-          __syncwarp();
-        }
-        if (lane == 0) {
-          if (!IDENT) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) tma_store_3d(&tmRo, ost + q * kRTile, h, q, t0);
-          }
-          if (prev) {
-            if (store_norm) tma_store_2d(&tmN, ost + kOffNormT, h, tp);
-            if (OUT == 1) tma_store_2d(&tmC, ost + kOffCodesT, h, tp);
-          }
-          tma_store_commit();
-          tma_store_wait_read_all();
-        }
-        if (lane == 0) mbar_arrive(&tl->out_empty[o]);
-        __syncwarp();
-      }
-      if (!ok) break;
-      // normalise-only passes: the norm tiles of a group of chunks per stage
-      int qa, qb;
-      S.norm_after(nit, i, qa, qb);
-      constexpr int NG = norm_group<OUT>();
-      for (int q = qa; q < qb && ok; ++q) {
-        const int tq = S.block(q) * kBM, gq = S.g0(q), nq = nchi(q);
-        for (int c0 = 0; c0 < nq; c0 += NG, ++j) {
-          const int o = j % kNO;
-          uint8_t* ost = sm + kOffOut + o * kOutStage;
-          if (!(ok = wait_warp(X, &tl->out_full[o], (j / kNO) & 1))) break;
-          const int ng = min(NG, nq - c0);
-          if (OUT == 1) {  // codes tiles in stage slot 4
-            for (int g = 0; g < ng; ++g)
-              quant_tile(ost + g * kRTile, ost + kOffNormT + g * 2048, tq, ((gq + c0 + g) * kCl + (int)rank) * kChunk);
-            fence_proxy_async_smem();
-            __syncwarp();
-          }
-          if (lane == 0) {
-            for (int g = 0; g < ng; ++g) {
-              const int h = ((gq + c0 + g) * kCl + (int)rank) * kChunk;
-              if (store_norm) tma_store_2d(&tmN, ost + g * kRTile, h, tq);
-              if (OUT == 1) tma_store_2d(&tmC, ost + kOffNormT + g * 2048, h, tq);
-            }
-            tma_store_commit();
-            tma_store_wait_read_all();
-            mbar_arrive(&tl->out_empty[o]);
-          }
-          __syncwarp();
-        }
-      }
-    }
-    // every bulk store issued has read its shared memory and written global
-    // memory before the CTA exits (the hardware wait always ends)
-    if (lane == 0) tma_store_wait_all();
-  } else if (OUT == 2 && warp >= 13) {
-    // ------------------------------------------------------ grid warps --
-    // fp8_grid: warp 13 + o reads the norm tiles of output stage o and writes
-    // their grid (bf16 of the dequantised e4m3 codes) straight to global
-    // memory; the stage is free again once it has read them.
-    const int me = warp - 13;
-    // lane = token: one norm tile row (64 bf16) into registers, so the stage
-    // can be released before the grid is computed from them
-    auto load_row = [&](const uint8_t* nt, uint32_t* nb) {
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        const uint4 v = *reinterpret_cast<const uint4*>(nt + lane * 128 + ((ch ^ (lane & 7)) << 4));
-        nb[4 * ch] = v.x; nb[4 * ch + 1] = v.y; nb[4 * ch + 2] = v.z; nb[4 * ch + 3] = v.w;
-      }
-    };
-    // the grid row of token tp + lane, columns h .. h + 63, straight from
-    // registers, one 32-group at a time: each lane writes its own 128
-    // contiguous bytes
-    auto grid_row = [&](int64_t tp, int h, const uint32_t* nb) {
-      const int64_t tt = tp + lane;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t gw[16];
-        grid_group32(nb + 16 * half, gw, a.amax_floor);
-        if (tt < T) {
-          uint4* dst = reinterpret_cast<uint4*>(a.grid + tt * H + h + 32 * half);
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch) st_stream(dst + ch, make_uint4(gw[4 * ch], gw[4 * ch + 1], gw[4 * ch + 2], gw[4 * ch + 3]));
-        }
-      }
-    };
-    int j = 0;
-    bool ok = true;
-    for (int i = 0; i < nit && ok; ++i) {
-      const bool prev = S.fused(i);
-      const int64_t tp = prev ? (int64_t)S.block(i - 1) * kBM : 0;
-      const int gb = S.g0(i), ni = nchi(i);
-      for (int c = 0; c < ni; ++c, ++j) {
-        const int o = j % kNO;
-        if (o != me) continue;
-        const uint8_t* ost = sm + kOffOut + o * kOutStage;
-        if (!(ok = wait_warp(X, &tl->out_full[o], (j / kNO) & 1))) break;
-        uint32_t nb[32];
-        if (prev) load_row(ost + kOffNormT, nb);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tl->out_empty[o]);
-        if (prev) grid_row(tp, ((gb + c) * kCl + (int)rank) * kChunk, nb);
-      }
-      if (!ok) break;
-      // normalise-only passes: the norm tiles of a group of chunks per stage
-      int qa, qb;
-      S.norm_after(nit, i, qa, qb);
-      constexpr int NG = norm_group<OUT>();
-      for (int q = qa; q < qb && ok; ++q) {
-        const int64_t tq = (int64_t)S.block(q) * kBM;
-        const int gq = S.g0(q), nq = nchi(q);
-        for (int c0 = 0; c0 < nq; c0 += NG, ++j) {
-          const int o = j % kNO;
-          if (o != me) continue;
-          const uint8_t* ost = sm + kOffOut + o * kOutStage;
-          if (!(ok = wait_warp(X, &tl->out_full[o], (j / kNO) & 1))) break;
-          const int ng = min(NG, nq - c0);
-          for (int g = 0; g < ng; ++g) {
-            uint32_t nb[32];
-            load_row(ost + g * kRTile, nb);
-            __syncwarp();
-            if (g == ng - 1 && lane == 0) mbar_arrive(&tl->out_empty[o]);
-            grid_row(tq, ((gq + c0 + g) * kCl + (int)rank) * kChunk, nb);
-          }
-        }
-      }
-    }
-  } else if (warp == 11) {
-    // ------------------------------------ exchange and gate finish warp --
-    // Per item: (1) this CTA's s_x partials to every CTA of the cluster (each
-    // forms rstd_x itself), (2) the 24 projections and s_R of each token to
-    // its owner CTA (token % KCL), (3) the gates of the tokens this CTA owns.
-    // Sends are st.async completing bytes on the receiver's mbarrier; the
-    // compute warps only hand their partials over and go on.  recv_free keeps
-    // the partials of item i + 2 out of a slot until every owner has read
-    // item i from it.  A unit (a column part of a block) also publishes its
-    // s_x partials and its owners' sums in the global workspace; the owner
-    // that completes a block's parts last finishes its tokens' gates.
-    if (lane < 27) tl->ab[lane] = lane < 3 ? a.alpha[lane] : a.bias[lane - 3];
-    __syncwarp();
-    for (int i = 0; i < nit; ++i) {
-      const int b = S.block(i), par = i & 1;
-      const bool unit = S.is_unit(i);
-      if (!wait_warp(X, &tl->red_full[par], (i >> 1) & 1)) break;
-      float sx = 0.f, sR = 0.f;
-#pragma unroll
-      for (int w = 0; w < 8; ++w) {
-        const float2 v = tl->red[par][w][lane];
-        sR += v.x;
-        sx += v.y;
-      }
-      if (unit) {  // this CTA's s_x partials of the unit, for every part's rstd_x
-        const int u = S.unit(i), r = S.rblk(i);
-        W.sxp[(u * kCl + (int)rank) * 32 + lane] = sx;
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) atomicAdd(&W.cnt[r * kCntStride], 1u);
-      }
-      if (lane == 0) mbar_arrive_expect_tx(&tl->xs_full[par], kXsBytes);
-      {
-        const uint32_t xa = smem_u32(&tl->xs[par][rank][lane]), xb = smem_u32(&tl->xs_full[par]);
-#pragma unroll
-        for (int dst = 0; dst < kCl; ++dst)
-          st_async_f32(mapa_shared(xa, (uint32_t)dst), sx, mapa_shared(xb, (uint32_t)dst));
-      }
-      if (!wait_warp(X, &tl->dbuf_full, i & 1)) break;
-      if (i >= 2 && !wait_warp_remote(X, &tl->recv_free[par], ((i >> 1) & 1) ^ 1)) break;
-      {
-        const uint32_t dst = (uint32_t)(lane % kCl);
-        const uint32_t ra = mapa_shared(smem_u32(&tl->recv[par][rank][lane / kCl][0]), dst);
-        const uint32_t rb = mapa_shared(smem_u32(&tl->recv_full[par]), dst);
-#pragma unroll
-        for (int k = 0; k < 24; k += 2) {
-          float s0 = tl->dbuf[0][lane][k], s1 = tl->dbuf[0][lane][k + 1];
-#pragma unroll
-          for (int q = 1; q < 4; ++q) {
-            s0 += tl->dbuf[q][lane][k];
-            s1 += tl->dbuf[q][lane][k + 1];
-          }
-          st_async_v2(ra + 4 * k, s0, s1, rb);
-        }
-        st_async_f32(ra + 4 * 24, sR, rb);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tl->dbuf_free);
-
-      if (lane == 0) mbar_arrive_expect_tx(&tl->recv_full[par], kRecvBytes);
-      if (!wait_warp(X, &tl->recv_full[par], (i >> 1) & 1)) break;
-      // sums over the cluster, one (owned token, part) pair per lane and round
-      for (int e = lane; e < kSlots * kOwnerParts; e += 32) {
-        const int sl = e / kOwnerParts, k = e - sl * kOwnerParts;
-        float s = 0.f;
-#pragma unroll
-        for (int src = 0; src < kCl; ++src) s += tl->recv[par][src][sl][k];
-        tl->pbuf[sl][k] = s;
-      }
-      __syncwarp();
-      if (lane < kCl) mbar_arrive_remote(mapa_shared(smem_u32(&tl->recv_free[par]), lane));
-      if (!unit) {
-        if (lane < kSlots) {
-          const int64_t tt = (int64_t)b * kBM + (int)rank + kCl * lane;
-          if (tt < T) finish_store_gates(a, tt, &tl->pbuf[lane][0], tl->ab, H);
-        }
-      } else {
-        // publish this owner's sums of the unit; the owner completing the
-        // block's k parts last adds them (parts in order, so the result does
-        // not depend on who is last) and finishes its tokens' gates
-        const int u = S.unit(i), r = S.rblk(i);
-        for (int e = lane; e < kSlots * kOwnerParts; e += 32) {
-          const int sl = e / kOwnerParts, k = e - sl * kOwnerParts;
-          W.pp[((size_t)u * 32 + (int)rank * kSlots + sl) * 32 + k] = tl->pbuf[sl][k];
-        }
-        __threadfence();
-        __syncwarp();
-        unsigned old = 0;
-        if (lane == 0) old = atom_add_acq_rel_gpu(&W.cnt[r * kCntStride + 2 + (int)rank], 1u);
-        old = __shfl_sync(0xffffffffu, old, 0);
-        if (old == (unsigned)S.k - 1) {
-          (void)ld_acquire_gpu(&W.cnt[r * kCntStride + 2 + (int)rank]);
-          for (int e = lane; e < kSlots * kOwnerParts; e += 32) {
-            const int sl = e / kOwnerParts, k = e - sl * kOwnerParts;
-            float s = 0.f;
-            for (int p = 0; p < S.k; ++p)
-              s += __ldcg(&W.pp[((size_t)(p * S.R + r) * 32 + (int)rank * kSlots + sl) * 32 + k]);
-            tl->pbuf[sl][k] = s;
-          }
-          __syncwarp();
-          if (lane < kSlots) {
-            const int64_t tt = (int64_t)b * kBM + (int)rank + kCl * lane;
-            if (tt < T) finish_store_gates(a, tt, &tl->pbuf[lane][0], tl->ab, H);
-          }
-          if (lane == 0) W.cnt[r * kCntStride + 2 + (int)rank] = 0;  // every part has arrived: reset for the next call
-        }
-      }
-      __syncwarp();
-    }
-  } else if (warp < 8) {
-    // ---------------------------------------------------- compute warps --
-    const int q4 = warp & 3, wq = warp >> 2;
-    const uint32_t colx = MS ? 0u : kDCols;
-    const uint32_t xaddr = tmem + ((uint32_t)(32 * q4) << 16) + colx + 8 * wq;
-    const uint32_t off = lane * 128 + ((warp ^ (lane & 7)) << 4);  // row = token, 16-byte chunk = warp
-    // gamma of the 8 columns of this warp in chunk c of group g
-    auto gamma8 = [&](int g) -> uint4 {
-      return g < G::kGamChunks ? tl->gam[g][warp]
-                               : __ldg(reinterpret_cast<const uint4*>(a.gamma + (g * kCl + (int)rank) * kChunk + 8 * warp));
-    };
-    // Warp-level projection (MS): warp w owns stream w % 4 and the 32 columns
-    // [32 (w / 4), +32) of every chunk: D[32 tokens x 24 logits] += R'[32 x 32]
-    // . (fn_hi + fn_lo)[32 x 24], m16n8k16 MMAs with fp32 accumulation, one
-    // chunk behind the R' writes of all eight warps.
-    float acc[2][3][4];
-    auto mma_chunk = [&](int jj, int jr) -> bool {
-      const int oo = jj % kNO, ff = jr % kNF;
-      if (!wait_warp(X, &tl->out_full[oo], (jj / kNO) & 1)) return false;
-      if (!wait_warp(X, &tl->fn_full[ff], (jr / kNF) & 1)) return false;
-      const uint32_t rt = smem_u32(sm + kOffOut + oo * kOutStage + (warp & 3) * kRTile);
-      const uint32_t ft = smem_u32(sm + kOffFn + ff * kFnStage + (warp & 3) * kFnTile);
-      const int mi = lane >> 3, rr = lane & 7;
-#pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-        const int kg = 2 * (warp >> 2) + kk;  // 16-column group of the chunk
-        uint32_t af[2][4], bq[3][4];
-#pragma unroll
-        for (int m = 0; m < 2; ++m) {
-          const int row = 16 * m + (mi & 1) * 8 + rr, ch = 2 * kg + (mi >> 1);
-          ldmatrix_x4(rt + row * 128 + ((ch ^ rr) << 4), af[m][0], af[m][1], af[m][2], af[m][3]);
-        }
-#pragma unroll
-        for (int pq = 0; pq < 3; ++pq) {  // fn rows 16 pq .. 16 pq + 15 (n8 tiles 2 pq, 2 pq + 1)
-          const int row = 16 * pq + (mi >> 1) * 8 + rr, ch = 2 * kg + (mi & 1);
-          ldmatrix_x4(ft + row * 128 + ((ch ^ rr) << 4), bq[pq][0], bq[pq][1], bq[pq][2], bq[pq][3]);
-        }
-#pragma unroll
-        for (int m = 0; m < 2; ++m) {
-#pragma unroll
-          for (int n = 0; n < 3; ++n) {
-            const int th = n, tlo = 3 + n;  // hi and lo rows of logits 8n .. 8n + 7
-            mma_bf16_16816(acc[m][n], af[m][0], af[m][1], af[m][2], af[m][3], bq[th >> 1][2 * (th & 1)],
-                           bq[th >> 1][2 * (th & 1) + 1]);
-            mma_bf16_16816(acc[m][n], af[m][0], af[m][1], af[m][2], af[m][3], bq[tlo >> 1][2 * (tlo & 1)],
-                           bq[tlo >> 1][2 * (tlo & 1) + 1]);
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&tl->out_empty[oo]);
-        mbar_arrive(&tl->fn_empty[ff]);
-      }
-      return true;
-    };
-
-    float rprev = 0.f;
-    // rstd_x of item q from the s_x partials the CTAs of the cluster sent (same
-    // sum order in every CTA, so all hold the same value); for a unit, from the
-    // partials every CTA of every part of its block published
-    auto take_rstd = [&](int q) -> bool {
-      const int pp = q & 1;
-      if (!wait_warp(X, &tl->xs_full[pp], (q >> 1) & 1)) return false;
-      float sx = 0.f;
-#pragma unroll
-      for (int src = 0; src < kCl; ++src) sx += tl->xs[pp][src][lane];
-      if (S.is_unit(q)) {
-        const int r = S.rblk(q);
-        const unsigned target = (unsigned)(S.k * kCl);
-        if (!__all_sync(0xffffffffu, wait_count(X, &W.cnt[r * kCntStride], target))) return false;
-        sx = 0.f;
-        for (int p = 0; p < S.k; ++p)
-#pragma unroll
-          for (int src = 0; src < kCl; ++src) sx += __ldcg(&W.sxp[((p * S.R + r) * kCl + src) * 32 + lane]);
-        __syncwarp();
-        if (lane == 0) {  // the last of the block's readers resets its counters for the next call
-          const unsigned old = atomicAdd(&W.cnt[r * kCntStride + 1], 1u);
-          if (old == target * 8 - 1) {
-            W.cnt[r * kCntStride] = 0;
-            W.cnt[r * kCntStride + 1] = 0;
-          }
-        }
-      }
-      const int64_t tt = (int64_t)S.block(q) * kBM + lane;
-      rprev = tt < T ? 1.0f / sqrtf(sx / (float)H + a.eps) : 0.f;
-      return true;
-    };
-
-    // tcgen05 projection: warp q4 reads stream q4's diagonal block of item
-    // ip's D (TMEM lanes 32 q4 .., columns 48 q4 .. 48 q4 + 47) during the
-    // next item's first chunk, frees D for that item's MMAs, and hands the
-    // hi + lo sums to the exchange warp through dbuf.
-    auto read_d = [&](int ip) -> bool {
-      float dv[48];
-      if (nchi(ip) > 0) {
-        if (!wait_warp(X, &tl->d_full, ip & 1)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < 6; ++k)
-          tc_ld_x8(tmem + ((uint32_t)(32 * warp) << 16) + kColD + 48 * warp + 8 * k, dv + 8 * k);
-      } else {
-#pragma unroll
-        for (int k = 0; k < 48; ++k) dv[k] = 0.f;
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tl->d_free);
-      if (!wait_warp(X, &tl->dbuf_free, (ip & 1) ^ 1)) return false;
-      float* r0 = &tl->dbuf[warp][lane][0];
-#pragma unroll
-      for (int k = 0; k < 24; ++k) r0[k] = dv[k] + dv[24 + k];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tl->dbuf_full);
-      return true;
-    };
-
-    int j = 0, ji = 0;
-    bool ok = true;
-    for (int i = 0; i < nit && ok; ++i) {
-      const bool prev = S.fused(i);  // this item's chunks normalise the previous item's x (same columns)
-      const int ni = nchi(i), gb = S.g0(i), sb = sbase(i);
-      float2 comb2[16], post2[4], pre2[4];  // each gate duplicated for the fp32x2 FMAs
-      {
-        float4 gc[4], gp = make_float4(0.f, 0.f, 0.f, 0.f), gq = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) gc[k] = gp;
-        {  // rows past T arrive as zeros; the buffer is released at the item's end
-          if (!(ok = wait_warp(X, &tl->gates_full[i & 1], (i >> 1) & 1))) break;
-          const GateTile& gt = tl->gates[i & 1];
-          if (!IDENT) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) gc[k] = *reinterpret_cast<const float4*>(&gt.comb[lane][4 * k]);
-          }
-          gp = *reinterpret_cast<const float4*>(&gt.pre[lane][0]);
-          if (POST) gq = *reinterpret_cast<const float4*>(&gt.post[lane][0]);
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          comb2[4 * k] = make_float2(gc[k].x, gc[k].x); comb2[4 * k + 1] = make_float2(gc[k].y, gc[k].y);
-          comb2[4 * k + 2] = make_float2(gc[k].z, gc[k].z); comb2[4 * k + 3] = make_float2(gc[k].w, gc[k].w);
-        }
-        pre2[0] = make_float2(gp.x, gp.x); pre2[1] = make_float2(gp.y, gp.y);
-        pre2[2] = make_float2(gp.z, gp.z); pre2[3] = make_float2(gp.w, gp.w);
-        post2[0] = make_float2(gq.x, gq.x); post2[1] = make_float2(gq.y, gq.y);
-        post2[2] = make_float2(gq.z, gq.z); post2[3] = make_float2(gq.w, gq.w);
-      }
-      float2 sR2 = make_float2(0.f, 0.f), sx2 = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int m = 0; m < 2; ++m)
-#pragma unroll
-        for (int n = 0; n < 3; ++n)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc[m][n][e] = 0.f;
-
-      for (int c = 0; c < ni; ++c, ++j) {
-        const int o = j % kNO;
-        uint32_t ow[4][4];
-        float x[8];
-        // the previous item's x and gamma of these columns, fetched now so
-        // their latency hides behind this chunk's post-mix
-        uint32_t xr[8];
-        uint4 gv = make_uint4(0, 0, 0, 0);
-        if (prev) {
-          tc_ld_x8_issue(xaddr + 16 * c, xr);
-          gv = gamma8(gb + c);
-        }
-        {
-          const int s = ji % kNI;
-          if (!(ok = wait_warp(X, &tl->in_full[s], (ji / kNI) & 1))) break;
-          const uint8_t* st = sm + kOffIn + s * kInStageF;
-          uint4 rin[4], yin = make_uint4(0, 0, 0, 0);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) rin[q] = *reinterpret_cast<const uint4*>(st + q * kRTile + off);
-          if (POST) yin = *reinterpret_cast<const uint4*>(st + 4 * kRTile + off);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&tl->in_empty[s]);
-          ++ji;
-          // two columns at a time with packed fp32x2 FMAs (each half rounds like a scalar FMA)
-#pragma unroll
-          for (int wd = 0; wd < 4; ++wd) {
-            const float2 r0 = bf16pair((&rin[0].x)[wd]), r1 = bf16pair((&rin[1].x)[wd]);
-            const float2 r2 = bf16pair((&rin[2].x)[wd]), r3 = bf16pair((&rin[3].x)[wd]);
-            const float2 yy = bf16pair((&yin.x)[wd]);
-            float2 xx = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint32_t w;
-              if (IDENT) {
-                w = (&rin[q].x)[wd];  // R' = R, bit for bit
-              } else {
-                float2 v = __fmul2_rn(comb2[4 * q], r0);
-                v = __ffma2_rn(comb2[4 * q + 1], r1, v);
-                v = __ffma2_rn(comb2[4 * q + 2], r2, v);
-                v = __ffma2_rn(comb2[4 * q + 3], r3, v);
-                if (POST) v = __ffma2_rn(post2[q], yy, v);
-                w = pack_bf16x2(v.x, v.y);
-              }
-              ow[q][wd] = w;
-              const float2 rr2 = bf16pair(w);
-              sR2 = __ffma2_rn(rr2, rr2, sR2);
-              xx = __ffma2_rn(pre2[q], rr2, xx);
-            }
-            x[2 * wd] = xx.x;
-            x[2 * wd + 1] = xx.y;
-            sx2 = __ffma2_rn(xx, xx, sx2);
-          }
-        }
-        if (prev && c == 0 && !(ok = take_rstd(i - 1))) break;
-        if (!(ok = wait_warp(X, &tl->out_empty[o], ((j / kNO) & 1) ^ 1))) break;
-        uint8_t* ost = sm + kOffOut + o * kOutStage;
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          *reinterpret_cast<uint4*>(ost + q * kRTile + off) = make_uint4(ow[q][0], ow[q][1], ow[q][2], ow[q][3]);
-        if (prev) {  // norm of the previous item's x in these columns, before x is overwritten
-          float xv[8], gm[8];
-          tc_wait_ld_x8(xr);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) xv[e] = __uint_as_float(xr[e]);
-          unpack8(gv, gm);
-          uint4 nv;
-          nv.x = pack_bf16x2(xv[0] * rprev * gm[0], xv[1] * rprev * gm[1]);
-          nv.y = pack_bf16x2(xv[2] * rprev * gm[2], xv[3] * rprev * gm[3]);
-          nv.z = pack_bf16x2(xv[4] * rprev * gm[4], xv[5] * rprev * gm[5]);
-          nv.w = pack_bf16x2(xv[6] * rprev * gm[6], xv[7] * rprev * gm[7]);
-          *reinterpret_cast<uint4*>(ost + kOffNormT + off) = nv;
-        }
-        tc_st_x8(xaddr + 16 * (sb + c), x);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tl->out_full[o]);
-        if (!MS && i > 0 && c == 0 && warp < 4 && !(ok = read_d(i - 1))) break;
-        if (MS && c > 0 && !(ok = mma_chunk(j - 1, ji - 2))) break;
-      }
-      if (!ok) break;
-      if (i > 0 && ni == 0) {  // no columns here: only consume the phases
-        if (prev && !(ok = take_rstd(i - 1))) break;
-        if (!MS && warp < 4 && !(ok = read_d(i - 1))) break;
-      }
-      if (MS && ni > 0 && !(ok = mma_chunk(j - 1, ji - 1))) break;
-      tc_wait_st();
-
-      // ------------- item finish: hand the partials to the exchange warp --
-      const int par = i & 1;
-      tl->red[par][warp][lane] = make_float2(sR2.x + sR2.y, sx2.x + sx2.y);
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&tl->red_full[par]);
-        // the item's gate buffer may now be refilled (for item i + 2): no read
-        // of it can still be pending, however the gates were kept or re-read
-        mbar_arrive(&tl->gates_empty[i & 1]);
-      }
-      // no MMA follows the last item: its D is read now
-      if (!MS && i == nit - 1 && warp < 4 && !(ok = read_d(i))) break;
-      if (MS) {  // warps w and w + 4 both hold stream w % 4: fold them into dbuf[w % 4]
-        const int g = lane >> 2, t4 = lane & 3;
-        if (warp >= 4) {
-          if (!(ok = wait_warp(X, &tl->dbuf_free, (i & 1) ^ 1))) break;
-#pragma unroll
-          for (int m = 0; m < 2; ++m) {
-#pragma unroll
-            for (int n = 0; n < 3; ++n) {
-              float* r0 = &tl->dbuf[warp - 4][16 * m + g][8 * n + 2 * t4];
-              r0[0] = acc[m][n][0];
-              r0[1] = acc[m][n][1];
-              r0[8 * kDPad] = acc[m][n][2];
-              r0[8 * kDPad + 1] = acc[m][n][3];
-            }
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&tl->fold_full);
-        } else {
-          if (!(ok = wait_warp(X, &tl->fold_full, i & 1))) break;
-#pragma unroll
-          for (int m = 0; m < 2; ++m) {
-#pragma unroll
-            for (int n = 0; n < 3; ++n) {
-              float* r0 = &tl->dbuf[warp][16 * m + g][8 * n + 2 * t4];
-              r0[0] += acc[m][n][0];
-              r0[1] += acc[m][n][1];
-              r0[8 * kDPad] += acc[m][n][2];
-              r0[8 * kDPad + 1] += acc[m][n][3];
-            }
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&tl->dbuf_full);
-        }
-      }
-
-      // ------------- normalise-only passes: the norm tiles of a group of
-      // chunks per output stage (the last whole block before the units, and
-      // at the end every unit or the last whole block)
-      int qa, qb;
-      S.norm_after(nit, i, qa, qb);
-      constexpr int NG = norm_group<OUT>();
-      for (int q = qa; q < qb && ok; ++q) {
-        if (!(ok = take_rstd(q))) break;
-        const int nq = nchi(q), gq = S.g0(q), sq = sbase(q);
-        for (int c0 = 0; c0 < nq; c0 += NG, ++j) {
-          const int o = j % kNO;
-          if (!(ok = wait_warp(X, &tl->out_empty[o], ((j / kNO) & 1) ^ 1))) break;
-          uint8_t* ost = sm + kOffOut + o * kOutStage;
-          const int ng = min(NG, nq - c0);
-          for (int g = 0; g < ng; ++g) {
-            const int c = c0 + g;
-            uint32_t xr[8];
-            tc_ld_x8_issue(xaddr + 16 * (sq + c), xr);
-            const uint4 gv = gamma8(gq + c);
-            tc_wait_ld_x8(xr);
-            float xv[8], gm[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) xv[e] = __uint_as_float(xr[e]);
-            unpack8(gv, gm);
-            uint4 nv;
-            nv.x = pack_bf16x2(xv[0] * rprev * gm[0], xv[1] * rprev * gm[1]);
-            nv.y = pack_bf16x2(xv[2] * rprev * gm[2], xv[3] * rprev * gm[3]);
-            nv.z = pack_bf16x2(xv[4] * rprev * gm[4], xv[5] * rprev * gm[5]);
-            nv.w = pack_bf16x2(xv[6] * rprev * gm[6], xv[7] * rprev * gm[7]);
-            *reinterpret_cast<uint4*>(ost + g * kRTile + off) = nv;
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&tl->out_full[o]);
-          if (MS) {  // the warp-level projection warps count in the stage's release
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tl->out_empty[o]);
-          }
-        }
-      }
-    }
-    // no tensor-memory load or store of this warp is outstanding at exit
-    tc_wait_ld();
-    tc_wait_st();
-  }
-
-  tc_fence_before();
-  __syncwarp();
-  // No CTA leaves while a peer may still write into it: every CTA arrives here
-  // after its last send, and the cluster barrier's release/acquire orders the
-  // peers' stores into this CTA before it goes on.
-  cluster_sync_all();
-  if (*X.aborted) {
-    // A CTA that abandoned the call may not have seen every partial a peer
-    // sent it arrive on its barriers: before its shared memory is released it
-    // also waits a fixed 20 us, far longer than a store into a cluster peer
-    // takes to land.
-    const uint64_t t0 = globaltimer_ns();
-    while (globaltimer_ns() - t0 < 20000) {
-    }
-  }
-  if (warp == 9) {
-    tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
-  }
-}
+// The variants with the wave-edge split (mhc_stream_split.cu).
+void* stream_kernel_ptr_split(int form, int out, bool ms, int kcl);
 
 // ------------------------------------------------------------- host side --
-template <int FORM, bool MS, int KCL>
-static void* kptr_f(int out) {
-  return out == 2 ? (void*)stream_seam_kernel<FORM, 2, MS, KCL>
-                  : out == 1 ? (void*)stream_seam_kernel<FORM, 1, MS, KCL> : (void*)stream_seam_kernel<FORM, 0, MS, KCL>;
-}
-template <bool MS, int KCL>
-static void* kptr_(int form, int out) {
-  return form == 2 ? kptr_f<2, MS, KCL>(out) : form == 1 ? kptr_f<1, MS, KCL>(out) : kptr_f<0, MS, KCL>(out);
-}
 // form: 0 no_post, 1 post, 2 identity.  Clusters of 16 run only the tcgen05
 // projection (at most 8 chunks per CTA).
-static void* stream_kernel_ptr(int form, int out, bool ms, int kcl) {
-  if (kcl == 16) return kptr_<false, 16>(form, out);
-  return ms ? kptr_<true, 4>(form, out) : kptr_<false, 4>(form, out);
+static void* stream_kernel_ptr(int form, int out, bool ms, int kcl, bool split) {
+  return split ? stream_kernel_ptr_split(form, out, ms, kcl) : stream_kernel_ptr_t<false>(form, out, ms, kcl);
 }
 static size_t smem_bytes(int kcl, int out) {
   if (kcl == 16)
@@ -1190,11 +23,11 @@ static size_t smem_bytes(int kcl, int out) {
 }
 
 cudaError_t stream_init() {
-  for (int p = 0; p < 3; ++p)        // form
-    for (int m = 0; m < 3; ++m)      // out mode
-      for (int v = 0; v < 3; ++v) {  // v: 0 tcgen05 / 4, 1 warp MMA / 4, 2 tcgen05 / 16
-        const int kcl = v == 2 ? 16 : 4;
-        void* k = stream_kernel_ptr(p, m, v == 1, kcl);
+  for (int p = 0; p < 3; ++p)          // form
+    for (int m = 0; m < 3; ++m)        // out mode
+      for (int v = 0; v < 6; ++v) {    // v % 3: 0 tcgen05 / 4, 1 warp MMA / 4, 2 tcgen05 / 16; v / 3: split
+        const int kcl = v % 3 == 2 ? 16 : 4;
+        void* k = stream_kernel_ptr(p, m, v % 3 == 1, kcl, v >= 3);
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes(kcl, m));
         if (e == cudaSuccess && kcl == 16) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
@@ -1244,11 +77,11 @@ static bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void*
 }
 
 // Clusters that fit at once, per device and kernel variant (queried once).
-static int max_clusters(int form, int out, bool ms, int kcl) {
-  static int cache[27][64] = {};
+static int max_clusters(int form, int out, bool ms, int kcl, bool split) {
+  static int cache[54][64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  const int v = form + 3 * out + 9 * (kcl == 16 ? 2 : (ms ? 1 : 0));
+  const int v = form + 3 * out + 9 * (kcl == 16 ? 2 : (ms ? 1 : 0)) + (split ? 27 : 0);
   if (cache[v][dev] > 0) return cache[v][dev];
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -1262,7 +95,7 @@ static int max_clusters(int form, int out, bool ms, int kcl) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, stream_kernel_ptr(form, out, ms, kcl), &cfg) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveClusters(&n, stream_kernel_ptr(form, out, ms, kcl, split), &cfg) != cudaSuccess) return 0;
   cache[v][dev] = n;
   return n;
 }
@@ -1276,40 +109,31 @@ int stream_last_parts() { return g_last_parts; }
 // status header of the caller's workspace).
 size_t stream_split_bytes() { return kSplitCntBytes + (kSplitSxFloats + kSplitPpFloats) * sizeof(float); }
 
-// Column parts per block of the partial last round (1: no split).  A block
-// takes about G chunk steps per CTA (G column groups); cut into k parts, the
-// partial round takes ceil(k R / ncl) units of ceil(G / k) chunks on its
-// busiest cluster, plus the fixed cost of a part (an extra normalise-only
-// pass, the global exchange and its wait), counted as kSplitCostChunks chunk
-// steps.  At most two units per cluster (the two-deep exchange buffers), all
-// units' x in tensor memory at once, whole column groups only.  `force`: 0 the
-// estimate decides, 1 never split, k >= 2 that many parts where it fits.
-constexpr int kSplitCostChunks = 3;
+// Column parts per block of the last R = n_blocks mod ncl blocks (1: no
+// split).  Cut into k parts, those blocks take about ceil(k R / ncl) units of
+// ceil(G / k) chunk steps on the busiest cluster (G column groups per CTA)
+// instead of G, but each part carries a fixed cost: the normalise-only pass of
+// the cluster's last whole block, the global exchange of s_x and of the
+// projections, the wait for the other parts and the owner's gate finish.
+// Measured on GB300 at H = 5120 that cost is about 24 chunk steps, more than a
+// whole block's 20, so the policy (`force` 0) does not split; k >= 2 asks for
+// at most k parts where they fit, 1 never splits.  The clusters together must
+// hold every unit: each holds at most kMaxUnitsCl of them and at most cap
+// tensor-memory chunks of them (their x stays there until the cluster's last
+// item); whole column groups only.
 static int wave_parts(int n_blocks, int ncl, int n64, int kcl, bool tc_proj, int force) {
-  if (force == 1 || n64 % kcl != 0 || ncl <= 0) return 1;
+  if (force <= 1 || n64 % kcl != 0 || ncl <= 0) return 1;
   const int G = n64 / kcl, R = n_blocks % ncl;
   if (R == 0 || G < 2 || R > kMaxSplitBlocks) return 1;
   const int cap = tc_proj ? kMaxChunksTC : kMaxChunks;
   auto fits = [&](int k) {
-    const int per = (k * R + ncl - 1) / ncl;
-    return k * R <= 2 * ncl && k * R <= kMaxUnits && per * ((G + k - 1) / k) <= cap;
+    const int maxng = (G + k - 1) / k;
+    const int per_cl = cap / maxng < kMaxUnitsCl ? cap / maxng : kMaxUnitsCl;
+    return k * R <= kMaxUnits && (long long)per_cl * ncl >= (long long)k * R;
   };
-  if (force >= 2) {
-    for (int k = force < G ? force : G; k >= 2; --k)
-      if (fits(k)) return k;
-    return 1;
-  }
-  int best_k = 1, best = G;
-  for (int k = 2; k <= G; ++k) {
-    if (!fits(k)) continue;
-    const int per = (k * R + ncl - 1) / ncl;
-    const int est = per * ((G + k - 1) / k) + kSplitCostChunks;
-    if (est < best) {
-      best = est;
-      best_k = k;
-    }
-  }
-  return best_k;
+  for (int k = force < G ? force : G; k >= 2; --k)
+    if (fits(k)) return k;
+  return 1;
 }
 
 static cudaError_t launch_with_maps(const SeamArgs& a, const CUtensorMap* m, bool tcgen05_proj, int kcl,
@@ -1420,11 +244,13 @@ static cudaError_t launch_range(const SeamArgs& a, const CUtensorMap* m, bool tc
   unsigned long long abort_ns = report_ns + 1000000000ull;
   const int form = a.comb_prev == nullptr ? 2 : a.Y != nullptr ? 1 : 0;
   const int mx = a.grid ? 2 : a.codes ? 1 : 0;
-  void* k = stream_kernel_ptr(form, mx, ms, kcl);
-  const int fit = max_clusters(form, mx, ms, kcl);
+  const int fit = max_clusters(form, mx, ms, kcl, false);
   if (fit <= 0) return cudaErrorInvalidValue;
   const int ncl = n_blocks < fit ? n_blocks : fit;
   int parts = wsx ? wave_parts(n_blocks, ncl, a.H / kChunk, kcl, tcgen05_proj, wave_split) : 1;
+  // the split variant's clusters must all be resident at once (cooperative launch)
+  if (parts > 1 && max_clusters(form, mx, ms, kcl, true) < ncl) parts = 1;
+  void* k = stream_kernel_ptr(form, mx, ms, kcl, parts > 1);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[3];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1437,7 +263,8 @@ static cudaError_t launch_range(const SeamArgs& a, const CUtensorMap* m, bool tc
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   // The parts of a split block wait for each other's partial sums: every
   // cluster of the grid must be resident at once, which a cooperative launch
-  // guarantees (the grid is at most the clusters that fit).
+  // guarantees (the grid is at most the clusters that fit).  Taking tickets
+  // needs no co-residency: a cluster that starts late takes what is left.
   attr[2].id = cudaLaunchAttributeCooperative;
   attr[2].val.cooperative = 1;
   cfg.gridDim = dim3((unsigned)(ncl * kcl), 1, 1);
@@ -1446,13 +273,14 @@ static cudaError_t launch_range(const SeamArgs& a, const CUtensorMap* m, bool tc
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = parts > 1 ? 3 : 2;
-  int b0 = block0, nfull = n_blocks / ncl, rem = n_blocks - (n_blocks / ncl) * ncl;
-  int kpart = rem > 0 ? parts : 1, groups = (a.H / kChunk + kcl - 1) / kcl;
+  // tickets: NB whole blocks, then the last R blocks in `parts` column parts
+  int b0 = block0, rsplit = parts > 1 ? n_blocks % ncl : 0, nb_whole = n_blocks - rsplit;
+  int kpart = rsplit > 0 ? parts : 1, groups = (a.H / kChunk + kcl - 1) / kcl;
   char* w = static_cast<char*>(wsx);
   void* args[] = {const_cast<SeamArgs*>(&a),    const_cast<CUtensorMap*>(m),     const_cast<CUtensorMap*>(m + 1),
                   const_cast<CUtensorMap*>(m + 2), const_cast<CUtensorMap*>(m + 3), const_cast<CUtensorMap*>(m + 4),
                   const_cast<CUtensorMap*>(m + 5), const_cast<CUtensorMap*>(m + 6), const_cast<CUtensorMap*>(m + 7),
-                  const_cast<CUtensorMap*>(m + 8), &b0, &nfull, &rem, &kpart, &groups, &w, &report_ns, &abort_ns};
+                  const_cast<CUtensorMap*>(m + 8), &b0, &nb_whole, &rsplit, &kpart, &groups, &w, &report_ns, &abort_ns};
   cudaError_t e = cudaLaunchKernelExC(&cfg, k, args);
   if (e == cudaSuccess) {
     ++*launches;

@@ -104,8 +104,9 @@ def test_unshifted_argument_rules(L):
     big = B.MhcConfig(block_m=32, cols_per_cta=640)
     assert _unsh(L, H=5120, cfg=C.byref(big)) == -10
     assert _seam(L, H=5120, cfg=C.byref(big), ws_bytes=1) == -5
-    # the streaming path's workspace: the status header and the split last round's 776 KiB
-    assert L.mhc_workspace_bytes_unshifted(4096, 5120, None) == L.mhc_workspace_bytes(4096, 5120, None) == 256 + 776 * 1024
+    # the streaming path's workspace: the status header, the split last round's 776 KiB and
+    # the item scheduler's 128-byte counter row
+    assert L.mhc_workspace_bytes_unshifted(4096, 5120, None) == L.mhc_workspace_bytes(4096, 5120, None) == 256 + 776 * 1024 + 128
     p1 = B.MhcConfig(path=1)
     need = L.mhc_workspace_bytes_unshifted(4096, 5120, C.byref(p1))
     assert need > 256 and _unsh(L, T=4096, H=5120, cfg=C.byref(p1), ws_bytes=need - 1) == -5
@@ -150,7 +151,7 @@ def test_workspace_grows_with_tokens_and_columns(L):
     b = L.mhc_workspace_bytes(64, 5120, C.byref(p1))
     c = L.mhc_workspace_bytes(1024, 5120, None)          # streaming path: status word + split last round
     d = L.mhc_workspace_bytes(1024, 5120, C.byref(p1))
-    stream = 256 + 776 * 1024
+    stream = 256 + 776 * 1024 + 128
     assert 256 < a < b < d and c == stream
     # small T: the automatic policy's workspace covers both paths it may take
     # (the split path without fn_packed, clusters of 16 with it)
