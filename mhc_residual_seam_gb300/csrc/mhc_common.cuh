@@ -160,18 +160,20 @@ __device__ __forceinline__ float rcp_approx(float x) {
 // 24 projections d[k]).  Logit order [pre 0..3 | post 4..7 | comb 8..23
 // row-major], alpha[0] pre, alpha[1] post, alpha[2] comb.  The Sinkhorn runs
 // on exp(l - rowmax): the row scale cancels in the first row normalisation.
-// Reciprocals use the hardware approximation (about 1 ulp): the 160
-// normalisations of the Sinkhorn are a serial chain per token, and the gates
-// are checked to 1e-3.
+// Reciprocals, the exponentials and the reciprocal square root use the fast
+// hardware forms (__expf, rsqrtf: a few ulp): the 160 normalisations of the
+// Sinkhorn are a serial chain per token on the launch's latency path, the
+// accurate forms cost several times the instructions (the finish is inlined
+// in every streaming kernel variant), and the gates are checked to 1e-3.
 __device__ __forceinline__ void finish_gates(float sR, const float* d, const float* alpha,
                                              const float* bias, int K, float eps, int iters,
                                              float* pre, float* post, float* comb) {
-  float rstdR = 1.0f / sqrtf(sR / (float)K + eps);
+  float rstdR = rsqrtf(sR / (float)K + eps);
   float a0 = alpha[0] * rstdR, a1 = alpha[1] * rstdR, a2 = alpha[2] * rstdR;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    pre[i] = rcp_approx(1.0f + expf(-(a0 * d[i] + bias[i])));
-    post[i] = 2.0f * rcp_approx(1.0f + expf(-(a1 * d[4 + i] + bias[4 + i])));
+    pre[i] = rcp_approx(1.0f + __expf(-(a0 * d[i] + bias[i])));
+    post[i] = 2.0f * rcp_approx(1.0f + __expf(-(a1 * d[4 + i] + bias[4 + i])));
   }
   float M[16];
 #pragma unroll
@@ -183,8 +185,11 @@ __device__ __forceinline__ void finish_gates(float sR, const float* d, const flo
       mx = fmaxf(mx, l[j]);
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) M[4 * i + j] = expf(l[j] - mx);
+    for (int j = 0; j < 4; ++j) M[4 * i + j] = __expf(l[j] - mx);
   }
+  // (kept rolled: each iteration depends on the last, so unrolling buys no
+  // overlap, only instruction footprint)
+#pragma unroll 1
   for (int it = 0; it < iters; ++it) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {

@@ -12,9 +12,17 @@ void* stream_kernel_ptr_split(int form, int out, bool ms, int kcl);
 
 // ------------------------------------------------------------- host side --
 // form: 0 no_post, 1 post, 2 identity.  Clusters of 16 run only the tcgen05
-// projection (at most 8 chunks per CTA).
-static void* stream_kernel_ptr(int form, int out, bool ms, int kcl, bool split) {
-  return split ? stream_kernel_ptr_split(form, out, ms, kcl) : stream_kernel_ptr_t<false>(form, out, ms, kcl);
+// projection (at most 8 chunks per CTA).  sched: 0 static, 1 tickets (only
+// the bf16 post and no_post forms on clusters of 4 with the tcgen05
+// projection: there a cluster's drift costs more than the larger code;
+// nullptr elsewhere), 2 tickets and the split.
+static void* stream_kernel_ptr(int form, int out, bool ms, int kcl, int sched) {
+  if (sched == 2) return stream_kernel_ptr_split(form, out, ms, kcl);
+  if (sched == 1) {
+    if (out != 0 || ms || kcl != 4 || form == 2) return nullptr;
+    return form == 1 ? (void*)stream_seam_kernel<1, 0, false, 4, 1> : (void*)stream_seam_kernel<0, 0, false, 4, 1>;
+  }
+  return stream_kernel_ptr_t<0>(form, out, ms, kcl);
 }
 static size_t smem_bytes(int kcl, int out) {
   if (kcl == 16)
@@ -25,9 +33,10 @@ static size_t smem_bytes(int kcl, int out) {
 cudaError_t stream_init() {
   for (int p = 0; p < 3; ++p)          // form
     for (int m = 0; m < 3; ++m)        // out mode
-      for (int v = 0; v < 6; ++v) {    // v % 3: 0 tcgen05 / 4, 1 warp MMA / 4, 2 tcgen05 / 16; v / 3: split
+      for (int v = 0; v < 9; ++v) {    // v % 3: 0 tcgen05 / 4, 1 warp MMA / 4, 2 tcgen05 / 16; v / 3: sched
         const int kcl = v % 3 == 2 ? 16 : 4;
-        void* k = stream_kernel_ptr(p, m, v % 3 == 1, kcl, v >= 3);
+        void* k = stream_kernel_ptr(p, m, v % 3 == 1, kcl, v / 3);
+        if (k == nullptr) continue;
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes(kcl, m));
         if (e == cudaSuccess && kcl == 16) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
@@ -77,11 +86,11 @@ static bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void*
 }
 
 // Clusters that fit at once, per device and kernel variant (queried once).
-static int max_clusters(int form, int out, bool ms, int kcl, bool split) {
-  static int cache[54][64] = {};
+static int max_clusters(int form, int out, bool ms, int kcl, int sched) {
+  static int cache[81][64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  const int v = form + 3 * out + 9 * (kcl == 16 ? 2 : (ms ? 1 : 0)) + (split ? 27 : 0);
+  const int v = form + 3 * out + 9 * (kcl == 16 ? 2 : (ms ? 1 : 0)) + 27 * sched;
   if (cache[v][dev] > 0) return cache[v][dev];
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -95,7 +104,8 @@ static int max_clusters(int form, int out, bool ms, int kcl, bool split) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, stream_kernel_ptr(form, out, ms, kcl, split), &cfg) != cudaSuccess) return 0;
+  void* kp = stream_kernel_ptr(form, out, ms, kcl, sched);
+  if (kp == nullptr || cudaOccupancyMaxActiveClusters(&n, kp, &cfg) != cudaSuccess) return 0;
   cache[v][dev] = n;
   return n;
 }
@@ -244,13 +254,15 @@ static cudaError_t launch_range(const SeamArgs& a, const CUtensorMap* m, bool tc
   unsigned long long abort_ns = report_ns + 1000000000ull;
   const int form = a.comb_prev == nullptr ? 2 : a.Y != nullptr ? 1 : 0;
   const int mx = a.grid ? 2 : a.codes ? 1 : 0;
-  const int fit = max_clusters(form, mx, ms, kcl, false);
+  const int fit = max_clusters(form, mx, ms, kcl, 0);
   if (fit <= 0) return cudaErrorInvalidValue;
   const int ncl = n_blocks < fit ? n_blocks : fit;
   int parts = wsx ? wave_parts(n_blocks, ncl, a.H / kChunk, kcl, tcgen05_proj, wave_split) : 1;
   // the split variant's clusters must all be resident at once (cooperative launch)
-  if (parts > 1 && max_clusters(form, mx, ms, kcl, true) < ncl) parts = 1;
-  void* k = stream_kernel_ptr(form, mx, ms, kcl, parts > 1);
+  if (parts > 1 && max_clusters(form, mx, ms, kcl, 2) < ncl) parts = 1;
+  // tickets where the variant exists and there is more than one round
+  const int sched = parts > 1 ? 2 : (wsx && n_blocks > ncl && stream_kernel_ptr(form, mx, ms, kcl, 1) != nullptr ? 1 : 0);
+  void* k = stream_kernel_ptr(form, mx, ms, kcl, sched);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[3];
   attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -238,6 +238,24 @@ __device__ __forceinline__ void drain(const Ctx& x, uint64_t* bar, uint32_t pari
 
 }  // namespace
 
+// The fp8_grid row of one token and 64 columns: the bf16 of the dequantised
+// e4m3 codes of each 32-group, from the norm values nb (64 bf16 in 32 words),
+// to dst (nullptr: a token past T), 128 contiguous bytes written by this
+// thread.  Out of line: the grid warps hold few live values, and one copy
+// keeps the kernel's instruction footprint small.
+static __device__ __noinline__ void grid_row_store(const uint32_t* nb, __nv_bfloat16* dst, float amax_floor) {
+#pragma unroll 1
+  for (int half = 0; half < 2; ++half) {
+    uint32_t gw[16];
+    grid_group32(nb + 16 * half, gw, amax_floor);
+    if (dst != nullptr) {
+      uint4* d = reinterpret_cast<uint4*>(dst + 32 * half);
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) st_stream(d + ch, make_uint4(gw[4 * ch], gw[4 * ch + 1], gw[4 * ch + 2], gw[4 * ch + 3]));
+    }
+  }
+}
+
 // Gate finish of one token on its owner CTA, kept out of line so its arrays
 // do not raise the register pressure of the kernel.
 static __device__ __noinline__ void finish_store_gates(const SeamArgs& a, int64_t t, const float* p, const float* ab, int H) {
@@ -378,11 +396,14 @@ static __device__ __noinline__ void unit_owner_finish(const SeamArgs& a, unsigne
 // first block's form, R' = R, no residual write.
 // OUT: 0 bf16 norm, 1 mxfp8 (+ e4m3 codes, e8m0 scales), 2 fp8_grid (+ the
 // quantisation dequantised to bf16)
-// SPLIT: the launch cuts the blocks of its partial last round into column
-// parts (units).  Without it every unit path is compiled out: the kernel's
-// instruction footprint sets how well its hot loops stay in the
-// instruction cache, measured at 2 to 5 % of the streaming time.
-template <int FORM, int OUT, bool MS, int KCL, bool SPLIT>
+// SCHED: how the clusters get their items.  0: blocks cid, cid + ncl, ...
+// (static); 1: tickets from a global counter (a cluster that runs slower
+// takes fewer blocks); 2: tickets, and the blocks of the partial last round
+// cut into column parts (units).  The ticket ring and the unit paths are
+// compiled only where used: the kernel's instruction footprint sets how well
+// its hot loops stay in the instruction cache (measured: 2 to 25 % of the
+// streaming time, by form).
+template <int FORM, int OUT, bool MS, int KCL, int SCHED>
 __global__ void __launch_bounds__(threads_of<OUT>(), 1)
     stream_seam_kernel(const __grid_constant__ SeamArgs a, const __grid_constant__ CUtensorMap tmR,
                        const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmRo,
@@ -391,6 +412,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
                        const __grid_constant__ CUtensorMap tmGp, const __grid_constant__ CUtensorMap tmGq,
                        int block0, int NB, int R, int k_parts, int G_groups, char* wsx,
                        unsigned long long report_ns, unsigned long long abort_ns) {
+  constexpr bool DYN = SCHED >= 1, SPLIT = SCHED == 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   using G = Geo<KCL, OUT>;
@@ -422,23 +444,36 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
   // chunks of this CTA in an item (a unit covers whole groups only)
   auto nchi = [&](const Item& it) { return SPLIT && it.unit >= 0 ? it.ng : nch; };
 
-  // ---- the item list.  Item i sits in slot i % kSchedD of this CTA's ring
-  // from its arrival until every reader released it (at the end of its work
-  // on the item); its fields are read from there where they are used, so no
-  // register holds them across the chunk loops.
+  // ---- the item list.  Static (SCHED 0): the cluster takes blocks cid,
+  // cid + ncl, cid + 2 ncl, ... (every item a whole block, known to every
+  // role without any exchange).  With tickets, rank 0 takes them from a
+  // global counter and publishes each item to its cluster: item i sits in
+  // slot i % kSchedD of each CTA's ring from its arrival until every reader
+  // released it (at the end of its work on the item); its fields are read
+  // from there where they are used, so no register holds them across the
+  // chunk loops.
   volatile Item* const ring = tl->sched;
-  auto iblock = [&](int i) -> int { return ring[i % kSchedD].block; };
-  auto ig0 = [&](int i) -> int { return ring[i % kSchedD].g0; };
+  auto iblock = [&](int i) -> int {
+    return DYN ? ring[i % kSchedD].block : cid + i * ncl < NB ? block0 + cid + i * ncl : -1;
+  };
+  auto ig0 = [&](int i) -> int { return SPLIT ? ring[i % kSchedD].g0 : 0; };
   auto iunit = [&](int i) -> int { return SPLIT ? ring[i % kSchedD].unit : -1; };
   auto inch = [&](int i) -> int { return SPLIT && ring[i % kSchedD].unit >= 0 ? ring[i % kSchedD].ng : nch; };
-  auto arrived = [&](int i) -> bool { return wait_local(X, &tl->sched_full[i % kSchedD], (i / kSchedD) & 1); };
-  auto arrived_warp = [&](int i) -> bool { return wait_warp(X, &tl->sched_full[i % kSchedD], (i / kSchedD) & 1); };
+  auto item = [&](int i) -> Item {
+    return DYN ? const_cast<const Item&>(ring[i % kSchedD]) : Item{iblock(i), 0, G_groups, -1};
+  };
+  auto arrived = [&](int i) -> bool { return !DYN || wait_local(X, &tl->sched_full[i % kSchedD], (i / kSchedD) & 1); };
+  auto arrived_warp = [&](int i) -> bool {
+    return !DYN || wait_warp(X, &tl->sched_full[i % kSchedD], (i / kSchedD) & 1);
+  };
   // one thread per reader role: the slot may be reused once every reader of
   // the cluster released it (a remote arrive on rank 0's sched_free).  The
   // arrive is relaxed: every read of the slot has returned before it (the
   // values decided the branches that lead here), and a release at cluster
   // scope was measured to stall the compute warps 2.5 us per item.
-  auto release = [&](int i) { mbar_arrive_remote_relaxed(mapa_shared(smem_u32(&tl->sched_free[i % kSchedD]), 0)); };
+  auto release = [&](int i) {
+    if (DYN) mbar_arrive_remote_relaxed(mapa_shared(smem_u32(&tl->sched_free[i % kSchedD]), 0));
+  };
 
   if (tid == 0) {
     for (int s = 0; s < kNI; ++s) {
@@ -569,7 +604,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
       // fetched an item ahead (during item n - 1, once its compute has begun),
       // so their load latency never stalls the compute warps between items.
       auto next_item = [&](int n) -> bool {
-        mbar_arrive_expect_tx(&tl->sched_full[n % kSchedD], (uint32_t)sizeof(Item));
+        if (DYN) mbar_arrive_expect_tx(&tl->sched_full[n % kSchedD], (uint32_t)sizeof(Item));
         if (!arrived(n)) return false;
         const int b = iblock(n);
         if (b < 0) return true;
@@ -582,43 +617,45 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
         ++ng;
         return true;
       };
-      bool ok = rank != 0 || publish();
-      ok = ok && next_item(0);
-      for (int i = 0; ok; ++i) {
-        const Item it = const_cast<const Item&>(ring[i % kSchedD]);
-        if (it.block < 0) {
-          release(i);
-          break;
-        }
-        if (SPLIT && it.unit >= 0) {  // the cluster's units, for the normalise-only passes after its last item
-          tl->ulist[tl->nunits] = it;
-          ++tl->nunits;
-        }
-        const int t0 = it.block * kBM, gb = it.g0, ni = nchi(it);
-        // item i + 1: published by rank 0 after this item's first load, its
-        // gates fetched once this item's compute has begun (its load for chunk
-        // kNI waited for chunk 0 to be consumed) or after the last load
-        const int cg = ni - 1 < kNI ? ni - 1 : kNI;
-        bool ahead = false;
-        for (int c = 0; c < ni; ++c, ++j) {
-          const int s = j % kNI;
-          if (!(ok = wait_local(X, &tl->in_empty[s], ((j / kNI) & 1) ^ 1))) break;
-          uint8_t* st = sm + kOffIn + s * kInStageF;
-          const int h = ((gb + c) * kCl + (int)rank) * kChunk;
-          mbar_arrive_expect_tx(&tl->in_full[s], bytes);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) tma_load_3d(st + q * kRTile, &tmR, &tl->in_full[s], h, q, t0, pol);
-          if (POST) tma_load_2d(st + 4 * kRTile, &tmY, &tl->in_full[s], h, t0, pol);
-          if (c == 0 && rank == 0 && pub == i + 1 && !(ok = publish())) break;
-          if (c == cg) {
-            ahead = true;
-            if (!(ok = next_item(i + 1))) break;
+      // Item i's loads; at its first step rank 0 publishes item i + 1, and
+      // once this item's compute has begun (its load for chunk kNI waited for
+      // chunk 0 to be consumed), or at its last step, item i + 1's gates are
+      // fetched.  Item -1 has no chunks: it publishes and fetches item 0.
+      // (One call site each keeps the producer's code small.)
+      bool ok = true;
+      for (int i = -1; ok; ++i) {
+        int t0 = 0, gb = 0, ni = 0;
+        if (i >= 0) {
+          const Item it = item(i);
+          if (it.block < 0) {
+            release(i);
+            break;
           }
+          if (SPLIT && it.unit >= 0) {  // the cluster's units, for the normalise-only passes after its last item
+            tl->ulist[tl->nunits] = it;
+            ++tl->nunits;
+          }
+          t0 = it.block * kBM;
+          gb = it.g0;
+          ni = nchi(it);
         }
-        if (!ok) break;
-        if (rank == 0 && pub == i + 1 && !(ok = publish())) break;
-        if (!ahead && !(ok = next_item(i + 1))) break;
-        release(i);
+        const int steps = ni > 0 ? ni : 1, cg = ni - 1 < kNI ? steps - 1 : kNI;
+        for (int c = 0; c < steps; ++c) {
+          if (c < ni) {
+            const int s = j % kNI;
+            if (!(ok = wait_local(X, &tl->in_empty[s], ((j / kNI) & 1) ^ 1))) break;
+            uint8_t* st = sm + kOffIn + s * kInStageF;
+            const int h = ((gb + c) * kCl + (int)rank) * kChunk;
+            mbar_arrive_expect_tx(&tl->in_full[s], bytes);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tma_load_3d(st + q * kRTile, &tmR, &tl->in_full[s], h, q, t0, pol);
+            if (POST) tma_load_2d(st + 4 * kRTile, &tmY, &tl->in_full[s], h, t0, pol);
+            ++j;
+          }
+          if (DYN && c == 0 && rank == 0 && !(ok = publish())) break;
+          if (c == cg && !(ok = next_item(i + 1))) break;
+        }
+        if (ok && i >= 0) release(i);
       }
       // Every load issued lands before the CTA exits.  A stage is refilled
       // only after all eight compute warps released it, and they release it
@@ -768,7 +805,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
       const int qa = full ? -1 : 0, qb = full ? (nblk < 0 || iunit(i + 1) >= 0 ? 0 : -1) : (nblk < 0 ? nu : 0);
       constexpr int NG = norm_group<OUT>();
       for (int q = qa; q < qb && ok; ++q) {
-        const Item u = !SPLIT || q < 0 ? const_cast<const Item&>(ring[i % kSchedD]) : const_cast<const Item&>(tl->ulist[q]);
+        const Item u = !SPLIT || q < 0 ? item(i) : const_cast<const Item&>(tl->ulist[q]);
         const int tq = u.block * kBM, gq = u.g0, nq = nchi(u);
         for (int c0 = 0; c0 < nq; c0 += NG, ++j) {
           const int o = j % kNO;
@@ -820,20 +857,10 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
       }
     };
     // the grid row of token tp + lane, columns h .. h + 63, straight from
-    // registers, one 32-group at a time: each lane writes its own 128
-    // contiguous bytes
+    // registers (one out-of-line copy for both call sites)
     auto grid_row = [&](int64_t tp, int h, const uint32_t* nb) {
       const int64_t tt = tp + lane;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t gw[16];
-        grid_group32(nb + 16 * half, gw, a.amax_floor);
-        if (tt < T) {
-          uint4* dst = reinterpret_cast<uint4*>(a.grid + tt * H + h + 32 * half);
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch) st_stream(dst + ch, make_uint4(gw[4 * ch], gw[4 * ch + 1], gw[4 * ch + 2], gw[4 * ch + 3]));
-        }
-      }
+      grid_row_store(nb, tt < T ? a.grid + tt * H + h : nullptr, a.amax_floor);
     };
     int j = 0, nu = 0, prevblk = -1;
     bool ok = arrived_warp(0);
@@ -860,7 +887,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
       const int qa = full ? -1 : 0, qb = full ? (nblk < 0 || iunit(i + 1) >= 0 ? 0 : -1) : (nblk < 0 ? nu : 0);
       constexpr int NG = norm_group<OUT>();
       for (int q = qa; q < qb && ok; ++q) {
-        const Item u = !SPLIT || q < 0 ? const_cast<const Item&>(ring[i % kSchedD]) : const_cast<const Item&>(tl->ulist[q]);
+        const Item u = !SPLIT || q < 0 ? item(i) : const_cast<const Item&>(tl->ulist[q]);
         const int64_t tq = (int64_t)u.block * kBM;
         const int gq = u.g0, nq = nchi(u);
         for (int c0 = 0; c0 < nq; c0 += NG, ++j) {
@@ -930,7 +957,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
         const uint32_t dst = (uint32_t)(lane % kCl);
         const uint32_t ra = mapa_shared(smem_u32(&tl->recv[par][rank][lane / kCl][0]), dst);
         const uint32_t rb = mapa_shared(smem_u32(&tl->recv_full[par]), dst);
-#pragma unroll
+#pragma unroll 1
         for (int k = 0; k < 24; k += 2) {
           float s0 = tl->dbuf[0][lane][k], s1 = tl->dbuf[0][lane][k + 1];
 #pragma unroll
@@ -1258,7 +1285,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
       constexpr int NG = norm_group<OUT>();
       int sq = 0;  // first tensor-memory slot of the pass's x
       for (int q = qa; q < qb && ok; ++q) {
-        const Item u = !SPLIT || q < 0 ? const_cast<const Item&>(ring[i % kSchedD]) : const_cast<const Item&>(tl->ulist[q]);
+        const Item u = !SPLIT || q < 0 ? item(i) : const_cast<const Item&>(tl->ulist[q]);
         if (!SPLIT || q < 0) {
           if (!(ok = take_rstd(i, u.block))) break;
         } else {
@@ -1335,24 +1362,24 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
   }
 }
 
-// Kernel pointers of one SPLIT setting (form: 0 no_post, 1 post, 2 identity;
+// Kernel pointers of one SCHED setting (form: 0 no_post, 1 post, 2 identity;
 // out: 0 bf16, 1 mxfp8, 2 fp8_grid; clusters of 16 run only the tcgen05
 // projection).
-template <int FORM, bool MS, int KCL, bool SPLIT>
+template <int FORM, bool MS, int KCL, int SCHED>
 inline void* stream_kptr_f(int out) {
-  return out == 2 ? (void*)stream_seam_kernel<FORM, 2, MS, KCL, SPLIT>
-         : out == 1 ? (void*)stream_seam_kernel<FORM, 1, MS, KCL, SPLIT>
-                    : (void*)stream_seam_kernel<FORM, 0, MS, KCL, SPLIT>;
+  return out == 2 ? (void*)stream_seam_kernel<FORM, 2, MS, KCL, SCHED>
+         : out == 1 ? (void*)stream_seam_kernel<FORM, 1, MS, KCL, SCHED>
+                    : (void*)stream_seam_kernel<FORM, 0, MS, KCL, SCHED>;
 }
-template <bool MS, int KCL, bool SPLIT>
+template <bool MS, int KCL, int SCHED>
 inline void* stream_kptr_(int form, int out) {
-  return form == 2 ? stream_kptr_f<2, MS, KCL, SPLIT>(out)
-         : form == 1 ? stream_kptr_f<1, MS, KCL, SPLIT>(out) : stream_kptr_f<0, MS, KCL, SPLIT>(out);
+  return form == 2 ? stream_kptr_f<2, MS, KCL, SCHED>(out)
+         : form == 1 ? stream_kptr_f<1, MS, KCL, SCHED>(out) : stream_kptr_f<0, MS, KCL, SCHED>(out);
 }
-template <bool SPLIT>
+template <int SCHED>
 inline void* stream_kernel_ptr_t(int form, int out, bool ms, int kcl) {
-  if (kcl == 16) return stream_kptr_<false, 16, SPLIT>(form, out);
-  return ms ? stream_kptr_<true, 4, SPLIT>(form, out) : stream_kptr_<false, 4, SPLIT>(form, out);
+  if (kcl == 16) return stream_kptr_<false, 16, SCHED>(form, out);
+  return ms ? stream_kptr_<true, 4, SCHED>(form, out) : stream_kptr_<false, 4, SCHED>(form, out);
 }
 
 }  // namespace mhc

@@ -6,6 +6,6 @@
 
 namespace mhc {
 
-void* stream_kernel_ptr_split(int form, int out, bool ms, int kcl) { return stream_kernel_ptr_t<true>(form, out, ms, kcl); }
+void* stream_kernel_ptr_split(int form, int out, bool ms, int kcl) { return stream_kernel_ptr_t<2>(form, out, ms, kcl); }
 
 }  // namespace mhc
