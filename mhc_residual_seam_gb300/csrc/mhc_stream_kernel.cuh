@@ -238,13 +238,24 @@ __device__ __forceinline__ void drain(const Ctx& x, uint64_t* bar, uint32_t pari
 
 }  // namespace
 
-// The fp8_grid row of one token and 64 columns: the bf16 of the dequantised
-// e4m3 codes of each 32-group, from the norm values nb (64 bf16 in 32 words),
-// to dst (nullptr: a token past T), 128 contiguous bytes written by this
-// thread.  Out of line: the grid warps hold few live values, and one copy
-// keeps the kernel's instruction footprint small.
-static __device__ __noinline__ void grid_row_store(const uint32_t* nb, __nv_bfloat16* dst, float amax_floor) {
-#pragma unroll 1
+// The fp8_grid row of one token (lane = token) and 64 columns: the row of
+// the 128-byte-swizzled norm tile nt (64 bf16) into registers, then `rel`
+// (if given) is arrived on by lane 0 once the warp has read the tile, then
+// the bf16 of the dequantised e4m3 codes of each 32-group to dst (nullptr: a
+// token past T), 128 contiguous bytes written by this thread.  Out of line
+// (one copy for both call sites, the grid warps hold few live values); the
+// row stays in registers (constant indices only).
+static __device__ __noinline__ void grid_tile_row(const uint8_t* nt, uint64_t* rel, __nv_bfloat16* dst,
+                                                  float amax_floor, int lane) {
+  uint32_t nb[32];
+#pragma unroll
+  for (int ch = 0; ch < 8; ++ch) {
+    const uint4 v = *reinterpret_cast<const uint4*>(nt + lane * 128 + ((ch ^ (lane & 7)) << 4));
+    nb[4 * ch] = v.x; nb[4 * ch + 1] = v.y; nb[4 * ch + 2] = v.z; nb[4 * ch + 3] = v.w;
+  }
+  __syncwarp();
+  if (rel != nullptr && lane == 0) mbar_arrive(rel);
+#pragma unroll
   for (int half = 0; half < 2; ++half) {
     uint32_t gw[16];
     grid_group32(nb + 16 * half, gw, amax_floor);
@@ -847,20 +858,11 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
     // their grid (bf16 of the dequantised e4m3 codes) straight to global
     // memory; the stage is free again once it has read them.
     const int me = warp - 13;
-    // lane = token: one norm tile row (64 bf16) into registers, so the stage
-    // can be released before the grid is computed from them
-    auto load_row = [&](const uint8_t* nt, uint32_t* nb) {
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        const uint4 v = *reinterpret_cast<const uint4*>(nt + lane * 128 + ((ch ^ (lane & 7)) << 4));
-        nb[4 * ch] = v.x; nb[4 * ch + 1] = v.y; nb[4 * ch + 2] = v.z; nb[4 * ch + 3] = v.w;
-      }
-    };
-    // the grid row of token tp + lane, columns h .. h + 63, straight from
-    // registers (one out-of-line copy for both call sites)
-    auto grid_row = [&](int64_t tp, int h, const uint32_t* nb) {
+    // the grid row of token tp + lane, columns h .. h + 63, from norm tile nt;
+    // `rel` is released once the tile is read (the row is then in registers)
+    auto grid_row = [&](const uint8_t* nt, uint64_t* rel, int64_t tp, int h) {
       const int64_t tt = tp + lane;
-      grid_row_store(nb, tt < T ? a.grid + tt * H + h : nullptr, a.amax_floor);
+      grid_tile_row(nt, rel, tt < T ? a.grid + tt * H + h : nullptr, a.amax_floor, lane);
     };
     int j = 0, nu = 0, prevblk = -1;
     bool ok = arrived_warp(0);
@@ -873,11 +875,11 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
         if (o != me) continue;
         const uint8_t* ost = sm + kOffOut + o * kOutStage;
         if (!(ok = wait_warp(X, &tl->out_full[o], (j / kNO) & 1))) break;
-        uint32_t nb[32];
-        if (fused) load_row(ost + kOffNormT, nb);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tl->out_empty[o]);
-        if (fused) grid_row(tp, ((gb + c) * kCl + (int)rank) * kChunk, nb);
+        if (fused) {
+          grid_row(ost + kOffNormT, &tl->out_empty[o], tp, ((gb + c) * kCl + (int)rank) * kChunk);
+        } else if (lane == 0) {
+          mbar_arrive(&tl->out_empty[o]);
+        }
       }
       if (!ok) break;
       if (!full) ++nu;
@@ -896,13 +898,8 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
           const uint8_t* ost = sm + kOffOut + o * kOutStage;
           if (!(ok = wait_warp(X, &tl->out_full[o], (j / kNO) & 1))) break;
           const int ng = min(NG, nq - c0);
-          for (int g = 0; g < ng; ++g) {
-            uint32_t nb[32];
-            load_row(ost + g * kRTile, nb);
-            __syncwarp();
-            if (g == ng - 1 && lane == 0) mbar_arrive(&tl->out_empty[o]);
-            grid_row(tq, ((gq + c0 + g) * kCl + (int)rank) * kChunk, nb);
-          }
+          for (int g = 0; g < ng; ++g)
+            grid_row(ost + g * kRTile, g == ng - 1 ? &tl->out_empty[o] : nullptr, tq, ((gq + c0 + g) * kCl + (int)rank) * kChunk);
         }
       }
       prevblk = full ? iblock(i) : -1;
