@@ -4,11 +4,12 @@
 // Persistent clusters of KCL CTAs (4, or 16 for small T; one CTA per SM).
 // CTA r of a cluster owns the 64-column chunks r, r + KCL, r + 2 KCL, ... of H
 // for all four streams (the cluster reads each row in long runs) and the
-// cluster walks blocks of 32 tokens.  Per 64-column chunk:
+// cluster walks blocks of 32 tokens (its items: blocks cid, cid + ncl, ...,
+// or blocks taken by ticket; see SCHED below).  Per 64-column chunk:
 //  - an input producer warp TMA-loads the four R tiles and the Y tile into a
-//    ring of 4 input stages (5 without Y; 128-byte swizzle), and each block's carried
-//    gates (comb, pre, post) into a buffer as it starts the block, so they
-//    wait in shared memory when compute gets there;
+//    ring of 4 input stages (5 without Y; 128-byte swizzle), and, during each
+//    item, the next item's carried gates (comb, pre, post) into one of two
+//    buffers, so they wait in shared memory when compute gets there;
 //  - an fn producer warp TMA-loads the four hi/lo-packed fn tiles [48 x 64]
 //    into a ring of 2 fn stages (L2 evict-last: every cluster reuses them);
 //  - eight compute warps (thread = token, warp = 8-column slice; the swizzle
@@ -38,6 +39,8 @@
 //    chunk;
 //  - the 24 projection sums and s_R of each token to the token's owner CTA
 //    (token % KCL), whose exchange warp then computes the gates.
+// With the split schedule the blocks of the partial last round are cut into
+// column parts whose partial sums meet in a global workspace instead.
 // ("[FlyDSL] Single-launch Mega-mHC on gfx950", Kernel Architecture: split-K
 // with a distributed finish; here the cluster launch makes every CTA of a
 // split co-resident.)
@@ -47,8 +50,9 @@
 // pass of the unshifted ordering, which needs only R' and the gates.
 //
 // Every wait is bounded, in two tiers.  A wait longer than the caller's limit
-// sets bit 1 of the status word and goes on waiting, so a short limit only
-// flags the call and the work completes as usual.  A wait one second longer
+// flags the CTA (the kernel's exit sets bit 1 of the status word) and goes on
+// waiting, so a short limit only flags the call and the work completes as
+// usual.  A wait one second longer
 // abandons the call: the CTA stops issuing copies, MMAs and stores, and before
 // it frees tensor memory and exits it waits (with a fixed cap) for the ones in
 // flight: the last TMA load of every input, fn and gate buffer (a buffer is
