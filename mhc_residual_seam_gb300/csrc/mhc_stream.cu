@@ -24,10 +24,15 @@ static void* stream_kernel_ptr(int form, int out, bool ms, int kcl, int sched) {
   }
   return stream_kernel_ptr_t<0>(form, out, ms, kcl);
 }
-static size_t smem_bytes(int kcl, int out) {
+// lean: the identity form with the tcgen05 projection (its own layout)
+template <bool L>
+static size_t smem_bytes_t(int kcl, int out) {
   if (kcl == 16)
-    return out == 2 ? Geo<16, 2>::kSmemBytes : out == 1 ? Geo<16, 1>::kSmemBytes : Geo<16, 0>::kSmemBytes;
-  return out == 2 ? Geo<4, 2>::kSmemBytes : out == 1 ? Geo<4, 1>::kSmemBytes : Geo<4, 0>::kSmemBytes;
+    return out == 2 ? Geo<16, 2, L>::kSmemBytes : out == 1 ? Geo<16, 1, L>::kSmemBytes : Geo<16, 0, L>::kSmemBytes;
+  return out == 2 ? Geo<4, 2, L>::kSmemBytes : out == 1 ? Geo<4, 1, L>::kSmemBytes : Geo<4, 0, L>::kSmemBytes;
+}
+static size_t smem_bytes(int kcl, int out, int form, bool ms) {
+  return form == 2 && !ms ? smem_bytes_t<true>(kcl, out) : smem_bytes_t<false>(kcl, out);
 }
 
 cudaError_t stream_init() {
@@ -37,7 +42,8 @@ cudaError_t stream_init() {
         const int kcl = v % 3 == 2 ? 16 : 4;
         void* k = stream_kernel_ptr(p, m, v % 3 == 1, kcl, v / 3);
         if (k == nullptr) continue;
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes(kcl, m));
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem_bytes(kcl, m, p, v % 3 == 1));
         if (e == cudaSuccess && kcl == 16) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
       }
@@ -100,7 +106,7 @@ static int max_clusters(int form, int out, bool ms, int kcl, int sched) {
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3((unsigned)kcl, 1, 1);
   cfg.blockDim = dim3(out == 2 ? threads_of<2>() : threads_of<0>(), 1, 1);
-  cfg.dynamicSmemBytes = smem_bytes(kcl, out);
+  cfg.dynamicSmemBytes = smem_bytes(kcl, out, form, ms);
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
@@ -281,7 +287,7 @@ static cudaError_t launch_range(const SeamArgs& a, const CUtensorMap* m, bool tc
   attr[2].val.cooperative = 1;
   cfg.gridDim = dim3((unsigned)(ncl * kcl), 1, 1);
   cfg.blockDim = dim3(mx == 2 ? threads_of<2>() : threads_of<0>(), 1, 1);
-  cfg.dynamicSmemBytes = smem_bytes(kcl, mx);
+  cfg.dynamicSmemBytes = smem_bytes(kcl, mx, form, ms);
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = parts > 1 ? 3 : 2;

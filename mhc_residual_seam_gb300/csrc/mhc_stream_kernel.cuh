@@ -85,7 +85,7 @@ constexpr uint32_t kInStage = 5 * kRTile;              // 20 KB: R tiles 0-3, Y 
 // The input ring of clusters of 4 holds 4 stages of R + Y, or, in the forms
 // without Y, 5 stages of R in the same bytes (more loads in flight per SM);
 // clusters of 16 (a CTA has at most 8 chunks per block) hold 3 stages.
-constexpr int kNIMax = 5;
+constexpr int kNIMax = 8;
 template <int FORM, int KCL>
 __host__ __device__ constexpr int in_stages() { return KCL == 16 ? 3 : FORM == 1 ? 4 : 5; }
 template <int FORM>
@@ -134,11 +134,25 @@ constexpr int kMaxUnitsCl = 16;    // units one cluster may hold
 // Geometry of a cluster of KCL CTAs: 4 for large T (bandwidth), 16 for small T
 // (each CTA takes a quarter of the columns it would take in a cluster of 4),
 // for output mode OUT (the mxfp8 output stages hold a codes tile more).
-template <int KCL, int OUT>
+// LEAN: the identity form with the tcgen05 projection, whose MMAs read
+// R' = R from the input stage: an output stage then holds only the norm tile
+// (and the codes tile), and the shared memory this frees goes to the input
+// ring (8 stages of R instead of 5 on clusters of 4: more loads in flight per
+// SM, which is what bounds that form).
+template <int KCL, int OUT, bool LEAN = false>
 struct Geo {
   static constexpr int kCl = KCL;
-  static constexpr uint32_t kInRing = (KCL == 16 ? 3 : 4) * kInStage;  // input ring: 80 KB (60 KB)
-  static constexpr uint32_t kOutStage = out_stage_bytes<OUT>();
+  static constexpr uint32_t kOutStage = LEAN ? (OUT == 1 ? kRTile + kBM * 64 : kRTile) : out_stage_bytes<OUT>();
+  static constexpr uint32_t kInRing = (KCL == 16 ? 3 : 4) * kInStage  // input ring: 80 KB (60 KB)
+                                      + (LEAN ? kNO * (out_stage_bytes<OUT>() - kOutStage) : 0);
+  // LEAN: input stages of R alone (16 KB) that fit the ring
+  static constexpr int kNILean = (int)(kInRing / (4 * kRTile)) < kNIMax ? (int)(kInRing / (4 * kRTile)) : kNIMax;
+  static constexpr uint32_t kOffNormT = LEAN ? 0 : 4 * kRTile;   // the norm tile in an output stage
+  static constexpr uint32_t kOffCodesT = LEAN ? kRTile : 5 * kRTile;  // (mxfp8) the codes tile [32 x 64] u8
+  // the normalise-only pass: norm tiles of kNormGroup chunks per stage (in
+  // the R' tile slots), the codes tiles from kPassCodes on
+  static constexpr int kNormGroup = LEAN ? 1 : norm_group<OUT>();
+  static constexpr uint32_t kPassCodes = LEAN ? kRTile : 4 * kRTile;
   static constexpr int kSlots = kBM / KCL;              // tokens owned per CTA and block
   // gamma of a CTA's first chunks, staged in shared memory (the mxfp8 form on
   // clusters of 4 has no room left: its chunks read gamma through L1/L2)
@@ -430,11 +444,13 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
   constexpr bool DYN = SCHED >= 1, SPLIT = SCHED == 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  using G = Geo<KCL, OUT>;
+  constexpr bool LEAN = FORM == 2 && !MS;  // the MMAs read R' = R from the input stage
+  using G = Geo<KCL, OUT, LEAN>;
   constexpr uint32_t kOutStage = G::kOutStage;
+  constexpr uint32_t kOffNormT = G::kOffNormT, kOffCodesT = G::kOffCodesT, kPassCodes = G::kPassCodes;
   constexpr int kThreads = threads_of<OUT>();
   constexpr bool POST = FORM == 1, IDENT = FORM == 2;
-  constexpr int kNI = in_stages<FORM, KCL>();
+  constexpr int kNI = LEAN ? G::kNILean : in_stages<FORM, KCL>();
   constexpr uint32_t kInStageF = in_stage_bytes<FORM>();
   static_assert(kNI <= kNIMax && kNI * kInStageF <= G::kInRing, "input ring");
   constexpr int kCl = G::kCl, kSlots = G::kSlots;
@@ -493,7 +509,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
   if (tid == 0) {
     for (int s = 0; s < kNI; ++s) {
       mbar_init(&tl->in_full[s], 1);
-      mbar_init(&tl->in_empty[s], 8);
+      mbar_init(&tl->in_empty[s], LEAN ? 9 : 8);  // (LEAN: and the MMAs that read the stage)
     }
     for (int s = 0; s < kNF; ++s) {
       mbar_init(&tl->fn_full[s], 1);
@@ -501,7 +517,9 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
     }
     for (int s = 0; s < kNO; ++s) {
       mbar_init(&tl->out_full[s], 8);
-      mbar_init(&tl->out_empty[s], (MS ? 9 : 2) + (OUT == 2 ? 1 : 0));
+      // released by the store warp, and the MMA commit (the warp-level MMA warps)
+      // unless the MMAs read the input stage, and the grid warp
+      mbar_init(&tl->out_empty[s], (MS ? 9 : LEAN ? 1 : 2) + (OUT == 2 ? 1 : 0));
     }
     mbar_init(&tl->d_full, 1);
     for (int p = 0; p < 2; ++p) {
@@ -718,19 +736,24 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
         const int ni = inch(i);
         for (int c = 0; c < ni; ++c, ++j) {
           const int o = j % kNO;
-          const int f = jr % kNF;
-          if (!(ok = wait_local(X, &tl->out_full[o], (j / kNO) & 1))) break;
+          const int f = jr % kNF, si = jr % kNI;  // (LEAN: chunk jr's input stage)
+          // the chunk's R': in the compute warps' output stage, or (LEAN) the
+          // input stage itself as soon as its load has landed
+          if (!(ok = LEAN ? wait_local(X, &tl->in_full[si], (jr / kNI) & 1)
+                          : wait_local(X, &tl->out_full[o], (j / kNO) & 1)))
+            break;
           // the first MMA of an item overwrites D: the previous item's D must have been read
           if (c == 0 && i > 0 && !(ok = wait_local(X, &tl->d_free, (i - 1) & 1))) break;
           if (!(ok = wait_local(X, &tl->fn_full[f], (jr / kNF) & 1))) break;
           tc_fence_after();
-          const uint32_t ra = smem_u32(sm + kOffOut + o * kOutStage);   // R' of the 4 streams [128 x 64]
-          const uint32_t fb = smem_u32(sm + kOffFn + f * kFnStage);     // fn of the 4 streams [192 x 64]
+          // R' of the 4 streams [128 x 64], fn of the 4 streams [192 x 64]
+          const uint32_t ra = smem_u32(LEAN ? sm + kOffIn + si * kInStageF : sm + kOffOut + o * kOutStage);
+          const uint32_t fb = smem_u32(sm + kOffFn + f * kFnStage);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             tc_mma_bf16(tmem + kColD, sdesc_k_sw128(ra + kk * 32), sdesc_k_sw128(fb + kk * 32), kIdesc, (c | kk) != 0);
           tc_commit(&tl->fn_empty[f]);
-          tc_commit(&tl->out_empty[o]);
+          tc_commit(LEAN ? &tl->in_empty[si] : &tl->out_empty[o]);
           if (c == ni - 1) tc_commit(&tl->d_full);
           ++jr;
         }
@@ -742,10 +765,11 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
         // normalise-only passes after this item (of this item when the next
         // covers other columns or there is none; of every unit after the
         // last): one stage per group of chunks, no MMA
-        const int qa = full ? -1 : 0, qb = full ? (nblk < 0 || iunit(i + 1) >= 0 ? 0 : -1) : (nblk < 0 ? nu : 0);
+        // (LEAN: the MMAs never hold an output stage)
+        const int qa = full ? -1 : 0, qb = LEAN ? -1 : full ? (nblk < 0 || iunit(i + 1) >= 0 ? 0 : -1) : (nblk < 0 ? nu : 0);
         for (int q = qa; q < qb && ok; ++q) {
           const int nq = !SPLIT || q < 0 ? nch : const_cast<const Item&>(tl->ulist[q]).ng;
-          for (int c0 = 0; c0 < nq; c0 += norm_group<OUT>(), ++j) {
+          for (int c0 = 0; c0 < nq; c0 += G::kNormGroup, ++j) {
             if (!(ok = wait_local(X, &tl->out_full[j % kNO], (j / kNO) & 1))) break;
             mbar_arrive(&tl->out_empty[j % kNO]);
           }
@@ -785,16 +809,17 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
       }
     };
     // (lane 0) a stage is given back once the bulk stores issued from it have
-    // read it.  With the fp8_grid output the newest group may still be
-    // reading: its stage is given back after the next group is committed (the
-    // compute warps need it only kNO - 1 stages later), so the store warp
-    // never waits on its own stores; measured: 396 to 386 us at T = 16384
-    // there, but 3 to 4 us slower for the bf16 forms, whose stages turn over
-    // faster.
+    // read it.  With the fp8_grid output, and in the identity form whose
+    // stages hold only the norm tile, the newest group may still be reading:
+    // its stage is given back after the next group is committed (the compute
+    // warps need it only kNO - 1 stages later), so the store warp never waits
+    // on its own stores; measured: fp8_grid at T = 16384 396 to 386 us, the
+    // identity form 193 to 191 us, but 3 to 4 us slower for the bf16 post and
+    // no_post forms, whose stages turn over faster.
     int pend = -1;
     auto retire = [&](int o) {
       tma_store_commit();
-      if (OUT == 2) {
+      if (OUT == 2 || LEAN) {
         tma_store_wait_read_1();  // every group but the newest has read its stage
         if (pend >= 0) mbar_arrive(&tl->out_empty[pend]);
         pend = o;
@@ -838,7 +863,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
       const int nblk = iblock(i + 1);
       // normalise-only passes: the norm tiles of a group of chunks per stage
       const int qa = full ? -1 : 0, qb = full ? (nblk < 0 || iunit(i + 1) >= 0 ? 0 : -1) : (nblk < 0 ? nu : 0);
-      constexpr int NG = norm_group<OUT>();
+      constexpr int NG = G::kNormGroup;
       for (int q = qa; q < qb && ok; ++q) {
         const Item u = !SPLIT || q < 0 ? item(i) : const_cast<const Item&>(tl->ulist[q]);
         const int tq = u.block * kBM, gq = u.g0, nq = nchi(u);
@@ -849,7 +874,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
           const int ng = min(NG, nq - c0);
           if (OUT == 1) {  // codes tiles in stage slot 4
             for (int g = 0; g < ng; ++g)
-              quant_tile(ost + g * kRTile, ost + kOffNormT + g * 2048, tq, ((gq + c0 + g) * kCl + (int)rank) * kChunk);
+              quant_tile(ost + g * kRTile, ost + kPassCodes + g * 2048, tq, ((gq + c0 + g) * kCl + (int)rank) * kChunk);
             fence_proxy_async_smem();
             __syncwarp();
           }
@@ -857,7 +882,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
             for (int g = 0; g < ng; ++g) {
               const int h = ((gq + c0 + g) * kCl + (int)rank) * kChunk;
               if (store_norm) tma_store_2d(&tmN, ost + g * kRTile, h, tq);
-              if (OUT == 1) tma_store_2d(&tmC, ost + kOffNormT + g * 2048, h, tq);
+              if (OUT == 1) tma_store_2d(&tmC, ost + kPassCodes + g * 2048, h, tq);
             }
             retire(o);
           }
@@ -913,7 +938,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
       const int nblk = iblock(i + 1);
       // normalise-only passes: the norm tiles of a group of chunks per stage
       const int qa = full ? -1 : 0, qb = full ? (nblk < 0 || iunit(i + 1) >= 0 ? 0 : -1) : (nblk < 0 ? nu : 0);
-      constexpr int NG = norm_group<OUT>();
+      constexpr int NG = G::kNormGroup;
       for (int q = qa; q < qb && ok; ++q) {
         const Item u = !SPLIT || q < 0 ? item(i) : const_cast<const Item&>(tl->ulist[q]);
         const int64_t tq = (int64_t)u.block * kBM;
@@ -1214,9 +1239,11 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
         if (fused && c == 0 && !(ok = take_rstd(i - 1, prevblk))) break;
         if (!(ok = wait_warp(X, &tl->out_empty[o], ((j / kNO) & 1) ^ 1))) break;
         uint8_t* ost = sm + kOffOut + o * kOutStage;
+        if (!LEAN) {  // (LEAN: the MMAs read R' = R from the input stage)
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          *reinterpret_cast<uint4*>(ost + q * kRTile + off) = make_uint4(ow[q][0], ow[q][1], ow[q][2], ow[q][3]);
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(ost + q * kRTile + off) = make_uint4(ow[q][0], ow[q][1], ow[q][2], ow[q][3]);
+        }
         if (fused) {  // norm of the previous item's x in these columns, before x is overwritten
           float xv[8], gm[8];
           tc_wait_ld_x8(xr);
@@ -1305,7 +1332,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
       // chunks per output stage (a whole block followed by a unit or by
       // nothing; after the last item, every unit once its block is complete)
       const int qa = full ? -1 : 0, qb = full ? (nblk < 0 || iunit(i + 1) >= 0 ? 0 : -1) : (nblk < 0 ? nu : 0);
-      constexpr int NG = norm_group<OUT>();
+      constexpr int NG = G::kNormGroup;
       int sq = 0;  // first tensor-memory slot of the pass's x
       for (int q = qa; q < qb && ok; ++q) {
         const Item u = !SPLIT || q < 0 ? item(i) : const_cast<const Item&>(tl->ulist[q]);
