@@ -195,14 +195,20 @@ cudaError_t stream_launch(const SeamArgs& a, bool tcgen05_proj, int kcl, cudaStr
     if (hit) return launch_with_maps(a, c.m, tcgen05_proj, kcl, stream, report_ns, launches, wsx, wave_split);
   }
   CUtensorMap mR, mY, mRo, mFn, mN, mC;
-  const cuuint64_t d3[3] = {(cuuint64_t)H, 4, T};
-  const cuuint64_t s3[2] = {(cuuint64_t)H * 2, (cuuint64_t)H * 8};
-  const cuuint32_t b3[3] = {kChunk, 1, kBM};
+  // R and R' [T, 4, H] as (column, token, stream) and the packed fn
+  // [48, 4H] as (column, row, stream): one box carries the four streams'
+  // tiles of a chunk, laid out in shared memory stream by stream (rows
+  // stream * 32 + token, each tile on an 8-row swizzle boundary), so a chunk
+  // is one copy each instead of four (the SM's TMA issue rate bounds the
+  // chunk rate at small T)
+  const cuuint64_t d3[3] = {(cuuint64_t)H, T, 4};
+  const cuuint64_t s3[2] = {(cuuint64_t)H * 8, (cuuint64_t)H * 2};
+  const cuuint32_t b3[3] = {kChunk, kBM, 4};
   const cuuint64_t d2[2] = {(cuuint64_t)H, T};
   const cuuint64_t s2[1] = {(cuuint64_t)H * 2};
   const cuuint32_t b2[2] = {kChunk, kBM};
-  const cuuint64_t dF[3] = {(cuuint64_t)H, 4, kFnRows};
-  const cuuint32_t bF[3] = {kChunk, 1, kFnRows};
+  const cuuint64_t dF[3] = {(cuuint64_t)H, kFnRows, 4};
+  const cuuint32_t bF[3] = {kChunk, kFnRows, 4};
   const cuuint64_t sC[1] = {(cuuint64_t)H};
   bool ok = encode(&mR, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.R, d3, s3, b3, CU_TENSOR_MAP_SWIZZLE_128B) &&
             encode(&mRo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.res_out ? (const void*)a.res_out : (const void*)a.R, d3, s3,

@@ -683,8 +683,8 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
             uint8_t* st = sm + kOffIn + s * kInStageF;
             const int h = ((gb + c) * kCl + (int)rank) * kChunk;
             mbar_arrive_expect_tx(&tl->in_full[s], bytes);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) tma_load_3d(st + q * kRTile, &tmR, &tl->in_full[s], h, q, t0, pol);
+            // the four streams' tiles in one copy: box [64 columns, 32 tokens, 4 streams]
+            tma_load_3d(st, &tmR, &tl->in_full[s], h, t0, 0, pol);
             if (POST) tma_load_2d(st + 4 * kRTile, &tmY, &tl->in_full[s], h, t0, pol);
             ++j;
           }
@@ -719,8 +719,8 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
           uint8_t* st = sm + kOffFn + f * kFnStage;
           const int h = ((gb + c) * kCl + (int)rank) * kChunk;
           mbar_arrive_expect_tx(&tl->fn_full[f], kFnStage);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) tma_load_3d(st + q * kFnTile, &tmFn, &tl->fn_full[f], h, q, 0, pol);
+          // the four streams' fn tiles in one copy: box [64 columns, 48 rows, 4 streams]
+          tma_load_3d(st, &tmFn, &tl->fn_full[f], h, 0, 0, pol);
         }
         if (ok) release(i);
       }
@@ -846,8 +846,7 @@ __global__ void __launch_bounds__(threads_of<OUT>(), 1)
         }
         if (lane == 0) {
           if (!IDENT) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) tma_store_3d(&tmRo, ost + q * kRTile, h, q, t0);
+            tma_store_3d(&tmRo, ost, h, t0, 0);  // the four R' tiles in one copy
           }
           if (fused) {
             if (store_norm) tma_store_2d(&tmN, ost + kOffNormT, h, tp);
