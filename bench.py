@@ -76,12 +76,12 @@ L2_BYTES = 126 * 1024 * 1024
 NCU_TRAFFIC = {
     # profiles/stream_seam_kernel_T16384_H5120_post_bf16_launches.md and
     # profiles/stream_seam_kernel_configs_dram.md (1-pass captures)
-    ("acc227870f036cac", "seam_T16384_H5120_post_bf16"): 842.55e6 + 787.42e6,
-    ("acc227870f036cac", "seam_T16384_H5120_nopost_bf16"): 674.47e6 + 783.87e6,
-    ("acc227870f036cac", "seam_T4160_H5120_post_bf16"): 215.51e6 + 161.93e6,
-    ("acc227870f036cac", "seam_T16384_H5120_post_fp8grid"): 842.58e6 + 953.17e6,
-    ("acc227870f036cac", "seam_T16384_H5120_first_bf16"): 673.40e6 + 142.65e6,
-    ("acc227870f036cac", "seam_T1024_H5120_post_mxfp8"): 54.58e6 + 8.76e6,
+    ("4fe4db54128e4d36", "seam_T16384_H5120_post_bf16"): 842.50e6 + 787.52e6,
+    ("4fe4db54128e4d36", "seam_T16384_H5120_nopost_bf16"): 674.47e6 + 783.95e6,
+    ("4fe4db54128e4d36", "seam_T4160_H5120_post_bf16"): 215.45e6 + 161.85e6,
+    ("4fe4db54128e4d36", "seam_T16384_H5120_post_fp8grid"): 842.59e6 + 952.74e6,
+    ("4fe4db54128e4d36", "seam_T16384_H5120_first_bf16"): 673.53e6 + 141.37e6,
+    ("4fe4db54128e4d36", "seam_T1024_H5120_post_mxfp8"): 54.59e6 + 8.67e6,
 }
 
 
