@@ -537,6 +537,21 @@ def test_identity_form(T, H, path, mode):
     compare(d, h)
 
 
+@pytest.mark.parametrize("mode", [B.MHC_OUT_BF16, B.MHC_OUT_MXFP8])
+def test_identity_form_warp_mma_projection(mode):
+    # with the tcgen05 projection the identity form's MMAs read R from the
+    # input stage (its own shared-memory layout); with the warp-level
+    # projection the compute warps still copy R into the output stage: both
+    # layouts at the same width
+    T, H = 300, 5120
+    d = make_case(T, H, 8650, ident=True, mxfp8=mode == B.MHC_OUT_MXFP8)
+    for proj in (1, 2):
+        cfg = B.MhcConfig(path=2, projection=proj)
+        out = B.alloc_outputs(T, H, d["out_mode"], "cuda", cfg)
+        out["residual_out"] = None
+        compare(d, to_host(run_gpu(d, cfg=cfg, out=out)))
+
+
 def test_identity_form_matches_identity_comb_and_rejects_y():
     # away from signed zeros (none in these draws) the identity form equals the
     # no_post seam with comb = I on the same inputs
