@@ -97,8 +97,10 @@ typedef struct {
                             bit 0).  Streaming paths: a wait past it is reported (status
                             bit 1) and goes on; a wait one second past it abandons the call
                             (the kernel stops issuing work, waits for its copies and MMAs in
-                            flight, frees tensor memory and returns).  Either way
-                            mhc_check_status() then returns MHC_ERR_TIMEOUT */
+                            flight, frees tensor memory and returns; the workspace's
+                            counters may then be left set: run mhc_workspace_init() on it
+                            before its next call).  Either way mhc_check_status() then
+                            returns MHC_ERR_TIMEOUT */
     int projection;      /* streaming path's gate projection: 0 = policy (2 when H <= 5120, else 1);
                             1 = warp-level tensor-core MMA (m16n8k16) in the compute warps;
                             2 = tcgen05 MMA issued by one thread into tensor memory (H <= 5120) */
@@ -118,9 +120,9 @@ typedef struct {
  * `cfg` (NULL = defaults): a status word plus, on the split path, the
  * per-CTA partial sums and the arrival counters of every token group, and on
  * the streaming paths the partial sums and counters of the split last round
- * and the item scheduler's ticket counter (776 KiB + 128 bytes).  Where the policy's path depends on whether fn_packed is given,
- * the size covers both.  One
- * workspace per stream whose calls can overlap on the GPU; it needs
+ * and the item scheduler's ticket counter (776 KiB + 128 bytes).  Where the
+ * policy's path depends on whether fn_packed is given, the size covers both.
+ * One workspace per stream whose calls can overlap on the GPU; it needs
  * mhc_workspace_init() once, after which the counters reset themselves and any
  * call (T' <= T, same H and cfg) may follow any other. */
 size_t mhc_workspace_bytes(int64_t T, int H, const mhc_config* cfg);
